@@ -1,0 +1,394 @@
+"""Benchmark of the fused MoE layer on GB300 (one JSON line on rank 0).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--config large] [--impl ours|reference]
+
+One step = one pass of the whole layer (route -> dispatch -> expert FFN ->
+combine) over one batch of synthetic tokens, inputs resident in HBM.  The
+default workload is the large prefill layer (T=32768, d=7168, E=256, k=8,
+ffn=2048), the largest configuration that fits one GPU; every input is larger
+than L2 (22.5 GB of expert weights, 470 MB of tokens), so no L2 flush is
+needed between steps.  Smaller configurations (--config) flush L2 between
+steps when their inputs fit in it.
+
+Multi-GPU (torchrun): every rank runs an independent replica of the layer on
+its own token batch (weak scaling, no data-path collective); the timed region
+is bracketed by barriers and the slowest rank's time is reported.
+
+--impl reference times the CPU oracle (the plain, slow restatement of the
+layer) on a bounded token sample of the same workload, on the host cores.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+import torch
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from dispatch_ffn_combine_gb300.workloads import CONFIGS, bf16_bits, make_inputs  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def load_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        with open(path) as fh:
+            p = json.load(fh)
+        p["source"] = "measured"
+        return p
+    p = dict(FALLBACK_PEAKS)
+    p["source"] = "fallback"
+    return p
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
+            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
+            self.fh = open(self.path, "w")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.2)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        self.fh.close()
+        sm, smax, power, reasons = [], [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        with open(self.path) as fh:
+            for ln in fh:
+                parts = [p.strip() for p in ln.split(",")]
+                if len(parts) < 9:
+                    continue
+                try:
+                    sm.append(float(parts[1]))
+                    smax.append(float(parts[2]))
+                    power.append(float(parts[3]))
+                except ValueError:
+                    continue
+                for nm, v in zip(names, parts[5:9]):
+                    if v.lower() == "active":
+                        reasons.add(nm)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
+                "samples": len(sm), "power_w_max": max(power)}
+
+
+def flops_bytes(cfg, offsets):
+    """Algorithmic work per layer call and per phase."""
+    T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
+    S = T * k
+    counts = np.diff(offsets)
+    touched = int(np.count_nonzero(counts))
+    w13 = 2 * touched * f * d * 2
+    w2 = touched * d * f * 2
+    return {
+        "gemm1": {"flops": 4 * S * d * f, "bytes": w13 + S * d * 2 + S * f * 2},
+        "gemm2": {"flops": 2 * S * d * f, "bytes": w2 + S * f * 2 + S * d * 2},
+        "combine": {"flops": 0, "bytes": S * d * 2 + T * d * 2},
+        "scatter": {"flops": 0, "bytes": T * d * 2 + S * d * 2},
+        "route_logits": {"flops": 2 * T * d * E, "bytes": T * d * 2 + E * d * 4 + T * E * 4},
+        "layer": {"flops": 6 * S * d * f, "bytes": w13 + w2 + 2 * T * d * 2 + E * d * 4},
+        "touched_experts": touched,
+    }
+
+
+def traffic_record(kernel: str, cfg_name: str):
+    """DRAM bytes per launch from a committed ncu summary, only while the kernel
+    source is unchanged since the counters were taken (else None)."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as fh:
+        rec = json.load(fh).get(kernel, {}).get(cfg_name)
+    if not rec:
+        return None
+    src = os.path.join(ROOT, "dispatch_ffn_combine_gb300", "csrc", rec["source"])
+    with open(src, "rb") as fh:
+        if hashlib.sha256(fh.read()).hexdigest()[:16] != rec["sha256_16"]:
+            return None
+    return rec["dram_bytes_per_launch"]
+
+
+def cpu_baseline(cfg, inp_host, budget_s: float, seed: int = 0):
+    """Oracle (fp64 FFN, fp32 canonical router) on a token sample, host cores."""
+    import oracle
+
+    xb = bf16_bits(inp_host["x"])
+    args = (xb, inp_host["wg"].numpy(), None if inp_host["bias"] is None else inp_host["bias"].numpy(),
+            bf16_bits(inp_host["w1"]), bf16_bits(inp_host["w3"]), bf16_bits(inp_host["w2"]), cfg.k)
+    cores = oracle.num_threads()
+    rs = np.random.RandomState(seed)
+    # calibrate on one token per core, then size the sample to the budget
+    n0 = min(cfg.T, cores)
+    t0 = time.perf_counter()
+    oracle.layer(*args, tokens=rs.choice(cfg.T, n0, replace=False))
+    dt0 = time.perf_counter() - t0
+    n = int(min(cfg.T, max(n0, n0 * budget_s / max(dt0, 1e-6))))
+    n = max(cores, (n // cores) * cores) if n >= cores else n
+    toks = rs.choice(cfg.T, n, replace=False)
+    t0 = time.perf_counter()
+    oracle.layer(*args, tokens=toks)
+    dt = time.perf_counter() - t0
+    return n / dt, n, dt, cores
+
+
+def run_reference(args):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    cfg = CONFIGS[args.config]
+    inp = make_inputs(cfg, seed=0, device="cuda" if torch.cuda.is_available() else "cpu")
+    inp = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
+    per_step_s = max(2.0, 150.0 / max(args.steps + args.warmup, 1))
+    vals, total_tok, total_t, cores, n = [], 0, 0.0, 1, 0
+    for i in range(args.warmup + args.steps):
+        tps, n, dt, cores = cpu_baseline(cfg, inp, per_step_s, seed=i)
+        if i >= args.warmup:
+            vals.append(tps)
+            total_tok += n
+            total_t += dt
+    value = total_tok / total_t
+    line = {
+        "impl": "reference", "metric": "MoE layer tokens/s (TFLOP/s beside it)", "value": value,
+        "unit": "tokens/s", "n_gpus": args.gpus, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": 1e3 * total_t / max(args.steps, 1), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": cfg.describe(), "sample_tokens_per_step": n},
+        "tflops": value * 6 * cfg.k * cfg.d * cfg.f / 1e12,
+        "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+                         "sample": f"{n} random tokens of the workload per step (route + k expert FFNs + "
+                                   f"combine, fp64), {args.steps} timed steps"},
+        "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import dispatch_ffn_combine_gb300 as mk
+
+    world, rank, local = dist_env()
+    dist = world > 1
+    if dist:
+        import torch.distributed as tdist
+        torch.cuda.set_device(local)
+        tdist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    cfg = CONFIGS[args.config]
+    peaks = load_peaks()
+
+    # Weights are shared (seed 0); each rank draws its own token batch.
+    inp = make_inputs(cfg, seed=0, device=dev)
+    if rank:
+        inp["x"] = make_inputs(cfg, seed=1000 + rank, device=dev, experts=False)["x"]
+    x, wg, bias, w1, w3, w2 = (inp[k] for k in ("x", "wg", "bias", "w1", "w3", "w2"))
+    ws = mk.alloc_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, dev)
+    y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+    stream = torch.cuda.current_stream()
+
+    input_bytes = sum(t.numel() * t.element_size() for t in (x, wg, w1, w3, w2))
+    flush = input_bytes < 2 * L2_BYTES
+    scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
+
+    nph = len(mk.PHASES)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
+    for row in ev:  # materialise the event handles before passing them to the library
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    def step(i=None):
+        mk.mk_moe_layer(x, wg, bias, w1, w3, w2, cfg.k, y=y, ws=ws,
+                        phase_events=None if i is None else ev[i], stream=stream)
+
+    for _ in range(args.warmup):
+        step()
+        if flush:
+            scrub.random_()
+    st, site = mk.mk_moe_last_device_error(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"device error during warm-up: {mk.status_string(st)} site {site:#x}")
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    if dist:
+        tdist.barrier()
+    torch.cuda.synchronize()
+    if flush:
+        total_ms = 0.0
+        for i in range(args.steps):
+            scrub.random_()
+            step(i)
+        torch.cuda.synchronize()
+        total_ms = sum(ev[i][0].elapsed_time(ev[i][nph]) for i in range(args.steps))
+    else:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(args.steps):
+            step(i)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t_start.elapsed_time(t_end)
+    if dist:
+        tdist.barrier()
+    clk = clocks.stop()
+    st, site = mk.mk_moe_last_device_error(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"device error in the timed region: {mk.status_string(st)} site {site:#x}")
+
+    phase_ms = {}
+    for p, name in enumerate(mk.PHASES):
+        phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(args.steps)) / args.steps
+
+    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
+    if dist:
+        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    total_ms = float(t.item())
+    ms_per_step = total_ms / args.steps
+    value = world * cfg.T / (ms_per_step / 1e3)
+
+    # ---- end to end through the host-buffer entry point (pinned host x in, y out)
+    x_host = x.cpu().pin_memory()
+    y_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
+    for _ in range(max(1, args.warmup)):
+        mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream)
+    torch.cuda.synchronize()
+    if dist:
+        tdist.barrier()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    if dist:
+        tdist.all_reduce(te, op=tdist.ReduceOp.MAX)
+        tdist.barrier()
+    e2e_value = world * cfg.T / (float(te.item()) / args.steps / 1e3)
+
+    if rank != 0:
+        if dist:
+            tdist.destroy_process_group()
+        return
+
+    # ---- roofline of the dominant kernel
+    _, _, offsets, _ = mk.mk_moe_layer_routing(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
+    fb = flops_bytes(cfg, offsets.cpu().numpy())
+    dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
+    dom_ms = phase_ms[dom]
+    work = fb[dom]
+    ai = work["flops"] / max(work["bytes"], 1)
+    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    if work["flops"] and ai >= ridge:
+        achieved = work["flops"] / (dom_ms / 1e3) / 1e12
+        roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
+                "frac": achieved / tensor_peak}
+    else:
+        achieved = work["bytes"] / (dom_ms / 1e3) / 1e9
+        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                "frac": achieved / peaks["hbm_gbs"]}
+    roof.update({"kernel": dom, "kernel_ms": dom_ms, "peak_source": peaks["source"] +
+                 (" (bf16 sustained)" if roof["bound"] == "tensor" else " (HBM copy)"),
+                 "traffic": traffic_record(dom, args.config)})
+
+    # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
+    cpu = None
+    if world == 1 and not args.no_cpu_baseline:
+        host = {k: (v.cpu() if v is not None else None) for k, v in inp.items()}
+        tps, n, dt, cores = cpu_baseline(cfg, host, args.cpu_budget)
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": f"{n} random tokens of the workload (route + k expert FFNs + combine in fp64), "
+                         f"{dt:.1f} s"}
+
+    layer_tflops = fb["layer"]["flops"] / (ms_per_step / 1e3) / 1e12 * world
+    line = {
+        "metric": "MoE layer tokens/s (TFLOP/s beside it)", "value": value, "unit": "tokens/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": cfg.describe(), "tokens_per_gpu": cfg.T,
+                   "l2": "flushed between steps" if flush else "inputs larger than L2 (no flush)",
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU"},
+        "tflops": layer_tflops,
+        "tflops_frac_of_measured_bf16": layer_tflops / world / peaks["bf16_tflops"],
+        "phase_ms": phase_ms,
+        "roofline": roof,
+        "cpu_baseline": cpu,
+        "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
+                "d2h_bytes_per_step": cfg.T * cfg.d * 2},
+        "gpu_launches": len(mk.PHASES) * args.steps,
+        "clocks": clk,
+        "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},
+    }
+    print(json.dumps(line), flush=True)
+    if dist:
+        tdist.destroy_process_group()
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--config", default="large", choices=sorted(CONFIGS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3 and args.impl == "ours":
+        print("note: fewer than 3 warm-up steps", file=sys.stderr)
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,364 @@
+// api.cu -- the C ABI (include/mkmoe.h): argument checks, workspace layout,
+// and the launch sequence of the layer's steps on the caller's stream.
+#include <algorithm>
+#include <mutex>
+
+#include "mk_internal.h"
+
+namespace mk {
+
+namespace {
+constexpr size_t kAlign = 256;
+size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
+}  // namespace
+
+WsLayout ws_layout(int64_t T, int d, int E, int k, int f) {
+    WsLayout L;
+    const size_t S = static_cast<size_t>(T) * k;
+    const size_t nch = static_cast<size_t>(num_chunks(T));
+    size_t o = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = o;
+        o = align_up(o + bytes);
+        return at;
+    };
+    L.ctrl = take(256);
+    L.logits = take(static_cast<size_t>(T) * E * 4);
+    L.ids = take(S * 4);
+    L.w = take(S * 4);
+    L.chunk_counts = take(nch * E * 4);
+    L.chunk_base = take(nch * E * 4);
+    L.rank = take(S * 4);
+    L.counts = take(static_cast<size_t>(E) * 4);
+    L.offsets = take((static_cast<size_t>(E) + 1) * 4);
+    L.mtile_start = take((static_cast<size_t>(E) + 1) * 4);
+    L.row_token = take(S * 4);
+    L.row_weight = take(S * 4);
+    L.slot_row = take(S * 4);
+    L.x_perm = take(S * d * 2);
+    L.h = take(S * f * 2);
+    L.P = take(S * d * 2);
+    L.x_stage = take(static_cast<size_t>(T) * d * 2);
+    L.y_stage = take(static_cast<size_t>(T) * d * 2);
+    L.total = o;
+    return L;
+}
+
+int device_sm_count() {
+    static int cache[64] = {0};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (dev >= 64) {
+        int n = 1;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n;
+    }
+    if (cache[dev] == 0) {
+        int n = 1;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        cache[dev] = n;
+    }
+    return cache[dev];
+}
+
+bool device_is_sm103() {
+    int dev = 0, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess) return false;
+    if (cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) return false;
+    return major == 10 && minor == 3;
+}
+
+}  // namespace mk
+
+using namespace mk;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+mk_status check_sizes(int64_t T, int d, int E, int k, int f_or_64) {
+    if (T < 0 || d <= 0 || E <= 0 || k <= 0 || f_or_64 <= 0) return MK_ERR_INVALID_ARG;
+    if (E > kMaxExperts || k > kMaxTopK || k > E) return MK_ERR_INVALID_ARG;
+    if (d % 64 != 0 || f_or_64 % 64 != 0) return MK_ERR_INVALID_ARG;
+    if (T * k >= (int64_t(1) << 31)) return MK_ERR_UNSUPPORTED;
+    if (T * static_cast<int64_t>(d) >= (int64_t(1) << 31)) return MK_ERR_UNSUPPORTED;
+    if (T * k * static_cast<int64_t>(std::max(d, f_or_64)) >= (int64_t(1) << 40)) return MK_ERR_UNSUPPORTED;
+    if (static_cast<int64_t>(E) * std::max(d, f_or_64) >= (int64_t(1) << 31)) return MK_ERR_UNSUPPORTED;
+    return MK_OK;
+}
+
+mk_status check_ws(const void* ws, size_t ws_bytes, const WsLayout& L) {
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < L.total) return MK_ERR_WORKSPACE;
+    return MK_OK;
+}
+
+mk_status device_ok() { return device_is_sm103() ? MK_OK : MK_ERR_UNSUPPORTED; }
+
+template <typename Tp>
+Tp* at(void* ws, size_t off) {
+    return reinterpret_cast<Tp*>(static_cast<uint8_t*>(ws) + off);
+}
+
+#define MK_TRY(expr)                                 \
+    do {                                             \
+        const cudaError_t _e = (expr);               \
+        if (_e != cudaSuccess) return MK_ERR_CUDA;   \
+    } while (0)
+
+struct PhaseMarks {
+    void** ev;
+    cudaStream_t s;
+    cudaError_t mark(int i) const {
+        if (ev == nullptr || ev[i] == nullptr) return cudaSuccess;
+        return cudaEventRecord(static_cast<cudaEvent_t>(ev[i]), s);
+    }
+};
+
+}  // namespace
+
+extern "C" {
+
+size_t mk_moe_workspace_size(int64_t T, int d, int E, int k, int ffn) {
+    if (check_sizes(T, d, E, k, ffn) != MK_OK) return 0;
+    return ws_layout(T, d, E, k, ffn).total;
+}
+
+const char* mk_moe_status_string(mk_status s) {
+    switch (s) {
+        case MK_OK: return "MK_OK";
+        case MK_ERR_INVALID_ARG: return "MK_ERR_INVALID_ARG: invalid size, pointer or alignment";
+        case MK_ERR_WORKSPACE: return "MK_ERR_WORKSPACE: workspace missing, misaligned or too small";
+        case MK_ERR_UNSUPPORTED: return "MK_ERR_UNSUPPORTED: outside this build's limits or not an sm_103 device";
+        case MK_ERR_CUDA: return "MK_ERR_CUDA: a CUDA call or kernel launch failed";
+        case MK_ERR_TIMEOUT: return "MK_ERR_TIMEOUT: a bounded device-side wait ran out";
+        case MK_ERR_BOUNDS: return "MK_ERR_BOUNDS: routing index out of range or repeated";
+    }
+    return "unknown mk_status";
+}
+
+mk_status mk_moe_route(const void* x, const float* wg, const float* bias, int64_t T, int d, int E, int k,
+                       int32_t* topk_ids, float* topk_w, int32_t* expert_counts, void* ws, size_t ws_bytes,
+                       void* stream) {
+    mk_status st = check_sizes(T, d, E, k, 64);
+    if (st != MK_OK) return st;
+    if (!x || !wg || !topk_ids || !topk_w) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wg)) return MK_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, 64);
+    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
+    if (T == 0) {
+        if (expert_counts) MK_TRY(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, (cudaStream_t)stream));
+        return MK_OK;
+    }
+    if ((st = device_ok()) != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    MK_TRY(cudaMemsetAsync(at<uint8_t>(ws, L.ctrl), 0, 8, s));
+    float* logits = at<float>(ws, L.logits);
+    MK_TRY(launch_route_logits(static_cast<const bf16*>(x), wg, bias, T, d, E, logits, s));
+    if (expert_counts) MK_TRY(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s));
+    MK_TRY(launch_topk(logits, T, E, k, topk_ids, topk_w, expert_counts, s));
+    return MK_OK;
+}
+
+mk_status mk_moe_dispatch(const void* x, const int32_t* topk_ids, const float* topk_w, int64_t T, int d, int E, int k,
+                          int32_t* expert_offsets, int32_t* row_token, float* row_weight, int32_t* slot_row,
+                          void* x_perm, void* ws, size_t ws_bytes, void* stream) {
+    mk_status st = check_sizes(T, d, E, k, 64);
+    if (st != MK_OK) return st;
+    if (!x || !topk_ids || !expert_offsets || !row_token || !slot_row || !x_perm) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(x_perm)) return MK_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, 64);
+    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {
+        MK_TRY(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s));
+        return MK_OK;
+    }
+    if ((st = device_ok()) != MK_OK) return st;
+    uint32_t* status = at<uint32_t>(ws, L.ctrl);
+    MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    int32_t* chunk_counts = at<int32_t>(ws, L.chunk_counts);
+    int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
+    int32_t* rank = at<int32_t>(ws, L.rank);
+    MK_TRY(launch_count(topk_ids, T, E, k, chunk_counts, rank, status, s));
+    MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), expert_offsets,
+                       at<int32_t>(ws, L.mtile_start), s));
+    MK_TRY(launch_scatter(static_cast<const bf16*>(x), topk_ids, topk_w, T, d, E, k, expert_offsets, chunk_base, rank,
+                          static_cast<bf16*>(x_perm), row_token, row_weight, slot_row, s));
+    return MK_OK;
+}
+
+mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, const float* row_weight, const void* w1,
+                            const void* w3, const void* w2, int64_t S, int d, int E, int ffn, void* h, void* P,
+                            void* ws, size_t ws_bytes, void* stream) {
+    mk_status st = check_sizes(S, d, E, 1, ffn);
+    if (st != MK_OK) return st;
+    if (!x_perm || !expert_offsets || !w1 || !w3 || !w2 || !h || !P) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(h) || !aligned16(P))
+        return MK_ERR_INVALID_ARG;
+    // Needs only the control block and the tile table that follows it.
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256 + 4 * (size_t(E) + 1))
+        return MK_ERR_WORKSPACE;
+    if (S == 0) return MK_OK;
+    if ((st = device_ok()) != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* status = at<uint32_t>(ws, 0);
+    int32_t* mtile = at<int32_t>(ws, 256);
+    MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    MK_TRY(launch_mtile_table(expert_offsets, E, S, mtile, status, s));
+    FfnArgs a;
+    a.x_perm = static_cast<const bf16*>(x_perm);
+    a.offsets = expert_offsets;
+    a.mtile_start = mtile;
+    a.row_weight = row_weight;
+    a.w1 = static_cast<const bf16*>(w1);
+    a.w3 = static_cast<const bf16*>(w3);
+    a.w2 = static_cast<const bf16*>(w2);
+    a.S = S;
+    a.d = d;
+    a.E = E;
+    a.f = ffn;
+    a.h = static_cast<bf16*>(h);
+    a.P = static_cast<bf16*>(P);
+    a.status = status;
+    a.timeout_ns = kDefaultTimeoutNs;
+    a.inject = 0;
+    MK_TRY(launch_gemm1(a, s));
+    MK_TRY(launch_gemm2(a, s));
+    return MK_OK;
+}
+
+mk_status mk_moe_combine(const void* P, const int32_t* slot_row, int64_t T, int d, int k, void* y, void* stream) {
+    mk_status st = check_sizes(T, d, k, k, 64);
+    if (st != MK_OK) return st;
+    if (!P || !slot_row || !y) return MK_ERR_INVALID_ARG;
+    if (!aligned16(P) || !aligned16(y)) return MK_ERR_INVALID_ARG;
+    if (T == 0) return MK_OK;
+    if ((st = device_ok()) != MK_OK) return st;
+    MK_TRY(launch_combine(static_cast<const bf16*>(P), slot_row, T, d, k, static_cast<bf16*>(y),
+                          static_cast<cudaStream_t>(stream)));
+    return MK_OK;
+}
+
+mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const void* w1, const void* w3,
+                       const void* w2, int64_t T, int d, int E, int k, int ffn, void* y, void* ws, size_t ws_bytes,
+                       const mk_moe_opts* opts, void* stream) {
+    mk_status st = check_sizes(T, d, E, k, ffn);
+    if (st != MK_OK) return st;
+    if (!x || !wg || !w1 || !w3 || !w2 || !y) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wg) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(y))
+        return MK_ERR_INVALID_ARG;
+    if (opts != nullptr) {
+        for (int r : opts->reserved)
+            if (r != 0) return MK_ERR_INVALID_ARG;
+        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1) return MK_ERR_INVALID_ARG;
+    }
+    const WsLayout L = ws_layout(T, d, E, k, ffn);
+    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
+    if (T == 0) return MK_OK;
+    if ((st = device_ok()) != MK_OK) return st;
+
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const PhaseMarks pm{opts ? opts->phase_events : nullptr, s};
+    uint32_t* status = at<uint32_t>(ws, L.ctrl);
+    int32_t* ids = at<int32_t>(ws, L.ids);
+    float* w = at<float>(ws, L.w);
+    float* logits = at<float>(ws, L.logits);
+    int32_t* chunk_counts = at<int32_t>(ws, L.chunk_counts);
+    int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
+    int32_t* rank = at<int32_t>(ws, L.rank);
+    int32_t* offsets = at<int32_t>(ws, L.offsets);
+    int32_t* mtile = at<int32_t>(ws, L.mtile_start);
+    int32_t* slot_row = at<int32_t>(ws, L.slot_row);
+    float* row_weight = at<float>(ws, L.row_weight);
+    bf16* x_perm = at<bf16>(ws, L.x_perm);
+
+    MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    MK_TRY(pm.mark(MK_PHASE_ROUTE_LOGITS));
+    MK_TRY(launch_route_logits(static_cast<const bf16*>(x), wg, bias, T, d, E, logits, s));
+    MK_TRY(pm.mark(MK_PHASE_TOPK));
+    MK_TRY(launch_topk(logits, T, E, k, ids, w, nullptr, s));
+    MK_TRY(pm.mark(MK_PHASE_COUNT));
+    MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s));
+    MK_TRY(pm.mark(MK_PHASE_SCAN));
+    MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile, s));
+    MK_TRY(pm.mark(MK_PHASE_SCATTER));
+    MK_TRY(launch_scatter(static_cast<const bf16*>(x), ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm,
+                          at<int32_t>(ws, L.row_token), row_weight, slot_row, s));
+    FfnArgs a;
+    a.x_perm = x_perm;
+    a.offsets = offsets;
+    a.mtile_start = mtile;
+    a.row_weight = row_weight;
+    a.w1 = static_cast<const bf16*>(w1);
+    a.w3 = static_cast<const bf16*>(w3);
+    a.w2 = static_cast<const bf16*>(w2);
+    a.S = T * k;
+    a.d = d;
+    a.E = E;
+    a.f = ffn;
+    a.h = at<bf16>(ws, L.h);
+    a.P = at<bf16>(ws, L.P);
+    a.status = status;
+    a.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+    a.inject = opts ? opts->inject : 0;
+    MK_TRY(pm.mark(MK_PHASE_GEMM1));
+    MK_TRY(launch_gemm1(a, s));
+    MK_TRY(pm.mark(MK_PHASE_GEMM2));
+    MK_TRY(launch_gemm2(a, s));
+    MK_TRY(pm.mark(MK_PHASE_COMBINE));
+    MK_TRY(launch_combine(a.P, slot_row, T, d, k, static_cast<bf16*>(y), s));
+    MK_TRY(pm.mark(MK_PHASE_COUNT_ALL));
+    return MK_OK;
+}
+
+mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bias, const void* w1, const void* w3,
+                            const void* w2, int64_t T, int d, int E, int k, int ffn, void* y_host, void* ws,
+                            size_t ws_bytes, const mk_moe_opts* opts, void* stream) {
+    mk_status st = check_sizes(T, d, E, k, ffn);
+    if (st != MK_OK) return st;
+    if (!x_host || !y_host) return MK_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, ffn);
+    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
+    if (T == 0) return MK_OK;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bytes = static_cast<size_t>(T) * d * 2;
+    void* xd = at<uint8_t>(ws, L.x_stage);
+    void* yd = at<uint8_t>(ws, L.y_stage);
+    MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+    st = mk_moe_layer(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, ws_bytes, opts, stream);
+    if (st != MK_OK) return st;
+    MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+    return MK_OK;
+}
+
+mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail) {
+    if (ws == nullptr) return MK_ERR_WORKSPACE;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(s) != cudaSuccess) return MK_ERR_CUDA;
+    uint32_t st[2] = {0, 0};
+    if (cudaMemcpy(st, ws, sizeof st, cudaMemcpyDeviceToHost) != cudaSuccess) return MK_ERR_CUDA;
+    if (cudaMemset(ws, 0, sizeof st) != cudaSuccess) return MK_ERR_CUDA;
+    if (detail) *detail = st[1];
+    return static_cast<mk_status>(st[0]);
+}
+
+mk_status mk_moe_layer_routing(const void* ws, int64_t T, int d, int E, int k, int ffn, int32_t* topk_ids,
+                               float* topk_w, int32_t* expert_offsets, int32_t* slot_row, void* stream) {
+    mk_status st = check_sizes(T, d, E, k, ffn);
+    if (st != MK_OK) return st;
+    if (ws == nullptr) return MK_ERR_WORKSPACE;
+    if (T == 0) return MK_OK;
+    const WsLayout L = ws_layout(T, d, E, k, ffn);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    void* w = const_cast<void*>(ws);
+    const size_t tk = static_cast<size_t>(T) * k * 4;
+    if (topk_ids) MK_TRY(cudaMemcpyAsync(topk_ids, at<uint8_t>(w, L.ids), tk, cudaMemcpyDeviceToDevice, s));
+    if (topk_w) MK_TRY(cudaMemcpyAsync(topk_w, at<uint8_t>(w, L.w), tk, cudaMemcpyDeviceToDevice, s));
+    if (expert_offsets)
+        MK_TRY(cudaMemcpyAsync(expert_offsets, at<uint8_t>(w, L.offsets), 4 * (E + 1), cudaMemcpyDeviceToDevice, s));
+    if (slot_row) MK_TRY(cudaMemcpyAsync(slot_row, at<uint8_t>(w, L.slot_row), tk, cudaMemcpyDeviceToDevice, s));
+    return MK_OK;
+}
+
+}  // extern "C"

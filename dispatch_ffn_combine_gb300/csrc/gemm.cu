@@ -1,0 +1,428 @@
+// gemm.cu -- grouped expert GEMMs on the 5th-generation tensor cores (tcgen05).
+//
+// The expert FFN of the layer (mKernel README, kernel table, row "MoE Dispatch
+// + FFN + Combine": "runs the per-expert FFN (gemm1 -> SwiGLU -> gemm2)") as
+// two persistent grouped GEMMs over the expert-contiguous rows:
+//   gemm1:  acc = X_e [W1_e ; W3_e]^T  (one 128 x 256 MMA tile: 128 gate
+//           columns and the matching 128 up columns), epilogue
+//           h = bf16(silu(gate) * up)
+//   gemm2:  acc = H_e W2_e^T (128 x 256 tile), epilogue
+//           P = bf16(row_weight * acc)
+// The paper builds its compute blocks from ThunderKittens tiles on Hopper
+// (section 3); here the tile is GB300-native:
+//   warp 0      TMA producer: box loads of A (128 x 64) and B (256 x 64) with
+//               the 128-byte swizzle into a 4-stage shared-memory ring
+//   warp 1      MMA issuer: one thread issues tcgen05.mma (bf16 in, fp32
+//               accumulate in TMEM), commits free smem stages and full
+//               accumulators to mbarriers
+//   warps 2..5  epilogue: tcgen05.ld of the accumulator (each warp owns the
+//               32 TMEM lanes its warp index allows), fused SwiGLU or weight
+//               scaling, bf16 stores of the valid rows
+// Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
+// tile overlap the main loop of the next.  One CTA per SM walks a static
+// stride over the tile list; a tile is (expert, 128-row block, N block), found
+// from the per-expert tile prefix table with a binary search.  Rows past the
+// expert's end are loaded (TMA fills past the tensor end with zeros) but never
+// stored.  Every wait is bounded (see mk_device.cuh): on a timeout the CTA
+// records MK_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM, returns.
+#include "mk_device.cuh"
+#include "mk_internal.h"
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+namespace mk {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int MMA_N = 256;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = MMA_N * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * MMA_N;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
+
+struct SharedCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t drain;
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+    uint32_t zero;
+};
+
+constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(SharedCtl) + 1024;
+
+struct GemmParams {
+    const int32_t* offsets;      // [E+1]
+    const int32_t* mtile_start;  // [E+1]
+    const float* row_weight;     // gemm2 only, may be null
+    bf16* out;
+    int64_t out_ld;
+    int E;
+    int n_tiles;    // N blocks per 128-row block
+    int tile_n;     // output columns per tile (128 gemm1, 256 gemm2)
+    int n_valid;    // output columns of the whole GEMM
+    int k_blocks;   // K / 64
+    int b_rows_per_expert;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int stall_first_stage;  // test hook: block 0 never loads its first stage
+};
+
+struct TileInfo {
+    int e;
+    int row0;
+    int rows;
+    int n0;
+};
+
+__device__ __forceinline__ TileInfo decode_tile(int tile, const GemmParams& p) {
+    const int g = tile / p.n_tiles;
+    const int nt = tile - g * p.n_tiles;
+    int lo = 0, hi = p.E - 1;  // largest e with mtile_start[e] <= g
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.mtile_start[mid] <= g)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int mt = g - p.mtile_start[lo];
+    const int off = p.offsets[lo];
+    const int cnt = p.offsets[lo + 1] - off;
+    TileInfo ti;
+    ti.e = lo;
+    ti.row0 = off + mt * BM;
+    ti.rows = min(BM, cnt - mt * BM);
+    ti.n0 = nt * p.tile_n;
+    return ti;
+}
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return (g / (1.0f + expf(-g))) * u; }
+
+template <int MODE>  // 0: gemm1 + SwiGLU, 1: gemm2 + row weight
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                        const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    SharedCtl* ctl = reinterpret_cast<SharedCtl*>(smem + STAGES * STAGE_BYTES);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int total_tiles = p.mtile_start[p.E] * p.n_tiles;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < STAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tmem_full[a]), 1);
+            mbar_init(smem_u32(&ctl->tmem_empty[a]), 4);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        ctl->zero = 0;
+        fence_mbar_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB0);
+        if (MODE == 0) prefetch_tensormap(&tmB1);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile uint32_t* abort_word = &ctl->abort_flag;
+    const volatile uint32_t* never = &ctl->zero;
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                const TileInfo ti = decode_tile(tile, p);
+                const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = smem_u32(&ctl->full[stage]);
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (p.stall_first_stage && blockIdx.x == 0 && tile == 0 && kb == 0) {
+                        // Injected stall: the stage is announced but never filled.
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
+                        }
+                        continue;
+                    }
+                    tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
+                    if (MODE == 0) {
+                        tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                        tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
+                    } else {
+                        tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                    }
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+            }
+            if (!ok) {
+                *abort_word = 1u;
+                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+            }
+            // Every copy this thread started must land before the CTA exits.
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0) {
+            // ------------------------------------------------ MMA issuer
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            bool ok = true;
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+                if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, abort_word, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * MMA_N;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_word, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = sw128_kmajor_desc(sa + kk * UMMA_K * 2);
+                        const uint64_t bd = sw128_kmajor_desc(sb + kk * UMMA_K * 2);
+                        mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit(smem_u32(&ctl->empty[stage]));
+                    if (++stage == STAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit(smem_u32(&ctl->tmem_full[acc]));
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                *abort_word = 1u;
+                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+            }
+            // All MMAs issued by this thread complete before TMEM is freed.
+            mma_commit(smem_u32(&ctl->drain));
+            if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0u, never, p.timeout_ns))
+                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmDrain);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue
+        const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
+        const int row_in_tile = sub * 32 + lane;
+        uint32_t acc = 0, acc_phase = 0;
+        bool ok = true;
+        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
+            const TileInfo ti = decode_tile(tile, p);
+            if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[acc]), acc_phase, abort_word, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * MMA_N;
+            const bool row_ok = row_in_tile < ti.rows;
+            const int64_t r = static_cast<int64_t>(ti.row0) + row_in_tile;
+            bf16* orow = p.out + r * p.out_ld;
+            if (MODE == 0) {
+#pragma unroll 1
+                for (int c = 0; c < 128; c += 32) {
+                    uint32_t g[32], u[32];
+                    tmem_ld_32x32b_x32(tbase + c, g);
+                    tmem_ld_32x32b_x32(tbase + 128 + c, u);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            pk[q] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * q]), __uint_as_float(u[2 * q])),
+                                                silu_mul(__uint_as_float(g[2 * q + 1]), __uint_as_float(u[2 * q + 1])));
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = ti.n0 + c + 8 * v;
+                            if (col < p.n_valid)
+                                *reinterpret_cast<uint4*>(orow + col) =
+                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        }
+                    }
+                }
+            } else {
+                const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
+#pragma unroll 1
+                for (int c = 0; c < MMA_N; c += 32) {
+                    uint32_t a[32];
+                    tmem_ld_32x32b_x32(tbase + c, a);
+                    tmem_ld_wait();
+                    if (row_ok) {
+                        uint32_t pk[16];
+#pragma unroll
+                        for (int q = 0; q < 16; ++q)
+                            pk[q] = pack_bf16x2(__uint_as_float(a[2 * q]) * wr, __uint_as_float(a[2 * q + 1]) * wr);
+#pragma unroll
+                        for (int v = 0; v < 4; ++v) {
+                            const int col = ti.n0 + c + 8 * v;
+                            if (col < p.n_valid)
+                                *reinterpret_cast<uint4*>(orow + col) =
+                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+                        }
+                    }
+                }
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->tmem_empty[acc]));
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok && lane == 0) {
+            *abort_word = 1u;
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] (row-major), box {64, box_rows}, 128-byte swizzle.
+bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int MODE>
+cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const GemmParams& p,
+                        int64_t S, cudaStream_t s) {
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !configured[dev]) {
+        err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   static_cast<int>(SMEM_BYTES));
+        if (err != cudaSuccess) return err;
+        configured[dev] = 1;
+    }
+    // Upper bound on the tile count: every expert adds at most one partial block.
+    const int64_t max_tiles = ((S + BM - 1) / BM + p.E) * static_cast<int64_t>(p.n_tiles);
+    const int grid = static_cast<int>(std::min<int64_t>(device_sm_count(), std::max<int64_t>(max_tiles, 1)));
+    grouped_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s) {
+    CUtensorMap ma, mb0, mb1;
+    if (!make_map(&ma, a.x_perm, a.d, a.S, BM) ||
+        !make_map(&mb0, a.w1, a.d, static_cast<uint64_t>(a.E) * a.f, MMA_N / 2) ||
+        !make_map(&mb1, a.w3, a.d, static_cast<uint64_t>(a.E) * a.f, MMA_N / 2))
+        return cudaErrorInvalidValue;
+    GemmParams p;
+    p.offsets = a.offsets;
+    p.mtile_start = a.mtile_start;
+    p.row_weight = nullptr;
+    p.out = a.h;
+    p.out_ld = a.f;
+    p.E = a.E;
+    p.tile_n = MMA_N / 2;
+    p.n_tiles = (a.f + p.tile_n - 1) / p.tile_n;
+    p.n_valid = a.f;
+    p.k_blocks = a.d / BK;
+    p.b_rows_per_expert = a.f;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
+    return launch_mode<0>(ma, mb0, mb1, p, a.S, s);
+}
+
+cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s) {
+    CUtensorMap ma, mb0;
+    if (!make_map(&ma, a.h, a.f, a.S, BM) || !make_map(&mb0, a.w2, a.f, static_cast<uint64_t>(a.E) * a.d, MMA_N))
+        return cudaErrorInvalidValue;
+    GemmParams p;
+    p.offsets = a.offsets;
+    p.mtile_start = a.mtile_start;
+    p.row_weight = a.row_weight;
+    p.out = a.P;
+    p.out_ld = a.d;
+    p.E = a.E;
+    p.tile_n = MMA_N;
+    p.n_tiles = (a.d + p.tile_n - 1) / p.tile_n;
+    p.n_valid = a.d;
+    p.k_blocks = a.f / BK;
+    p.b_rows_per_expert = a.d;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.stall_first_stage = 0;
+    return launch_mode<1>(ma, mb0, mb0, p, a.S, s);
+}
+
+}  // namespace mk

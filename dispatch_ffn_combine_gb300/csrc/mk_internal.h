@@ -1,0 +1,101 @@
+// mk_internal.h -- workspace layout and kernel launchers shared by the
+// translation units of libmkmoe.so (not part of the public ABI).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "mkmoe.h"
+
+namespace mk {
+
+using bf16 = __nv_bfloat16;
+
+constexpr int kChunkTokens = 128;    // tokens per histogram chunk (dispatch)
+constexpr int kTileM = 128;          // rows per grouped-GEMM tile
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;  // 2 s
+
+// Device error sites (status[1]).
+enum : uint32_t {
+    kSiteGemmProducer = 0x100,
+    kSiteGemmMma = 0x200,
+    kSiteGemmEpilogue = 0x300,
+    kSiteGemmDrain = 0x400,
+    kSiteCountIds = 0x500,
+    kSiteCountRepeat = 0x600,
+};
+
+// Byte offsets of every region of the caller's workspace.  The first 256
+// bytes hold the control block: status[0] = first device error code,
+// status[1] = its site.
+struct WsLayout {
+    size_t ctrl = 0;
+    size_t logits = 0;        // fp32 [T, E]
+    size_t ids = 0;           // int32 [T, k]
+    size_t w = 0;             // fp32 [T, k]
+    size_t chunk_counts = 0;  // int32 [nchunks, E]
+    size_t chunk_base = 0;    // int32 [nchunks, E]  rows of expert e before chunk c
+    size_t rank = 0;          // int32 [T, k]        rank of (t, j) inside its chunk and expert
+    size_t counts = 0;        // int32 [E]
+    size_t offsets = 0;       // int32 [E + 1]
+    size_t mtile_start = 0;   // int32 [E + 1]       prefix sum of ceil(count / 128)
+    size_t row_token = 0;     // int32 [S]
+    size_t row_weight = 0;    // fp32  [S]
+    size_t slot_row = 0;      // int32 [S]
+    size_t x_perm = 0;        // bf16  [S, d]
+    size_t h = 0;             // bf16  [S, f]
+    size_t P = 0;             // bf16  [S, d]
+    size_t x_stage = 0;       // bf16  [T, d]  host-buffer entry point: staged input
+    size_t y_stage = 0;       // bf16  [T, d]  host-buffer entry point: staged output
+    size_t total = 0;
+};
+
+WsLayout ws_layout(int64_t T, int d, int E, int k, int f);
+
+inline int64_t num_chunks(int64_t T) { return (T + kChunkTokens - 1) / kChunkTokens; }
+
+// ----------------------------------------------------------------- launchers
+cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
+                                float* logits, cudaStream_t s);
+cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
+                        int32_t* counts_or_null, cudaStream_t s);
+cudaError_t launch_count(const int32_t* ids, int64_t T, int E, int k, int32_t* chunk_counts, int32_t* rank,
+                         uint32_t* status, cudaStream_t s);
+cudaError_t launch_scan(const int32_t* chunk_counts, int64_t nchunks, int E, int32_t* chunk_base, int32_t* counts,
+                        int32_t* offsets, int32_t* mtile_start, cudaStream_t s);
+cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, int64_t T, int d, int E, int k,
+                           const int32_t* offsets, const int32_t* chunk_base, const int32_t* rank, bf16* x_perm,
+                           int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s);
+cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t* mtile_start, uint32_t* status,
+                               cudaStream_t s);
+cudaError_t launch_combine(const bf16* P, const int32_t* slot_row, int64_t T, int d, int k, bf16* y,
+                           cudaStream_t s);
+
+struct FfnArgs {
+    const bf16* x_perm;
+    const int32_t* offsets;      // [E+1]
+    const int32_t* mtile_start;  // [E+1]
+    const float* row_weight;     // [S] or null
+    const bf16* w1;
+    const bf16* w3;
+    const bf16* w2;
+    int64_t S;
+    int d, E, f;
+    bf16* h;
+    bf16* P;
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int inject;                  // MK_INJECT_STALL_GEMM1 or 0
+};
+cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s);
+
+int device_sm_count();      // SMs of the current device (cached per device)
+bool device_is_sm103();     // current device is compute capability 10.3
+
+}  // namespace mk

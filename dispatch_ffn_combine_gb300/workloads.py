@@ -87,16 +87,19 @@ def zipf_bias(E: int, s: float) -> torch.Tensor:
     return torch.tensor([-s * math.log(e + 1.0) for e in range(E)], dtype=torch.float32)
 
 
-def make_inputs(cfg: MoEConfig, seed: int = 0, device="cpu", T: int | None = None) -> dict:
+def make_inputs(cfg: MoEConfig, seed: int = 0, device="cpu", T: int | None = None, experts: bool = True) -> dict:
     """Draw one workload.  Returns a dict of torch tensors on ``device``:
     x [T,d] bf16, wg [E,d] f32, bias [E] f32 or None, w1/w3 [E,f,d] bf16,
-    w2 [E,d,f] bf16.  ``T`` overrides the token count (weights unchanged)."""
+    w2 [E,d,f] bf16.  ``T`` overrides the token count (weights unchanged);
+    ``experts=False`` skips the expert weights (router-only uses)."""
     T = cfg.T if T is None else T
     d, E, f = cfg.d, cfg.E, cfg.f
     dev = torch.device(device)
     x = _normal((T, d), 1.0, tensor_seed(seed, "x"), dev).to(torch.bfloat16)
     wg = _normal((E, d), d ** -0.5, tensor_seed(seed, "wg"), dev)
     bias = zipf_bias(E, cfg.zipf_s).to(dev) if cfg.zipf_s else None
+    if not experts:
+        return {"x": x, "wg": wg, "bias": bias, "w1": None, "w3": None, "w2": None}
     w1 = torch.empty((E, f, d), dtype=torch.bfloat16, device=dev)
     w3 = torch.empty((E, f, d), dtype=torch.bfloat16, device=dev)
     w2 = torch.empty((E, d, f), dtype=torch.bfloat16, device=dev)

@@ -1,0 +1,189 @@
+/*
+ * mkmoe.h -- C ABI of the GB300 (sm_103a) fused mixture-of-experts layer.
+ *
+ * The layer is the one the mKernel README describes in its kernel table, row
+ * "MoE Dispatch + FFN + Combine": tokens are routed to experts, each expert
+ * runs its FFN (gemm1 -> SwiGLU -> gemm2), and the weighted expert outputs
+ * are combined back into each token's row.  The mKernel paper ("mKernel: Fast
+ * Multi-GPU, Multi-Node Fused Kernels", section 3 and Figure 2) runs such
+ * layers as persistent kernels whose thread blocks take compute or
+ * data-movement roles, with per-tile ready flags (section 4, "epoch-stamped
+ * readiness flags").  On one GPU the expert-parallel exchanges become a
+ * permutation inside HBM (dispatch) and a gather (combine).
+ *
+ * Conventions for every entry point:
+ *   - Pointers to tensors are DEVICE pointers owned by the caller; the library
+ *     keeps no reference after the call returns.  All tensors are row-major,
+ *     contiguous, 16-byte aligned.  bf16 tensors are passed as void*.
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     are asynchronous on that stream; the library allocates nothing per call.
+ *   - `ws` is a caller-owned device workspace of at least
+ *     mk_moe_workspace_size(...) bytes, 256-byte aligned.  One workspace per
+ *     stream in flight: two calls that use one workspace concurrently race.
+ *   - Argument errors are returned synchronously, before anything is enqueued.
+ *     Errors found on the device (a bounded wait that ran out, an index out of
+ *     range in caller-supplied routing) are recorded in the workspace and
+ *     reported by mk_moe_last_device_error().  A failed CUDA launch returns
+ *     MK_ERR_CUDA.
+ *   - T == 0 is a valid no-op.
+ *   - Limits: 1 <= E <= 256, 1 <= k <= min(E, 8), d and ffn multiples of 64,
+ *     T * k < 2^31, T * k * max(d, ffn) < 2^40.
+ *
+ * Routing (the pages leave the router open; this is the reading used):
+ *   logit[t,e] = sum_i x[t,i] * wg[e,i] (+ bias[e]) in fp32, in a fixed
+ *   order: 32 interleaved partial sums s_j over i = j, j+32, ..., each a chain
+ *   of correctly rounded fused multiply-adds, then the pairwise tree
+ *   s_j += s_{j+off} for off = 16, 8, 4, 2, 1, then + bias[e].  The k largest
+ *   logits are chosen, ties to the lower expert id; slot j holds the j-th
+ *   largest.  weight_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0) (softmax over
+ *   the chosen k, equal to the full softmax renormalised over the k).
+ */
+#ifndef MKMOE_H
+#define MKMOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MK_API __attribute__((visibility("default")))
+#else
+#define MK_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MK_OK = 0,
+    MK_ERR_INVALID_ARG = 1,   /* a size, pointer or alignment argument is invalid */
+    MK_ERR_WORKSPACE = 2,     /* ws is NULL, misaligned or smaller than required */
+    MK_ERR_UNSUPPORTED = 3,   /* valid request outside this build's limits, or no sm_103a device */
+    MK_ERR_CUDA = 4,          /* a CUDA runtime call or kernel launch failed */
+    MK_ERR_TIMEOUT = 5,       /* device: a bounded wait ran out (detail = wait site) */
+    MK_ERR_BOUNDS = 6         /* device: caller-supplied routing out of range or repeated */
+} mk_status;
+
+/* Phases of mk_moe_layer, in launch order (indices into opts->phase_events). */
+enum {
+    MK_PHASE_ROUTE_LOGITS = 0, /* gate logits, fp32 fixed order                    */
+    MK_PHASE_TOPK = 1,         /* top-k + softmax weights                          */
+    MK_PHASE_COUNT = 2,        /* per-chunk expert histograms + ranks               */
+    MK_PHASE_SCAN = 3,         /* expert offsets, chunk bases, M-tile table          */
+    MK_PHASE_SCATTER = 4,      /* token rows -> expert-contiguous rows (dispatch)    */
+    MK_PHASE_GEMM1 = 5,        /* grouped x W1^T, x W3^T, SwiGLU -> h                */
+    MK_PHASE_GEMM2 = 6,        /* grouped h W2^T, scaled by the routing weight -> P  */
+    MK_PHASE_COMBINE = 7,      /* y[t] = sum_j P[slot_row[t,j]] in j order           */
+    MK_PHASE_COUNT_ALL = 8
+};
+
+/* Optional per-call settings (pass NULL for defaults). */
+typedef struct {
+    uint64_t timeout_ns;   /* bound on each device-side wait; 0 = 2 s                       */
+    void** phase_events;   /* NULL, or MK_PHASE_COUNT_ALL + 1 cudaEvent_t handles created by
+                              the caller; event i is recorded on `stream` before phase i and
+                              the last one after the final phase (for per-phase timing)      */
+    int inject;            /* test hook, 0 = off.  MK_INJECT_STALL_GEMM1: block 0 of the first
+                              grouped GEMM announces one shared-memory stage but never loads
+                              it, so its consumers' bounded waits run out; the call then
+                              reports MK_ERR_TIMEOUT (no fault, no hang).                    */
+    int reserved[3];       /* must be zero                                                   */
+} mk_moe_opts;
+
+#define MK_INJECT_STALL_GEMM1 1
+
+/* Bytes of workspace mk_moe_layer needs for these sizes (also enough for
+ * mk_moe_route, mk_moe_dispatch and mk_moe_expert_ffn on the same sizes).
+ * Returns 0 if the sizes are invalid. */
+MK_API size_t mk_moe_workspace_size(int64_t T, int d, int E, int k, int ffn);
+
+/* Router (routing step of the README's "MoE Dispatch + FFN + Combine" row).
+ *   x        bf16 [T, d]            token activations
+ *   wg       fp32 [E, d]            gate matrix
+ *   bias     fp32 [E] or NULL       per-expert logit offset
+ *   topk_ids int32 [T, k] (out)     chosen experts, slot order as above
+ *   topk_w   fp32 [T, k] (out)      routing weights, sum to 1 per token
+ *   expert_counts int32 [E] (out, may be NULL)  rows routed to each expert */
+MK_API mk_status mk_moe_route(const void* x, const float* wg, const float* bias,
+                       int64_t T, int d, int E, int k,
+                       int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch: permute token rows into expert-contiguous order (the local form of
+ * the README's all-to-all dispatch; paper section 3.1 and Table 3 describe the
+ * expert-parallel version that pulls tokens from peers).
+ *   x, topk_ids [T,k], topk_w [T,k] (inputs; topk_w may be NULL)
+ *   expert_offsets int32 [E+1] (out)  expert e owns rows [off[e], off[e+1])
+ *   row_token      int32 [T*k] (out)  source token of each row; ascending within an expert
+ *   row_weight     fp32  [T*k] (out, may be NULL)  routing weight of each row
+ *   slot_row       int32 [T, k] (out) row that holds (token t, slot j)
+ *   x_perm         bf16  [T*k, d] (out) x_perm[slot_row[t,j]] = x[t]
+ * Ids outside [0, E) or repeated within a token set MK_ERR_BOUNDS on the device. */
+MK_API mk_status mk_moe_dispatch(const void* x, const int32_t* topk_ids, const float* topk_w,
+                          int64_t T, int d, int E, int k,
+                          int32_t* expert_offsets, int32_t* row_token, float* row_weight,
+                          int32_t* slot_row, void* x_perm,
+                          void* ws, size_t ws_bytes, void* stream);
+
+/* Grouped expert FFN on dispatched rows (README row: "gemm1 -> SwiGLU -> gemm2",
+ * "weighted expert outputs"), on the tensor cores:
+ *   h[r]  = bf16( silu(x_perm[r] W1_e^T) * (x_perm[r] W3_e^T) )   (fp32 accumulate)
+ *   P[r]  = bf16( row_weight[r] * (h[r] W2_e^T) )                  (fp32 accumulate)
+ * for every row r of expert e.
+ *   x_perm bf16 [S, d]; expert_offsets int32 [E+1] with off[0] = 0, off[E] = S
+ *   row_weight fp32 [S] or NULL (= 1)
+ *   w1, w3 bf16 [E, ffn, d]; w2 bf16 [E, d, ffn]   (out x in)
+ *   h bf16 [S, ffn] (out), P bf16 [S, d] (out) */
+MK_API mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, const float* row_weight,
+                            const void* w1, const void* w3, const void* w2,
+                            int64_t S, int d, int E, int ffn,
+                            void* h, void* P,
+                            void* ws, size_t ws_bytes, void* stream);
+
+/* Combine (README row: "combines the weighted expert outputs back to each
+ * token's source rank"; here: back to the token's row):
+ *   y[t] = bf16( sum_{j=0..k-1} P[slot_row[t,j]] ), fp32 sum in ascending j.
+ *   P bf16 [T*k, d]; slot_row int32 [T, k]; y bf16 [T, d] (out) */
+MK_API mk_status mk_moe_combine(const void* P, const int32_t* slot_row, int64_t T, int d, int k,
+                         void* y, void* stream);
+
+/* The whole layer: route -> dispatch -> expert FFN -> combine.
+ *   x bf16 [T,d]; wg fp32 [E,d]; bias fp32 [E] or NULL;
+ *   w1, w3 bf16 [E,ffn,d]; w2 bf16 [E,d,ffn]; y bf16 [T,d] (out).
+ *   opts may be NULL. */
+MK_API mk_status mk_moe_layer(const void* x, const float* wg, const float* bias,
+                       const void* w1, const void* w3, const void* w2,
+                       int64_t T, int d, int E, int k, int ffn,
+                       void* y, void* ws, size_t ws_bytes,
+                       const mk_moe_opts* opts, void* stream);
+
+/* The layer on HOST buffers: copies x_host (T*d bf16, pinned for an
+ * asynchronous copy) into a staging region of `ws`, runs mk_moe_layer, and
+ * copies y back into y_host.  Weights stay on the device.  Asynchronous on
+ * `stream`; the result is in y_host once the stream has reached this point. */
+MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bias,
+                            const void* w1, const void* w3, const void* w2,
+                            int64_t T, int d, int E, int k, int ffn,
+                            void* y_host, void* ws, size_t ws_bytes,
+                            const mk_moe_opts* opts, void* stream);
+
+/* Synchronises `stream`, then returns and clears the device-side status of
+ * `ws` (MK_OK if no device error).  *detail (may be NULL) receives the site
+ * code of the error. */
+MK_API mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail);
+
+/* Static, human-readable name of a status code. */
+MK_API const char* mk_moe_status_string(mk_status s);
+
+/* Reads the internal routing tables that mk_moe_layer left in `ws`
+ * (asynchronous device-to-device copies on `stream`; any pointer may be NULL):
+ * topk_ids [T,k], topk_w [T,k], expert_offsets [E+1], slot_row [T,k]. */
+MK_API mk_status mk_moe_layer_routing(const void* ws, int64_t T, int d, int E, int k, int ffn,
+                               int32_t* topk_ids, float* topk_w, int32_t* expert_offsets,
+                               int32_t* slot_row, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MKMOE_H */

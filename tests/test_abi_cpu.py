@@ -1,0 +1,112 @@
+"""C-ABI checks that need no GPU: the library builds and loads, exports exactly
+the entry points include/mkmoe.h declares, sizes its workspace, and rejects
+bad arguments synchronously (before any CUDA call)."""
+import ctypes
+import os
+import re
+import subprocess
+
+import pytest
+
+import dispatch_ffn_combine_gb300 as mk
+from dispatch_ffn_combine_gb300 import build as cuda_build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    cuda_build.build()
+    return mk.load_library()
+
+
+def _declared():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            txt = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"^MK_API\s+[\w\s\*]+?\b(mk_\w+)\s*\(", txt, flags=re.M))
+    return names
+
+
+def test_exports_match_header(lib):
+    declared = _declared()
+    assert declared == set(mk.ENTRY_POINTS)
+    out = subprocess.run(["nm", "-D", "--defined-only", mk.LIB_PATH], capture_output=True, text=True, check=True)
+    exported = {ln.split()[-1] for ln in out.stdout.splitlines() if " T " in ln}
+    assert exported == declared, (exported ^ declared)
+
+
+def test_workspace_size(lib):
+    n = mk.workspace_size(32768, 7168, 256, 8, 2048)
+    S = 32768 * 8
+    # at least x_perm + h + P + the host staging buffers
+    assert n >= 2 * S * 7168 + 2 * S * 2048 + 2 * S * 7168 + 2 * 2 * 32768 * 7168
+    assert mk.workspace_size(0, 256, 8, 2, 512) > 0
+    for bad in [(16, 100, 8, 2, 512), (16, 256, 0, 1, 512), (16, 256, 8, 9, 512), (16, 256, 4, 5, 512),
+                (16, 256, 300, 2, 512), (16, 256, 8, 2, 500), (-1, 256, 8, 2, 512)]:
+        assert mk.workspace_size(*bad) == 0, bad
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert mk.status_string(s).startswith("MK_")
+    assert "unknown" in mk.status_string(99)
+
+
+def _vp(v):
+    return ctypes.c_void_p(v)
+
+
+def test_layer_rejects_bad_arguments(lib):
+    A = _vp(0x10000)  # never dereferenced: every case fails validation first
+    T, d, E, k, f = 64, 256, 8, 2, 512
+    need = mk.workspace_size(T, d, E, k, f)
+    L = lib.mk_moe_layer
+    ok_args = [A, A, None, A, A, A, T, d, E, k, f, A, A, need, None, None]
+
+    def call(**over):
+        args = list(ok_args)
+        names = ["x", "wg", "bias", "w1", "w3", "w2", "T", "d", "E", "k", "f", "y", "ws", "wsb", "opts", "s"]
+        for key, v in over.items():
+            args[names.index(key)] = v
+        return L(*args)
+
+    assert call(d=100) == mk.MK_ERR_INVALID_ARG
+    assert call(f=96) == mk.MK_ERR_INVALID_ARG
+    assert call(k=0) == mk.MK_ERR_INVALID_ARG
+    assert call(k=9, E=16) == mk.MK_ERR_INVALID_ARG
+    assert call(E=257) == mk.MK_ERR_INVALID_ARG
+    assert call(T=-5) == mk.MK_ERR_INVALID_ARG
+    assert call(x=None) == mk.MK_ERR_INVALID_ARG
+    assert call(w2=None) == mk.MK_ERR_INVALID_ARG
+    assert call(x=_vp(0x10008)) == mk.MK_ERR_INVALID_ARG  # not 16-byte aligned
+    assert call(ws=None) == mk.MK_ERR_WORKSPACE
+    assert call(ws=_vp(0x10080)) == mk.MK_ERR_WORKSPACE  # not 256-byte aligned
+    assert call(wsb=need - 1) == mk.MK_ERR_WORKSPACE
+    assert call(T=1 << 28, k=8) == mk.MK_ERR_UNSUPPORTED  # T*k >= 2^31
+    opts = mk.MkMoeOpts()
+    opts.reserved[0] = 1
+    assert call(opts=ctypes.pointer(opts)) == mk.MK_ERR_INVALID_ARG
+    opts = mk.MkMoeOpts()
+    opts.inject = 7
+    assert call(opts=ctypes.pointer(opts)) == mk.MK_ERR_INVALID_ARG
+    # T == 0 is a no-op that enqueues nothing
+    assert call(T=0, wsb=mk.workspace_size(0, d, E, k, f)) == mk.MK_OK
+
+
+def test_other_entry_points_reject_bad_arguments(lib):
+    A = _vp(0x10000)
+    T, d, E, k = 64, 256, 8, 2
+    need = mk.workspace_size(T, d, E, k, 64)
+    assert lib.mk_moe_route(None, A, None, T, d, E, k, A, A, None, A, need, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_route(A, A, None, T, 96, E, k, A, A, None, A, need, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_route(A, A, None, T, d, E, k, A, A, None, A, need - 1, None) == mk.MK_ERR_WORKSPACE
+    assert lib.mk_moe_dispatch(A, A, None, T, d, E, k, None, A, None, A, A, A, need, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_dispatch(A, A, None, T, d, E, 9, A, A, None, A, A, A, need, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_expert_ffn(A, A, None, A, A, A, T, d, E, 100, A, A, A, 4096, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_expert_ffn(A, A, None, A, A, A, T, d, E, 512, A, A, A, 16, None) == mk.MK_ERR_WORKSPACE
+    assert lib.mk_moe_combine(A, A, T, d, 9, A, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_combine(None, A, T, d, k, A, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_combine(A, A, 0, d, k, A, None) == mk.MK_OK
+    assert lib.mk_moe_last_device_error(None, None, None) == mk.MK_ERR_WORKSPACE

@@ -1,0 +1,122 @@
+"""GPU parity of the whole layer (mk_moe_layer) against the CPU oracle.
+
+Small shapes are checked on every token; the full-size workloads run in the
+launch configuration the benchmark times, with routing and dispatch checked on
+every token (bit-exact) and the output on a fixed token sample."""
+import gc
+
+import numpy as np
+import pytest
+import torch
+
+import dispatch_ffn_combine_gb300 as mk
+import oracle
+from _support import Workload, check_output, sample_tokens
+
+pytestmark = pytest.mark.gpu
+
+
+def _run_layer(wl, **kw):
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    y = mk.mk_moe_layer(wl.g["x"], wl.g["wg"], wl.g["bias"], wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k, ws=ws, **kw)
+    st, site = mk.mk_moe_last_device_error(ws)
+    assert st == mk.MK_OK, (st, hex(site))
+    return y, ws
+
+
+def _check_routing(wl, ws, ids_ref, w_ref):
+    c = wl.cfg
+    ids, w, offsets, slot = mk.mk_moe_layer_routing(ws, wl.T, c.d, c.E, c.k, c.f)
+    torch.cuda.synchronize()
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-6, atol=1e-7)
+    _, off_ref, _, slot_ref = oracle.dispatch(ids_ref, c.E)
+    np.testing.assert_array_equal(offsets.cpu().numpy(), off_ref)
+    np.testing.assert_array_equal(slot.cpu().numpy(), slot_ref)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single"])
+def test_layer_small_all_tokens(name):
+    wl = Workload(name)
+    y, ws = _run_layer(wl)
+    y_ref, ids_ref, w_ref = wl.oracle_layer()
+    _check_routing(wl, ws, ids_ref, w_ref)
+    check_output(y.cpu(), y_ref, name)
+
+
+@pytest.mark.parametrize("T", [1, 2, 129])
+def test_layer_few_tokens(T):
+    wl = Workload("ragged", T=T)
+    y, ws = _run_layer(wl)
+    y_ref, ids_ref, w_ref = wl.oracle_layer()
+    _check_routing(wl, ws, ids_ref, w_ref)
+    check_output(y.cpu(), y_ref, f"ragged T={T}")
+
+
+def test_layer_zero_tokens_is_noop():
+    wl = Workload("tiny", T=0)
+    c = wl.cfg
+    ws = mk.alloc_workspace(0, c.d, c.E, c.k, c.f, wl.dev)
+    y = mk.mk_moe_layer(wl.g["x"], wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k, ws=ws)
+    assert y.shape == (0, c.d)
+
+
+def test_layer_mid_sampled():
+    wl = Workload("mid")
+    y, ws = _run_layer(wl)
+    _, ids_ref, w_ref = wl.oracle_routing()
+    _check_routing(wl, ws, ids_ref, w_ref)
+    toks = sample_tokens(wl.T, 256)
+    y_ref, _, _ = wl.oracle_layer(tokens=toks)
+    check_output(y.cpu()[torch.from_numpy(toks)], y_ref, "mid")
+
+
+def test_layer_deterministic():
+    wl = Workload("ragged_skew")
+    y1, ws = _run_layer(wl)
+    y2, _ = _run_layer(wl)
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+
+
+def test_layer_host_buffers_match_device_call():
+    wl = Workload("ragged")
+    c = wl.cfg
+    y_dev, ws = _run_layer(wl)
+    x_host = wl.g["x"].cpu().pin_memory()
+    y_host = torch.empty((wl.T, c.d), dtype=torch.bfloat16).pin_memory()
+    mk.mk_moe_layer_host(x_host, wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k, y_host, ws)
+    torch.cuda.synchronize()
+    assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+
+def test_layer_bounded_wait_times_out_cleanly():
+    """A grouped-GEMM stage that is announced but never filled: the waits on it
+    run out after the given limit, the call reports MK_ERR_TIMEOUT, nothing
+    faults or hangs, and the next call on the same context is correct."""
+    wl = Workload("ragged")
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    args = (wl.g["x"], wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
+    mk.mk_moe_layer(*args, ws=ws, inject=mk.MK_INJECT_STALL_GEMM1, timeout_ns=20_000_000)
+    st, site = mk.mk_moe_last_device_error(ws)
+    assert st == mk.MK_ERR_TIMEOUT, (st, hex(site))
+    y = mk.mk_moe_layer(*args, ws=ws)
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    y_ref, _, _ = wl.oracle_layer()
+    check_output(y.cpu(), y_ref, "after timeout")
+
+
+@pytest.mark.parametrize("name,n_sample", [("skewed", 96), ("decode", 128), ("large", 64)])
+def test_layer_full_size(name, n_sample):
+    """Full-size workload in the benchmark's launch configuration."""
+    wl = Workload(name)
+    y, ws = _run_layer(wl)
+    _, ids_ref, w_ref = wl.oracle_routing()
+    _check_routing(wl, ws, ids_ref, w_ref)
+    toks = sample_tokens(wl.T, n_sample)
+    y_ref, _, _ = wl.oracle_layer(tokens=toks)
+    check_output(y.cpu()[torch.from_numpy(toks)], y_ref, name)
+    del wl, y, ws
+    gc.collect()
+    torch.cuda.empty_cache()

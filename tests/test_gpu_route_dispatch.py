@@ -1,0 +1,125 @@
+"""GPU parity: router and dispatch against the CPU oracle, through the C ABI.
+
+Routing decides integers, so ids, counts, offsets, row order and slot rows
+must match the oracle bit for bit; the fp32 routing weights (GPU expf vs the
+oracle's fp64 exp of the same fp32 logits) must agree to 1e-6 relative."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import dispatch_ffn_combine_gb300 as mk
+import oracle
+from _support import Workload
+
+pytestmark = pytest.mark.gpu
+
+ROUTE_CONFIGS = ["tiny", "ragged", "ragged_skew", "single", "mid", "skewed", "decode", "large"]
+
+
+@pytest.mark.parametrize("name", ROUTE_CONFIGS)
+def test_route_bit_exact(name):
+    wl = Workload(name, experts=False)
+    E, k = wl.cfg.E, wl.cfg.k
+    ids, w, counts = mk.mk_moe_route(wl.g["x"], wl.g["wg"], wl.g["bias"], k)
+    torch.cuda.synchronize()
+    _, ids_ref, w_ref = wl.oracle_routing()
+    ids_g = ids.cpu().numpy()
+    mismatch = np.nonzero(np.any(ids_g != ids_ref, axis=1))[0]
+    assert mismatch.size == 0, f"{mismatch.size} tokens routed differently (first {mismatch[:5]}); " \
+                               f"near-ties in fp64: {wl.near_ties(ids_ref)}"
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-6, atol=1e-7)
+    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(ids_ref.ravel(), minlength=E))
+
+
+def test_route_fixed_order_decides_weights():
+    """Hand-worked order case on the GPU: token 0's expert 0 row is the
+    'tree_not_chain' vector (R1 logit 2^24+2; a single sequential chain gives
+    2^24, exact-then-round 2^24+4); expert 1's logit is exactly 2^24.  The
+    routing weights are then 1/(1+e^-2) and e^-2/(1+e^-2) only under R1."""
+    d, E, k = 64, 2, 2
+    dev = torch.device("cuda:0")
+    x = torch.zeros((1, d), dtype=torch.float32)
+    x[0, :4] = 1.0
+    wg = torch.zeros((E, d), dtype=torch.float32)
+    wg[0, 0] = 16777216.0
+    wg[0, 1:4] = 1.0
+    wg[1, 0] = 16777216.0
+    xb = x.to(torch.bfloat16).to(dev)
+    ids, w, _ = mk.mk_moe_route(xb, wg.to(dev), None, k)
+    torch.cuda.synchronize()
+    assert ids.cpu().tolist() == [[0, 1]]
+    e2 = math.exp(-2.0)
+    np.testing.assert_allclose(w.cpu().numpy()[0], [1 / (1 + e2), e2 / (1 + e2)], rtol=1e-6)
+
+
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "mid", "skewed", "decode"])
+def test_dispatch_bit_exact(name):
+    """GPU dispatch of the oracle's routing equals the oracle's dispatch."""
+    wl = Workload(name, experts=False)
+    E, k, T, d = wl.cfg.E, wl.cfg.k, wl.T, wl.cfg.d
+    _, ids_ref, w_ref = wl.oracle_routing()
+    ids_dev = torch.from_numpy(ids_ref).to(wl.dev)
+    w_dev = torch.from_numpy(w_ref.astype(np.float32)).to(wl.dev)
+    ws = mk.alloc_workspace(T, d, E, k, 64, wl.dev)
+    res = mk.mk_moe_dispatch(wl.g["x"], ids_dev, w_dev, E, ws=ws)
+    st, site = mk.mk_moe_last_device_error(ws)
+    assert st == mk.MK_OK, (st, hex(site))
+    counts, offsets, row_token, slot_row = oracle.dispatch(ids_ref, E)
+    np.testing.assert_array_equal(res["expert_offsets"].cpu().numpy(), offsets)
+    np.testing.assert_array_equal(res["row_token"].cpu().numpy(), row_token)
+    np.testing.assert_array_equal(res["slot_row"].cpu().numpy(), slot_row)
+    rw = res["row_weight"].cpu().numpy()
+    np.testing.assert_array_equal(rw[slot_row.ravel()], w_ref.astype(np.float32).ravel())
+    # x_perm rows are bitwise copies of the token rows
+    xp = res["x_perm"].view(torch.int16)
+    xs = wl.g["x"].view(torch.int16)
+    rt = torch.from_numpy(row_token.astype(np.int64)).to(wl.dev)
+    assert torch.equal(xp, xs.index_select(0, rt))
+
+
+def test_dispatch_random_routing_and_edge_counts():
+    """Routing not produced by the router: every expert count from 0 upward,
+    including experts nobody picks."""
+    T, d, E, k = 531, 128, 16, 4
+    rs = np.random.RandomState(5)
+    ids = np.stack([rs.choice(np.arange(E - 3), size=k, replace=False) for _ in range(T)]).astype(np.int32)
+    ids[::7, k - 1] = E - 1  # a rarely used expert; experts E-3 and E-2 stay empty
+    for r in ids:
+        assert len(set(r.tolist())) == k
+    dev = torch.device("cuda:0")
+    x = (torch.randn((T, d), generator=torch.Generator().manual_seed(3))).to(torch.bfloat16).to(dev)
+    res = mk.mk_moe_dispatch(x, torch.from_numpy(ids).to(dev), None, E)
+    torch.cuda.synchronize()
+    counts, offsets, row_token, slot_row = oracle.dispatch(ids, E)
+    assert counts[E - 3] == 0 and counts[E - 2] == 0
+    np.testing.assert_array_equal(res["expert_offsets"].cpu().numpy(), offsets)
+    np.testing.assert_array_equal(res["row_token"].cpu().numpy(), row_token)
+    np.testing.assert_array_equal(res["slot_row"].cpu().numpy(), slot_row)
+    np.testing.assert_array_equal(res["row_weight"].cpu().numpy(), 1.0)
+
+
+def test_dispatch_rejects_bad_ids_on_device():
+    """Out-of-range and repeated expert ids are caught by the kernel's own
+    checks (MK_ERR_BOUNDS), every access stays in bounds, and the next call on
+    the same workspace works."""
+    T, d, E, k = 300, 128, 8, 2
+    dev = torch.device("cuda:0")
+    x = torch.zeros((T, d), dtype=torch.bfloat16, device=dev)
+    ws = mk.alloc_workspace(T, d, E, k, 64, dev)
+    good = np.stack([np.array([t % E, (t + 1) % E]) for t in range(T)]).astype(np.int32)
+    for bad_fill in ("range", "repeat"):
+        ids = good.copy()
+        if bad_fill == "range":
+            ids[17, 1] = E + 3
+            ids[200, 0] = -1
+        else:
+            ids[42, 1] = ids[42, 0]
+        mk.mk_moe_dispatch(x, torch.from_numpy(ids).to(dev), None, E, ws=ws)
+        st, site = mk.mk_moe_last_device_error(ws)
+        assert st == mk.MK_ERR_BOUNDS, (bad_fill, st, hex(site))
+    res = mk.mk_moe_dispatch(x, torch.from_numpy(good).to(dev), None, E, ws=ws)
+    st, _ = mk.mk_moe_last_device_error(ws)
+    assert st == mk.MK_OK
+    np.testing.assert_array_equal(res["slot_row"].cpu().numpy(), oracle.dispatch(good, E)[3])
