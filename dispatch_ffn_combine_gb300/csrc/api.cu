@@ -193,6 +193,7 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
                             void* ws, size_t ws_bytes, void* stream) {
     mk_status st = check_sizes(S, d, E, 1, ffn);
     if (st != MK_OK) return st;
+    if (S == 0) return MK_OK;
     if (!x_perm || !expert_offsets || !w1 || !w3 || !w2 || !h || !P) return MK_ERR_INVALID_ARG;
     if (!aligned16(x_perm) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(h) || !aligned16(P))
         return MK_ERR_INVALID_ARG;
@@ -231,6 +232,7 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
 mk_status mk_moe_combine(const void* P, const int32_t* slot_row, int64_t T, int d, int k, void* y, void* stream) {
     mk_status st = check_sizes(T, d, k, k, 64);
     if (st != MK_OK) return st;
+    if (T == 0) return MK_OK;
     if (!P || !slot_row || !y) return MK_ERR_INVALID_ARG;
     if (!aligned16(P) || !aligned16(y)) return MK_ERR_INVALID_ARG;
     if (T == 0) return MK_OK;
@@ -245,6 +247,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
                        const mk_moe_opts* opts, void* stream) {
     mk_status st = check_sizes(T, d, E, k, ffn);
     if (st != MK_OK) return st;
+    if (T == 0) return MK_OK;  // empty batch: nothing to read or write
     if (!x || !wg || !w1 || !w3 || !w2 || !y) return MK_ERR_INVALID_ARG;
     if (!aligned16(x) || !aligned16(wg) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(y))
         return MK_ERR_INVALID_ARG;
@@ -317,6 +320,7 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
                             size_t ws_bytes, const mk_moe_opts* opts, void* stream) {
     mk_status st = check_sizes(T, d, E, k, ffn);
     if (st != MK_OK) return st;
+    if (T == 0) return MK_OK;
     if (!x_host || !y_host) return MK_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, d, E, k, ffn);
     if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
