@@ -52,6 +52,23 @@ def load_peaks():
     return p
 
 
+def token_seed(rank: int) -> int:
+    """Seed of a rank's token batch: rank 0 uses the workload seed (0), so its
+    batch is the one the parity tests check; other ranks draw their own."""
+    return 0 if rank == 0 else 1000 + rank
+
+
+def max_over_ranks(value: float, device, dist_on: bool) -> float:
+    """Slowest rank's value (all-reduce MAX); the value itself on one rank."""
+    if not dist_on:
+        return float(value)
+    import torch.distributed as tdist
+
+    t = torch.tensor([value], dtype=torch.float64, device=device)
+    tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
+    return float(t.item())
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -223,7 +240,7 @@ def run_ours(args):
     # Weights are shared (seed 0); each rank draws its own token batch.
     inp = make_inputs(cfg, seed=0, device=dev)
     if rank:
-        inp["x"] = make_inputs(cfg, seed=1000 + rank, device=dev, experts=False)["x"]
+        inp["x"] = make_inputs(cfg, seed=token_seed(rank), device=dev, experts=False)["x"]
     x, wg, bias, w1, w3, w2 = (inp[k] for k in ("x", "wg", "bias", "w1", "w3", "w2"))
     ws = mk.alloc_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, dev)
     y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
@@ -284,10 +301,7 @@ def run_ours(args):
     for p, name in enumerate(mk.PHASES):
         phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(args.steps)) / args.steps
 
-    t = torch.tensor([total_ms], dtype=torch.float64, device=dev)
-    if dist:
-        tdist.all_reduce(t, op=tdist.ReduceOp.MAX)
-    total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, dev, dist)
     ms_per_step = total_ms / args.steps
     value = world * cfg.T / (ms_per_step / 1e3)
 
@@ -306,11 +320,10 @@ def run_ours(args):
         mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream)
     e1.record(stream)
     torch.cuda.synchronize()
-    te = torch.tensor([e0.elapsed_time(e1)], dtype=torch.float64, device=dev)
+    te = max_over_ranks(e0.elapsed_time(e1), dev, dist)
     if dist:
-        tdist.all_reduce(te, op=tdist.ReduceOp.MAX)
         tdist.barrier()
-    e2e_value = world * cfg.T / (float(te.item()) / args.steps / 1e3)
+    e2e_value = world * cfg.T / (te / args.steps / 1e3)
 
     if rank != 0:
         if dist:
