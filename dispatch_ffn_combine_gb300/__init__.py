@@ -34,7 +34,7 @@ PHASES = ("route_logits", "topk", "count", "scan", "scatter", "gemm1", "gemm2", 
 ENTRY_POINTS = (
     "mk_moe_workspace_size", "mk_moe_route", "mk_moe_dispatch", "mk_moe_expert_ffn", "mk_moe_combine",
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
-    "mk_moe_layer_routing",
+    "mk_moe_layer_routing", "mk_moe_route_noalloc",
 )
 
 _lock = threading.Lock()
@@ -77,6 +77,7 @@ def load_library():
         lib.mk_moe_layer_host.argtypes = lib.mk_moe_layer.argtypes
         lib.mk_moe_last_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         lib.mk_moe_layer_routing.argtypes = [P, I64, I, I, I, I, P, P, P, P, P]
+        lib.mk_moe_route_noalloc.argtypes = [P, P, P, I64, I, I, I, P, P, P, P]
         for name in ENTRY_POINTS:
             if name not in ("mk_moe_workspace_size", "mk_moe_status_string"):
                 getattr(lib, name).restype = I
@@ -143,6 +144,26 @@ def mk_moe_route(x, wg, bias, k, topk_ids=None, topk_w=None, expert_counts=None,
     st = load_library().mk_moe_route(_p(x), _p(wg), _p(bias), T, d, E, k, _p(topk_ids), _p(topk_w),
                                      _p(expert_counts), _p(ws), ws.numel(), _stream(stream))
     _check(st, "mk_moe_route")
+    return topk_ids, topk_w, expert_counts
+
+
+def mk_moe_route_noalloc(x, wg, bias, k, topk_ids, topk_w, expert_counts=None, stream=None):
+    """Router for callers that cannot allocate device memory: no workspace, the
+    logits go to a static 8 MiB device array inside the library (T*E <= 2**21).
+    The outputs must be passed in; nothing is allocated by this call."""
+    T, d = x.shape
+    E = wg.shape[0]
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(wg, torch.float32, (E, d), "wg")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    _need(topk_ids, torch.int32, (T, k), "topk_ids")
+    _need(topk_w, torch.float32, (T, k), "topk_w")
+    if expert_counts is not None:
+        _need(expert_counts, torch.int32, (E,), "expert_counts")
+    st = load_library().mk_moe_route_noalloc(_p(x), _p(wg), _p(bias), T, d, E, k, _p(topk_ids), _p(topk_w),
+                                             _p(expert_counts), _stream(stream))
+    _check(st, "mk_moe_route_noalloc")
     return topk_ids, topk_w, expert_counts
 
 

@@ -109,6 +109,21 @@ MK_API mk_status mk_moe_route(const void* x, const float* wg, const float* bias,
                        int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
                        void* ws, size_t ws_bytes, void* stream);
 
+/* The router without a workspace, for callers that cannot allocate device
+ * memory (a runtime with a fixed memory plan, a path that may not call
+ * cudaMalloc, a plug-in handed only its inputs and outputs).  The paper has no
+ * counterpart; this is an addition of this library.  Same arguments, results
+ * and slot order as mk_moe_route, minus ws.  Its fp32 logits live in a static
+ * device array of 8 MiB that the library keeps on every GPU it runs on until
+ * the process exits; T * E above 2,097,152 returns MK_ERR_UNSUPPORTED.  The
+ * first call on a device looks up that array's device address, so make the
+ * first call on each device before any stream capture.  All calls share the
+ * array: calls that overlap on the GPU race.  Allocates nothing. */
+MK_API mk_status mk_moe_route_noalloc(const void* x, const float* wg, const float* bias,
+                                      int64_t T, int d, int E, int k,
+                                      int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
+                                      void* stream);
+
 /* Dispatch: permute token rows into expert-contiguous order (the local form of
  * the README's all-to-all dispatch; paper section 3.1 and Table 3 describe the
  * expert-parallel version that pulls tokens from peers).
