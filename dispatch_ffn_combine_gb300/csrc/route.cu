@@ -11,12 +11,14 @@
 //   + bias[e].
 // A warp owns a 16-token x 8-expert block; lane j carries partial sum s_j of
 // all 128 logits of the block, so the chains need no cross-lane traffic until
-// the end.  The final tree is done as a transpose-reduction: at each level a
+// the end.  The operands reach the warps through a shared-memory pipeline fed
+// by asynchronous copies, and two tokens' chains advance per packed fp32x2 FMA.  The final tree is done as a transpose-reduction: at each level a
 // lane keeps half of its accumulators and adds the partner's matching half,
 // which performs exactly the additions s_j + s_{j+off} of the tree (fp32
 // addition is commutative) with 124 shuffles instead of 640.
 #include <math.h>
 
+#include "mk_device.cuh"
 #include "mk_internal.h"
 
 namespace mk {
@@ -40,51 +42,117 @@ __device__ __forceinline__ void reduce_level(float (&acc)[kAcc], int lane, int o
     }
 }
 
+constexpr int kKC = 128;     // K elements per pipeline stage (4 chain steps per lane)
+constexpr int kStages = 4;   // cp.async pipeline depth
+
 template <int WT, int WE>
-__global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t* __restrict__ x,
-                                                           const float* __restrict__ wg,
-                                                           const float* __restrict__ bias, int T, int d, int E,
-                                                           float* __restrict__ logits) {
+struct RouteTile {
+    static constexpr int CT = kTT * WT;          // tokens per block
+    static constexpr int CE = kTE * WE;          // experts per block
+    static constexpr int XB = CT * kKC * 2;      // bytes of x per stage (bf16)
+    static constexpr int WB = CE * kKC * 4;      // bytes of Wg per stage (fp32)
+    static constexpr int SB = XB + WB;
+    static constexpr int SMEM = kStages * SB;
+};
+
+// Gate logits of a (CT tokens) x (CE experts) block.  x and Wg chunks of 128
+// columns stream through a 4-stage cp.async ring in shared memory; each warp
+// owns a 16 x 8 block of logits, lane j holding partial sum s_j of all 128.
+// The FMAs are packed two tokens at a time (fp32x2 fused multiply-add: each
+// element is one correctly rounded fma, the same bits as a scalar fmaf).
+template <int WT, int WE>
+__global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __restrict__ x,
+                                                              const float* __restrict__ wg,
+                                                              const float* __restrict__ bias, int T, int d, int E,
+                                                              float* __restrict__ logits) {
     static_assert(WT * WE == 8, "8 warps per block");
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
+    using RT = RouteTile<WT, WE>;
+    extern __shared__ __align__(128) uint8_t smem[];
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
     const int wt = warp / WE;
     const int we = warp % WE;
     // 1-D grid, expert groups fastest: the blocks that read the same token rows
     // run together, so x comes from HBM once and from L2 for the other groups.
-    const int n_eg = (E + kTE * WE - 1) / (kTE * WE);
+    const int n_eg = (E + RT::CE - 1) / RT::CE;
     const int eg = static_cast<int>(blockIdx.x % n_eg);
     const int tg = static_cast<int>(blockIdx.x / n_eg);
-    const int t0 = tg * (kTT * WT) + wt * kTT;
-    const int e0 = eg * (kTE * WE) + we * kTE;
-    if (t0 >= T || e0 >= E) return;  // uniform per warp; no block-level barrier below
+    const int ct0 = tg * RT::CT;
+    const int ce0 = eg * RT::CE;
+    const int nk = (d + kKC - 1) / kKC;
 
-    // Element offsets of this lane's first element in each row (rows past the
-    // end are clamped to the last row; their results are not stored).
-    int xo[kTT];
-    int wo[kTE];
+    // Rows past the end are clamped to the last row: loaded, never stored.
+    auto load_stage = [&](int stage, int k0) {
+        uint8_t* sx = smem + stage * RT::SB;
+        uint8_t* sw = sx + RT::XB;
+        const int kc = min(kKC, d - k0);
+        const int xpr = kc / 8;  // 16-byte pieces per x row
+        for (int p = tid; p < RT::CT * xpr; p += 256) {
+            const int r = p / xpr, c = p - (p / xpr) * xpr;
+            const int t = min(ct0 + r, T - 1);
+            cp_async16(sx + r * (kKC * 2) + c * 16, x + static_cast<int64_t>(t) * d + k0 + c * 8);
+        }
+        const int wpr = kc / 4;  // 16-byte pieces per Wg row
+        for (int p = tid; p < RT::CE * wpr; p += 256) {
+            const int r = p / wpr, c = p - (p / wpr) * wpr;
+            const int e = min(ce0 + r, E - 1);
+            cp_async16(sw + r * (kKC * 4) + c * 16, wg + static_cast<int64_t>(e) * d + k0 + c * 4);
+        }
+    };
+
 #pragma unroll
-    for (int a = 0; a < kTT; ++a) xo[a] = min(t0 + a, T - 1) * d + lane;
+    for (int s = 0; s < kStages - 1; ++s) {
+        if (s < nk) load_stage(s, s * kKC);
+        cp_async_commit();
+    }
+
+    float2 acc2[kTT / 2][kTE];  // (token 2a, token 2a+1) x expert b
 #pragma unroll
-    for (int b = 0; b < kTE; ++b) wo[b] = min(e0 + b, E - 1) * d + lane;
+    for (int a = 0; a < kTT / 2; ++a)
+#pragma unroll
+        for (int b = 0; b < kTE; ++b) acc2[a][b] = make_float2(0.0f, 0.0f);
+
+    for (int kc = 0; kc < nk; ++kc) {
+        cp_async_wait<kStages - 2>();
+        __syncthreads();
+        {
+            const int nxt = kc + kStages - 1;
+            if (nxt < nk) load_stage(nxt % kStages, nxt * kKC);
+            cp_async_commit();
+        }
+        const uint8_t* base = smem + (kc % kStages) * RT::SB;
+        const uint16_t* sx = reinterpret_cast<const uint16_t*>(base) + (wt * kTT) * kKC + lane;
+        const float* sw = reinterpret_cast<const float*>(base + RT::XB) + (we * kTE) * kKC + lane;
+        const int steps = min(kKC, d - kc * kKC) / 32;
+#pragma unroll
+        for (int s = 0; s < kKC / 32; ++s) {
+            if (s < steps) {
+                float2 xv[kTT / 2];
+#pragma unroll
+                for (int a = 0; a < kTT / 2; ++a)
+                    xv[a] = make_float2(__uint_as_float(static_cast<uint32_t>(sx[(2 * a) * kKC + 32 * s]) << 16),
+                                        __uint_as_float(static_cast<uint32_t>(sx[(2 * a + 1) * kKC + 32 * s]) << 16));
+#pragma unroll
+                for (int b = 0; b < kTE; ++b) {
+                    const float w = sw[b * kKC + 32 * s];
+                    const float2 w2 = make_float2(w, w);
+#pragma unroll
+                    for (int a = 0; a < kTT / 2; ++a) acc2[a][b] = __ffma2_rn(xv[a], w2, acc2[a][b]);
+                }
+            }
+        }
+    }
+    cp_async_wait<0>();
 
     float acc[kAcc];
 #pragma unroll
-    for (int q = 0; q < kAcc; ++q) acc[q] = 0.0f;
-
-#pragma unroll 2
-    for (int i = 0; i < d; i += 32) {
-        float xv[kTT];
-        float wv[kTE];
+    for (int a = 0; a < kTT / 2; ++a)
 #pragma unroll
-        for (int a = 0; a < kTT; ++a) xv[a] = __uint_as_float(static_cast<uint32_t>(__ldg(x + xo[a] + i)) << 16);
-#pragma unroll
-        for (int b = 0; b < kTE; ++b) wv[b] = __ldg(wg + wo[b] + i);
-#pragma unroll
-        for (int a = 0; a < kTT; ++a)
-#pragma unroll
-            for (int b = 0; b < kTE; ++b) acc[a * kTE + b] = __fmaf_rn(xv[a], wv[b], acc[a * kTE + b]);
-    }
+        for (int b = 0; b < kTE; ++b) {
+            acc[(2 * a) * kTE + b] = acc2[a][b].x;
+            acc[(2 * a + 1) * kTE + b] = acc2[a][b].y;
+        }
 
     // Transpose-reduction over the 32 lanes (see file comment).  After level
     // `off`, lane L holds, in acc[0 .. n/2), the level-`off` sums of partial
@@ -95,11 +163,11 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t* __res
     reduce_level<kAcc / 8>(acc, lane, 4);
     reduce_level<kAcc / 16>(acc, lane, 2);
     reduce_level<kAcc / 32>(acc, lane, 1);
-    const int t = t0 + (lane >> 1);
+    const int t = ct0 + wt * kTT + (lane >> 1);
     if (t < T) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int e = e0 + 4 * (lane & 1) + q;
+            const int e = ce0 + we * kTE + 4 * (lane & 1) + q;
             if (e < E) {
                 float l = acc[q];
                 if (bias != nullptr) l = __fadd_rn(l, __ldg(bias + e));
@@ -107,6 +175,25 @@ __global__ void __launch_bounds__(256) route_logits_kernel(const uint16_t* __res
             }
         }
     }
+}
+
+template <int WT, int WE>
+cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float* bias, int64_t T, int d, int E,
+                                float* logits, cudaStream_t s) {
+    using RT = RouteTile<WT, WE>;
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    if (dev < 64 && !configured[dev]) {
+        err = cudaFuncSetAttribute(route_logits_kernel<WT, WE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   RT::SMEM);
+        if (err != cudaSuccess) return err;
+        configured[dev] = 1;
+    }
+    const unsigned grid = static_cast<unsigned>(((E + RT::CE - 1) / RT::CE) * ((T + RT::CT - 1) / RT::CT));
+    route_logits_kernel<WT, WE><<<grid, 256, RT::SMEM, s>>>(xb, wg, bias, static_cast<int>(T), d, E, logits);
+    return cudaGetLastError();
 }
 
 // One warp per token: k rounds of a warp-wide arg-max (larger logit wins,
@@ -177,19 +264,9 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* logits, cudaStream_t s) {
     const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
-    const int Ti = static_cast<int>(T);
-    dim3 block(256);
-    if (E >= 32) {
-        const unsigned grid = static_cast<unsigned>(((E + 31) / 32) * ((T + 31) / 32));
-        route_logits_kernel<2, 4><<<grid, block, 0, s>>>(xb, wg, bias, Ti, d, E, logits);
-    } else if (E >= 16) {
-        const unsigned grid = static_cast<unsigned>(((E + 15) / 16) * ((T + 63) / 64));
-        route_logits_kernel<4, 2><<<grid, block, 0, s>>>(xb, wg, bias, Ti, d, E, logits);
-    } else {
-        const unsigned grid = static_cast<unsigned>(((E + 7) / 8) * ((T + 127) / 128));
-        route_logits_kernel<8, 1><<<grid, block, 0, s>>>(xb, wg, bias, Ti, d, E, logits);
-    }
-    return cudaGetLastError();
+    if (E >= 32) return launch_logits_shape<2, 4>(xb, wg, bias, T, d, E, logits, s);
+    if (E >= 16) return launch_logits_shape<4, 2>(xb, wg, bias, T, d, E, logits, s);
+    return launch_logits_shape<8, 1>(xb, wg, bias, T, d, E, logits, s);
 }
 
 cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
