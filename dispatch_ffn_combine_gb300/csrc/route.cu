@@ -27,6 +27,8 @@ namespace {
 constexpr int kTT = 16;  // tokens per warp tile
 constexpr int kTE = 8;   // experts per warp tile
 constexpr int kAcc = kTT * kTE;
+constexpr int kKC = 256;     // K elements per pipeline stage (8 chain steps per lane)
+constexpr int kStages = 3;   // cp.async pipeline depth
 
 // One level of the transpose-reduction: lanes L and L^off exchange halves;
 // each adds the partner's copy of the half it keeps.
@@ -42,8 +44,17 @@ __device__ __forceinline__ void reduce_level(float (&acc)[kAcc], int lane, int o
     }
 }
 
-constexpr int kKC = 128;     // K elements per pipeline stage (4 chain steps per lane)
-constexpr int kStages = 4;   // cp.async pipeline depth
+// Lane j's operands of chain step s: x[2a], x[2a+1] (bf16 -> fp32, exact) for
+// the warp's 16 tokens and Wg for its 8 experts, all at column 32*s + j.
+__device__ __forceinline__ void load_operands(const uint16_t* sx, const float* sw, int s, float2 (&xv)[kTT / 2],
+                                              float (&wv)[kTE]) {
+#pragma unroll
+    for (int a = 0; a < kTT / 2; ++a)
+        xv[a] = make_float2(__uint_as_float(static_cast<uint32_t>(sx[(2 * a) * kKC + 32 * s]) << 16),
+                            __uint_as_float(static_cast<uint32_t>(sx[(2 * a + 1) * kKC + 32 * s]) << 16));
+#pragma unroll
+    for (int b = 0; b < kTE; ++b) wv[b] = sw[b * kKC + 32 * s];
+}
 
 template <int WT, int WE>
 struct RouteTile {
@@ -125,20 +136,28 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
         const uint16_t* sx = reinterpret_cast<const uint16_t*>(base) + (wt * kTT) * kKC + lane;
         const float* sw = reinterpret_cast<const float*>(base + RT::XB) + (we * kTE) * kKC + lane;
         const int steps = min(kKC, d - kc * kKC) / 32;
+        // Operands of step s+1 are read from shared memory while the FMAs of
+        // step s run, so the shared-memory latency hides behind the FMA pipe.
+        float2 xv[kTT / 2];
+        float wv[kTE];
+        load_operands(sx, sw, 0, xv, wv);
 #pragma unroll
         for (int s = 0; s < kKC / 32; ++s) {
             if (s < steps) {
-                float2 xv[kTT / 2];
-#pragma unroll
-                for (int a = 0; a < kTT / 2; ++a)
-                    xv[a] = make_float2(__uint_as_float(static_cast<uint32_t>(sx[(2 * a) * kKC + 32 * s]) << 16),
-                                        __uint_as_float(static_cast<uint32_t>(sx[(2 * a + 1) * kKC + 32 * s]) << 16));
+                float2 xn[kTT / 2];
+                float wn[kTE];
+                if (s + 1 < steps) load_operands(sx, sw, s + 1, xn, wn);
 #pragma unroll
                 for (int b = 0; b < kTE; ++b) {
-                    const float w = sw[b * kKC + 32 * s];
-                    const float2 w2 = make_float2(w, w);
+                    const float2 w2 = make_float2(wv[b], wv[b]);
 #pragma unroll
                     for (int a = 0; a < kTT / 2; ++a) acc2[a][b] = __ffma2_rn(xv[a], w2, acc2[a][b]);
+                }
+                if (s + 1 < steps) {
+#pragma unroll
+                    for (int a = 0; a < kTT / 2; ++a) xv[a] = xn[a];
+#pragma unroll
+                    for (int b = 0; b < kTE; ++b) wv[b] = wn[b];
                 }
             }
         }
