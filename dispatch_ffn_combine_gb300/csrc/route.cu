@@ -24,53 +24,51 @@
 namespace mk {
 namespace {
 
-constexpr int kTT = 16;  // tokens per warp tile
-constexpr int kTE = 8;   // experts per warp tile
-constexpr int kAcc = kTT * kTE;
-constexpr int kKC = 256;     // K elements per pipeline stage (8 chain steps per lane)
+constexpr int kTT = 16;      // tokens per warp tile
+constexpr int kTE = 8;       // experts per warp tile
+constexpr int kHP = 64;      // (token, expert) pairs per half-warp: 8 tokens x 8 experts
+constexpr int kKC = 256;     // K elements per pipeline stage (8 chain steps)
 constexpr int kStages = 3;   // cp.async pipeline depth
+constexpr int kXPad = 64;    // bytes of padding per staged x row (bank spread)
 
-// One level of the transpose-reduction: lanes L and L^off exchange halves;
-// each adds the partner's copy of the half it keeps.
+// One level of the transpose-reduction on float2 accumulators: lanes L and
+// L^off (same half-warp) exchange halves of their pair lists; each adds the
+// partner's copy of the half it keeps (fp32 adds, element by element).
 template <int HALF>
-__device__ __forceinline__ void reduce_level(float (&acc)[kAcc], int lane, int off) {
+__device__ __forceinline__ void reduce_level2(float2 (&acc)[kHP], int lane, int off) {
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int q = 0; q < HALF; ++q) {
-        const float send = upper ? acc[q] : acc[q + HALF];
-        const float keep = upper ? acc[q + HALF] : acc[q];
-        const float recv = __shfl_xor_sync(0xffffffffu, send, off);
-        acc[q] = __fadd_rn(keep, recv);
+        const float2 send = upper ? acc[q] : acc[q + HALF];
+        const float2 keep = upper ? acc[q + HALF] : acc[q];
+        float2 recv;
+        recv.x = __shfl_xor_sync(0xffffffffu, send.x, off);
+        recv.y = __shfl_xor_sync(0xffffffffu, send.y, off);
+        acc[q] = make_float2(__fadd_rn(keep.x, recv.x), __fadd_rn(keep.y, recv.y));
     }
-}
-
-// Lane j's operands of chain step s: x[2a], x[2a+1] (bf16 -> fp32, exact) for
-// the warp's 16 tokens and Wg for its 8 experts, all at column 32*s + j.
-__device__ __forceinline__ void load_operands(const uint16_t* sx, const float* sw, int s, float2 (&xv)[kTT / 2],
-                                              float (&wv)[kTE]) {
-#pragma unroll
-    for (int a = 0; a < kTT / 2; ++a)
-        xv[a] = make_float2(__uint_as_float(static_cast<uint32_t>(sx[(2 * a) * kKC + 32 * s]) << 16),
-                            __uint_as_float(static_cast<uint32_t>(sx[(2 * a + 1) * kKC + 32 * s]) << 16));
-#pragma unroll
-    for (int b = 0; b < kTE; ++b) wv[b] = sw[b * kKC + 32 * s];
 }
 
 template <int WT, int WE>
 struct RouteTile {
-    static constexpr int CT = kTT * WT;          // tokens per block
-    static constexpr int CE = kTE * WE;          // experts per block
-    static constexpr int XB = CT * kKC * 2;      // bytes of x per stage (bf16)
-    static constexpr int WB = CE * kKC * 4;      // bytes of Wg per stage (fp32)
+    static constexpr int CT = kTT * WT;               // tokens per block
+    static constexpr int CE = kTE * WE;               // experts per block
+    static constexpr int XROW = kKC * 2 + kXPad;      // bytes per staged x row
+    static constexpr int XB = CT * XROW;              // bytes of x per stage
+    static constexpr int WB = CE * kKC * 4;           // bytes of Wg per stage
     static constexpr int SB = XB + WB;
     static constexpr int SMEM = kStages * SB;
 };
 
-// Gate logits of a (CT tokens) x (CE experts) block.  x and Wg chunks of 128
-// columns stream through a 4-stage cp.async ring in shared memory; each warp
-// owns a 16 x 8 block of logits, lane j holding partial sum s_j of all 128.
-// The FMAs are packed two tokens at a time (fp32x2 fused multiply-add: each
-// element is one correctly rounded fma, the same bits as a scalar fmaf).
+// Gate logits of a (CT tokens) x (CE experts) block.
+//
+// Chain layout: lane L of a warp works in half h = L / 16 with index
+// c = L % 16 and carries the chains of classes 2c and 2c+1 (columns
+// i = 2c + 32m and 2c + 1 + 32m, m = 0, 1, ...) for the half's 64 pairs:
+// tokens 2a + h (a = 0..7) of the warp's 16, times the warp's 8 experts.
+// One 32-bit shared load gives a token's two bf16 columns, one 64-bit load
+// the matching two Wg columns, and one packed fp32x2 FMA advances both chains
+// (each element a correctly rounded fma, the same bits as a scalar fmaf).
+// x and Wg chunks of 256 columns stream through a 3-stage cp.async ring.
 template <int WT, int WE>
 __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __restrict__ x,
                                                               const float* __restrict__ wg,
@@ -82,6 +80,8 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
     const int lane = tid & 31;
+    const int half = lane >> 4;
+    const int c = lane & 15;
     const int wt = warp / WE;
     const int we = warp % WE;
     // 1-D grid, expert groups fastest: the blocks that read the same token rows
@@ -100,15 +100,15 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
         const int kc = min(kKC, d - k0);
         const int xpr = kc / 8;  // 16-byte pieces per x row
         for (int p = tid; p < RT::CT * xpr; p += 256) {
-            const int r = p / xpr, c = p - (p / xpr) * xpr;
+            const int r = p / xpr, q = p - (p / xpr) * xpr;
             const int t = min(ct0 + r, T - 1);
-            cp_async16(sx + r * (kKC * 2) + c * 16, x + static_cast<int64_t>(t) * d + k0 + c * 8);
+            cp_async16(sx + r * RT::XROW + q * 16, x + static_cast<int64_t>(t) * d + k0 + q * 8);
         }
         const int wpr = kc / 4;  // 16-byte pieces per Wg row
         for (int p = tid; p < RT::CE * wpr; p += 256) {
-            const int r = p / wpr, c = p - (p / wpr) * wpr;
+            const int r = p / wpr, q = p - (p / wpr) * wpr;
             const int e = min(ce0 + r, E - 1);
-            cp_async16(sw + r * (kKC * 4) + c * 16, wg + static_cast<int64_t>(e) * d + k0 + c * 4);
+            cp_async16(sw + r * (kKC * 4) + q * 16, wg + static_cast<int64_t>(e) * d + k0 + q * 4);
         }
     };
 
@@ -118,11 +118,9 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
         cp_async_commit();
     }
 
-    float2 acc2[kTT / 2][kTE];  // (token 2a, token 2a+1) x expert b
+    float2 acc[kHP];  // pair p = a * 8 + b: token 2a + half, expert b; (.x, .y) = classes 2c, 2c+1
 #pragma unroll
-    for (int a = 0; a < kTT / 2; ++a)
-#pragma unroll
-        for (int b = 0; b < kTE; ++b) acc2[a][b] = make_float2(0.0f, 0.0f);
+    for (int p = 0; p < kHP; ++p) acc[p] = make_float2(0.0f, 0.0f);
 
     for (int kc = 0; kc < nk; ++kc) {
         cp_async_wait<kStages - 2>();
@@ -133,29 +131,34 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
             cp_async_commit();
         }
         const uint8_t* base = smem + (kc % kStages) * RT::SB;
-        const uint16_t* sx = reinterpret_cast<const uint16_t*>(base) + (wt * kTT) * kKC + lane;
-        const float* sw = reinterpret_cast<const float*>(base + RT::XB) + (we * kTE) * kKC + lane;
+        // this lane's 32-bit word (columns 2c, 2c+1) of token 2a + half of the warp's tile
+        const uint32_t* sx = reinterpret_cast<const uint32_t*>(base + (wt * kTT + half) * RT::XROW) + c;
+        const float2* sw = reinterpret_cast<const float2*>(base + RT::XB + (we * kTE) * (kKC * 4)) + c;
         const int steps = min(kKC, d - kc * kKC) / 32;
-        // Operands of step s+1 are read from shared memory while the FMAs of
-        // step s run, so the shared-memory latency hides behind the FMA pipe.
-        float2 xv[kTT / 2];
-        float wv[kTE];
-        load_operands(sx, sw, 0, xv, wv);
+        uint32_t xw[8];
+        float2 wv[kTE];
+        auto load_ops = [&](int s, uint32_t(&xo)[8], float2(&wo)[kTE]) {
+#pragma unroll
+            for (int a = 0; a < 8; ++a) xo[a] = sx[(2 * a) * (RT::XROW / 4) + 16 * s];
+#pragma unroll
+            for (int b = 0; b < kTE; ++b) wo[b] = sw[b * (kKC / 2) + 16 * s];
+        };
+        load_ops(0, xw, wv);
 #pragma unroll
         for (int s = 0; s < kKC / 32; ++s) {
             if (s < steps) {
-                float2 xn[kTT / 2];
-                float wn[kTE];
-                if (s + 1 < steps) load_operands(sx, sw, s + 1, xn, wn);
+                uint32_t xn[8];
+                float2 wn[kTE];
+                if (s + 1 < steps) load_ops(s + 1, xn, wn);
 #pragma unroll
-                for (int b = 0; b < kTE; ++b) {
-                    const float2 w2 = make_float2(wv[b], wv[b]);
+                for (int a = 0; a < 8; ++a) {
+                    const float2 x2 = make_float2(__uint_as_float(xw[a] << 16), __uint_as_float(xw[a] & 0xffff0000u));
 #pragma unroll
-                    for (int a = 0; a < kTT / 2; ++a) acc2[a][b] = __ffma2_rn(xv[a], w2, acc2[a][b]);
+                    for (int b = 0; b < kTE; ++b) acc[a * kTE + b] = __ffma2_rn(x2, wv[b], acc[a * kTE + b]);
                 }
                 if (s + 1 < steps) {
 #pragma unroll
-                    for (int a = 0; a < kTT / 2; ++a) xv[a] = xn[a];
+                    for (int a = 0; a < 8; ++a) xw[a] = xn[a];
 #pragma unroll
                     for (int b = 0; b < kTE; ++b) wv[b] = wn[b];
                 }
@@ -164,31 +167,21 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
     }
     cp_async_wait<0>();
 
-    float acc[kAcc];
-#pragma unroll
-    for (int a = 0; a < kTT / 2; ++a)
-#pragma unroll
-        for (int b = 0; b < kTE; ++b) {
-            acc[(2 * a) * kTE + b] = acc2[a][b].x;
-            acc[(2 * a + 1) * kTE + b] = acc2[a][b].y;
-        }
-
-    // Transpose-reduction over the 32 lanes (see file comment).  After level
-    // `off`, lane L holds, in acc[0 .. n/2), the level-`off` sums of partial
-    // sum (L mod off) for half of its previous accumulators; after the last
-    // level lane L holds the finished logits of accumulators 4L .. 4L+3.
-    reduce_level<kAcc / 2>(acc, lane, 16);
-    reduce_level<kAcc / 4>(acc, lane, 8);
-    reduce_level<kAcc / 8>(acc, lane, 4);
-    reduce_level<kAcc / 16>(acc, lane, 2);
-    reduce_level<kAcc / 32>(acc, lane, 1);
-    const int t = ct0 + wt * kTT + (lane >> 1);
+    // The fixed tree s_j += s_{j+off}, off = 16, 8, 4, 2 pairs class 2c+b with
+    // class 2(c ^ 8)+b, 2(c ^ 4)+b, ... (the partner lane c ^ 8, ^ 4, ^ 2, ^ 1
+    // of the same half); the last level, off = 1, adds the two classes a lane
+    // holds.  After the four shuffle levels lane c holds pairs 4c .. 4c+3.
+    reduce_level2<kHP / 2>(acc, c, 8);
+    reduce_level2<kHP / 4>(acc, c, 4);
+    reduce_level2<kHP / 8>(acc, c, 2);
+    reduce_level2<kHP / 16>(acc, c, 1);
+    const int t = ct0 + wt * kTT + 2 * (c >> 1) + half;
     if (t < T) {
 #pragma unroll
         for (int q = 0; q < 4; ++q) {
-            const int e = ce0 + we * kTE + 4 * (lane & 1) + q;
+            const int e = ce0 + we * kTE + 4 * (c & 1) + q;
             if (e < E) {
-                float l = acc[q];
+                float l = __fadd_rn(acc[q].x, acc[q].y);
                 if (bias != nullptr) l = __fadd_rn(l, __ldg(bias + e));
                 logits[static_cast<int64_t>(t) * E + e] = l;
             }
