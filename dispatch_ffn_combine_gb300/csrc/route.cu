@@ -276,9 +276,10 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* logits, cudaStream_t s) {
     const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
+    // 32 x 32 blocks when there are enough experts, else 64 tokens x 16 experts
+    // (expert rows past E are clamped duplicates whose logits are not stored).
     if (E >= 32) return launch_logits_shape<2, 4>(xb, wg, bias, T, d, E, logits, s);
-    if (E >= 16) return launch_logits_shape<4, 2>(xb, wg, bias, T, d, E, logits, s);
-    return launch_logits_shape<8, 1>(xb, wg, bias, T, d, E, logits, s);
+    return launch_logits_shape<4, 2>(xb, wg, bias, T, d, E, logits, s);
 }
 
 cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
