@@ -135,33 +135,37 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
         const uint32_t* sx = reinterpret_cast<const uint32_t*>(base + (wt * kTT + half) * RT::XROW) + c;
         const float2* sw = reinterpret_cast<const float2*>(base + RT::XB + (we * kTE) * (kKC * 4)) + c;
         const int steps = min(kKC, d - kc * kKC) / 32;
-        uint32_t xw[8];
-        float2 wv[kTE];
-        auto load_ops = [&](int s, uint32_t(&xo)[8], float2(&wo)[kTE]) {
+        // Operands of step s+1 are read from shared memory and widened to fp32
+        // while the FMAs of step s run (two register sets, used in turn).
+        float2 xa[8], wa[kTE], xb[8], wb[kTE];
+        auto load_ops = [&](int s, float2(&xo)[8], float2(&wo)[kTE]) {
 #pragma unroll
-            for (int a = 0; a < 8; ++a) xo[a] = sx[(2 * a) * (RT::XROW / 4) + 16 * s];
+            for (int a = 0; a < 8; ++a) {
+                const uint32_t v = sx[(2 * a) * (RT::XROW / 4) + 16 * s];
+                xo[a] = make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
+            }
 #pragma unroll
             for (int b = 0; b < kTE; ++b) wo[b] = sw[b * (kKC / 2) + 16 * s];
         };
-        load_ops(0, xw, wv);
+        auto fma_step = [&](const float2(&xo)[8], const float2(&wo)[kTE]) {
 #pragma unroll
-        for (int s = 0; s < kKC / 32; ++s) {
-            if (s < steps) {
-                uint32_t xn[8];
-                float2 wn[kTE];
-                if (s + 1 < steps) load_ops(s + 1, xn, wn);
+            for (int a = 0; a < 8; ++a)
 #pragma unroll
-                for (int a = 0; a < 8; ++a) {
-                    const float2 x2 = make_float2(__uint_as_float(xw[a] << 16), __uint_as_float(xw[a] & 0xffff0000u));
+                for (int b = 0; b < kTE; ++b) acc[a * kTE + b] = __ffma2_rn(xo[a], wo[b], acc[a * kTE + b]);
+        };
+        if (steps == kKC / 32) {  // full chunk: 8 steps, no guards
+            load_ops(0, xa, wa);
 #pragma unroll
-                    for (int b = 0; b < kTE; ++b) acc[a * kTE + b] = __ffma2_rn(x2, wv[b], acc[a * kTE + b]);
-                }
-                if (s + 1 < steps) {
-#pragma unroll
-                    for (int a = 0; a < 8; ++a) xw[a] = xn[a];
-#pragma unroll
-                    for (int b = 0; b < kTE; ++b) wv[b] = wn[b];
-                }
+            for (int s2 = 0; s2 < kKC / 64; ++s2) {
+                load_ops(2 * s2 + 1, xb, wb);
+                fma_step(xa, wa);
+                if (2 * s2 + 2 < kKC / 32) load_ops(2 * s2 + 2, xa, wa);
+                fma_step(xb, wb);
+            }
+        } else {  // last, partial chunk (d not a multiple of 256)
+            for (int s = 0; s < steps; ++s) {
+                load_ops(s, xa, wa);
+                fma_step(xa, wa);
             }
         }
     }
