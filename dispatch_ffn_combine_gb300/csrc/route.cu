@@ -93,11 +93,30 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
     const int ce0 = eg * RT::CE;
     const int nk = (d + kKC - 1) / kKC;
 
-    // Rows past the end are clamped to the last row: loaded, never stored.
+    // Full blocks (every row in range) stream full chunks with a fixed
+    // per-thread progression: x piece (row warp + 8i, 16-byte column lane),
+    // Wg piece (row tid/64 + 4i, column tid%64).  Blocks at the token or expert
+    // edge, and the last partial chunk, use the general loader, which clamps
+    // rows past the end to the last row (loaded, never stored).
+    static_assert(RT::CT % 8 == 0 && (RT::CE * (kKC / 4)) % 256 == 0, "loader shape");
+    const bool full_block = (ct0 + RT::CT <= T) && (ce0 + RT::CE <= E);
+    const uint16_t* xsrc = x + static_cast<int64_t>(ct0 + warp) * d + lane * 8;
+    const int wr = tid / (kKC / 4), wq = tid % (kKC / 4);
+    const float* wsrc = wg + static_cast<int64_t>(ce0 + wr) * d + wq * 4;
     auto load_stage = [&](int stage, int k0) {
         uint8_t* sx = smem + stage * RT::SB;
         uint8_t* sw = sx + RT::XB;
         const int kc = min(kKC, d - k0);
+        if (full_block && kc == kKC) {
+#pragma unroll
+            for (int i = 0; i < RT::CT / 8; ++i)
+                cp_async16(sx + (warp + 8 * i) * RT::XROW + lane * 16, xsrc + static_cast<int64_t>(8 * i) * d + k0);
+#pragma unroll
+            for (int i = 0; i < (RT::CE * (kKC / 4)) / 256; ++i)
+                cp_async16(sw + (wr + (256 / (kKC / 4)) * i) * (kKC * 4) + wq * 16,
+                           wsrc + static_cast<int64_t>((256 / (kKC / 4)) * i) * d + k0);
+            return;
+        }
         const int xpr = kc / 8;  // 16-byte pieces per x row
         for (int p = tid; p < RT::CT * xpr; p += 256) {
             const int r = p / xpr, q = p - (p / xpr) * xpr;
