@@ -24,9 +24,7 @@
 namespace mk {
 namespace {
 
-constexpr int kTT = 16;      // tokens per warp tile
 constexpr int kTE = 8;       // experts per warp tile
-constexpr int kHP = 64;      // (token, expert) pairs per half-warp: 8 tokens x 8 experts
 constexpr int kKC = 256;     // K elements per pipeline stage (8 chain steps)
 constexpr int kStages = 3;   // cp.async pipeline depth
 constexpr int kXPad = 64;    // bytes of padding per staged x row (bank spread)
@@ -34,8 +32,8 @@ constexpr int kXPad = 64;    // bytes of padding per staged x row (bank spread)
 // One level of the transpose-reduction on float2 accumulators: lanes L and
 // L^off (same half-warp) exchange halves of their pair lists; each adds the
 // partner's copy of the half it keeps (fp32 adds, element by element).
-template <int HALF>
-__device__ __forceinline__ void reduce_level2(float2 (&acc)[kHP], int lane, int off) {
+template <int HALF, int NP>
+__device__ __forceinline__ void reduce_level2(float2 (&acc)[NP], int lane, int off) {
     const bool upper = (lane & off) != 0;
 #pragma unroll
     for (int q = 0; q < HALF; ++q) {
@@ -48,8 +46,12 @@ __device__ __forceinline__ void reduce_level2(float2 (&acc)[kHP], int lane, int 
     }
 }
 
-template <int WT, int WE>
+// Block shape: WT x WE warps; each warp owns 2*HT tokens x 8 experts (HT
+// tokens per half-warp).  MINB blocks are meant to share an SM.
+template <int WT, int WE, int HT, int MINB>
 struct RouteTile {
+    static constexpr int kTT = 2 * HT;                // tokens per warp tile
+    static constexpr int kHP = HT * kTE;              // pairs per half-warp
     static constexpr int CT = kTT * WT;               // tokens per block
     static constexpr int CE = kTE * WE;               // experts per block
     static constexpr int XROW = kKC * 2 + kXPad;      // bytes per staged x row
@@ -69,13 +71,15 @@ struct RouteTile {
 // the matching two Wg columns, and one packed fp32x2 FMA advances both chains
 // (each element a correctly rounded fma, the same bits as a scalar fmaf).
 // x and Wg chunks of 256 columns stream through a 3-stage cp.async ring.
-template <int WT, int WE>
-__global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __restrict__ x,
+template <int WT, int WE, int HT, int MINB>
+__global__ void __launch_bounds__(256, MINB) route_logits_kernel(const uint16_t* __restrict__ x,
                                                               const float* __restrict__ wg,
                                                               const float* __restrict__ bias, int T, int d, int E,
                                                               float* __restrict__ logits) {
     static_assert(WT * WE == 8, "8 warps per block");
-    using RT = RouteTile<WT, WE>;
+    using RT = RouteTile<WT, WE, HT, MINB>;
+    constexpr int kTT = RT::kTT;
+    constexpr int kHP = RT::kHP;
     extern __shared__ __align__(128) uint8_t smem[];
     const int tid = threadIdx.x;
     const int warp = tid >> 5;
@@ -156,19 +160,19 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
         const int steps = min(kKC, d - kc * kKC) / 32;
         // Operands of step s+1 are read from shared memory and widened to fp32
         // while the FMAs of step s run (two register sets, used in turn).
-        float2 xa[8], wa[kTE], xb[8], wb[kTE];
-        auto load_ops = [&](int s, float2(&xo)[8], float2(&wo)[kTE]) {
+        float2 xa[HT], wa[kTE], xb[HT], wb[kTE];
+        auto load_ops = [&](int s, float2(&xo)[HT], float2(&wo)[kTE]) {
 #pragma unroll
-            for (int a = 0; a < 8; ++a) {
+            for (int a = 0; a < HT; ++a) {
                 const uint32_t v = sx[(2 * a) * (RT::XROW / 4) + 16 * s];
                 xo[a] = make_float2(__uint_as_float(v << 16), __uint_as_float(v & 0xffff0000u));
             }
 #pragma unroll
             for (int b = 0; b < kTE; ++b) wo[b] = sw[b * (kKC / 2) + 16 * s];
         };
-        auto fma_step = [&](const float2(&xo)[8], const float2(&wo)[kTE]) {
+        auto fma_step = [&](const float2(&xo)[HT], const float2(&wo)[kTE]) {
 #pragma unroll
-            for (int a = 0; a < 8; ++a)
+            for (int a = 0; a < HT; ++a)
 #pragma unroll
                 for (int b = 0; b < kTE; ++b) acc[a * kTE + b] = __ffma2_rn(xo[a], wo[b], acc[a * kTE + b]);
         };
@@ -198,36 +202,36 @@ __global__ void __launch_bounds__(256, 1) route_logits_kernel(const uint16_t* __
     reduce_level2<kHP / 4>(acc, c, 4);
     reduce_level2<kHP / 8>(acc, c, 2);
     reduce_level2<kHP / 16>(acc, c, 1);
-    const int t = ct0 + wt * kTT + 2 * (c >> 1) + half;
-    if (t < T) {
+    constexpr int PPL = kHP / 16;  // pairs per lane after the reduction: PPL*c .. PPL*c + PPL-1
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-            const int e = ce0 + we * kTE + 4 * (c & 1) + q;
-            if (e < E) {
-                float l = __fadd_rn(acc[q].x, acc[q].y);
-                if (bias != nullptr) l = __fadd_rn(l, __ldg(bias + e));
-                logits[static_cast<int64_t>(t) * E + e] = l;
-            }
+    for (int q = 0; q < PPL; ++q) {
+        const int p = PPL * c + q;
+        const int t = ct0 + wt * kTT + 2 * (p / kTE) + half;
+        const int e = ce0 + we * kTE + (p % kTE);
+        if (t < T && e < E) {
+            float l = __fadd_rn(acc[q].x, acc[q].y);
+            if (bias != nullptr) l = __fadd_rn(l, __ldg(bias + e));
+            logits[static_cast<int64_t>(t) * E + e] = l;
         }
     }
 }
 
-template <int WT, int WE>
+template <int WT, int WE, int HT, int MINB>
 cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* logits, cudaStream_t s) {
-    using RT = RouteTile<WT, WE>;
+    using RT = RouteTile<WT, WE, HT, MINB>;
     static int configured[64] = {0};
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     if (dev < 64 && !configured[dev]) {
-        err = cudaFuncSetAttribute(route_logits_kernel<WT, WE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        err = cudaFuncSetAttribute(route_logits_kernel<WT, WE, HT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    RT::SMEM);
         if (err != cudaSuccess) return err;
         configured[dev] = 1;
     }
     const unsigned grid = static_cast<unsigned>(((E + RT::CE - 1) / RT::CE) * ((T + RT::CT - 1) / RT::CT));
-    route_logits_kernel<WT, WE><<<grid, 256, RT::SMEM, s>>>(xb, wg, bias, static_cast<int>(T), d, E, logits);
+    route_logits_kernel<WT, WE, HT, MINB><<<grid, 256, RT::SMEM, s>>>(xb, wg, bias, static_cast<int>(T), d, E, logits);
     return cudaGetLastError();
 }
 
@@ -301,8 +305,8 @@ cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bia
     const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
     // 32 x 32 blocks when there are enough experts, else 64 tokens x 16 experts
     // (expert rows past E are clamped duplicates whose logits are not stored).
-    if (E >= 32) return launch_logits_shape<2, 4>(xb, wg, bias, T, d, E, logits, s);
-    return launch_logits_shape<4, 2>(xb, wg, bias, T, d, E, logits, s);
+    if (E >= 32) return launch_logits_shape<2, 4, 8, 1>(xb, wg, bias, T, d, E, logits, s);
+    return launch_logits_shape<4, 2, 8, 1>(xb, wg, bias, T, d, E, logits, s);
 }
 
 cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
