@@ -259,7 +259,8 @@ def run_ours(args):
 
     def step(i=None):
         mk.mk_moe_layer(x, wg, bias, w1, w3, w2, cfg.k, y=y, ws=ws,
-                        phase_events=None if i is None else ev[i], stream=stream)
+                        phase_events=None if i is None else ev[i], stream=stream, path=args.path,
+                        mover_ctas=args.mover_ctas)
 
     for _ in range(args.warmup):
         step()
@@ -298,8 +299,11 @@ def run_ours(args):
         raise RuntimeError(f"device error in the timed region: {mk.status_string(st)} site {site:#x}")
 
     phase_ms = {}
-    for p, name in enumerate(mk.PHASES):
-        phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(args.steps)) / args.steps
+    if args.path == mk.MK_PATH_FUSED:  # one kernel: event 0 before it, the others after it
+        phase_ms["fused_layer"] = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)) / args.steps
+    else:
+        for p, name in enumerate(mk.PHASES):
+            phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(args.steps)) / args.steps
 
     total_ms = max_over_ranks(total_ms, dev, dist)
     ms_per_step = total_ms / args.steps
@@ -309,7 +313,8 @@ def run_ours(args):
     x_host = x.cpu().pin_memory()
     y_host = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16).pin_memory()
     for _ in range(max(1, args.warmup)):
-        mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream)
+        mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream, path=args.path,
+                             mover_ctas=args.mover_ctas)
     torch.cuda.synchronize()
     if dist:
         tdist.barrier()
@@ -317,7 +322,8 @@ def run_ours(args):
     e1 = torch.cuda.Event(enable_timing=True)
     e0.record(stream)
     for _ in range(args.steps):
-        mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream)
+        mk.mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, cfg.k, y_host, ws, stream=stream, path=args.path,
+                             mover_ctas=args.mover_ctas)
     e1.record(stream)
     torch.cuda.synchronize()
     te = max_over_ranks(e0.elapsed_time(e1), dev, dist)
@@ -333,9 +339,13 @@ def run_ours(args):
     # ---- roofline of the dominant kernel
     _, _, offsets, _ = mk.mk_moe_layer_routing(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
     fb = flops_bytes(cfg, offsets.cpu().numpy())
-    dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
+    if args.path == mk.MK_PATH_FUSED:
+        dom = "fused_layer"
+        work = fb["layer"]
+    else:
+        dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
+        work = fb[dom]
     dom_ms = phase_ms[dom]
-    work = fb[dom]
     ai = work["flops"] / max(work["bytes"], 1)
     tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
     ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
@@ -376,7 +386,9 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
-        "gpu_launches": len(mk.PHASES) * args.steps,
+        "gpu_launches": (1 if args.path == mk.MK_PATH_FUSED else len(mk.PHASES)) * args.steps,
+        "path": "fused persistent kernel" if args.path == mk.MK_PATH_FUSED else "one kernel per step",
+        "mover_ctas": args.mover_ctas,
         "clocks": clk,
         "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},
     }
@@ -394,6 +406,9 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--path", type=int, default=0, help="0: one persistent kernel (default), 1: one kernel per step")
+    ap.add_argument("--mover-ctas", type=int, default=0,
+                    help="fused path: 0 adaptive SM split, n > 0 fixed split with n mover blocks, -1 none")
     args = ap.parse_args()
     if args.warmup < 3 and args.impl == "ours":
         print("note: fewer than 3 warm-up steps", file=sys.stderr)

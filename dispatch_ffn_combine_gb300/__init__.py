@@ -49,10 +49,13 @@ class MoEError(RuntimeError):
 
 class MkMoeOpts(ctypes.Structure):
     _fields_ = [("timeout_ns", ctypes.c_uint64), ("phase_events", ctypes.POINTER(ctypes.c_void_p)),
-                ("inject", ctypes.c_int), ("reserved", ctypes.c_int * 3)]
+                ("inject", ctypes.c_int), ("path", ctypes.c_int), ("mover_ctas", ctypes.c_int),
+                ("reserved", ctypes.c_int)]
 
 
 MK_INJECT_STALL_GEMM1 = 1
+MK_PATH_FUSED = 0
+MK_PATH_STEPS = 1
 
 
 def load_library():
@@ -225,12 +228,14 @@ def mk_moe_combine(P, slot_row, y=None, stream=None):
     return y
 
 
-def _opts(phase_events, timeout_ns, inject=0):
-    if phase_events is None and not timeout_ns and not inject:
+def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_FUSED, mover_ctas=0):
+    if phase_events is None and not timeout_ns and not inject and path == MK_PATH_FUSED and mover_ctas == 0:
         return None
     o = MkMoeOpts()
     o.timeout_ns = int(timeout_ns or 0)
     o.inject = int(inject)
+    o.path = int(path)
+    o.mover_ctas = int(mover_ctas)
     if phase_events is not None:
         if len(phase_events) != len(PHASES) + 1:
             raise ValueError(f"phase_events needs {len(PHASES) + 1} events")
@@ -254,24 +259,29 @@ def _layer_shapes(x, wg, bias, w1, w3, w2, device=True):
 
 
 def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None, timeout_ns=0, stream=None,
-                 inject=0):
-    """The whole layer on device tensors; returns y [T, d] bf16."""
+                 inject=0, path=MK_PATH_FUSED, mover_ctas=0):
+    """The whole layer on device tensors; returns y [T, d] bf16.
+
+    path: MK_PATH_FUSED (one persistent kernel, default) or MK_PATH_STEPS
+    (one kernel per step).  mover_ctas: fused-path SM split, 0 = adaptive."""
     T, d, E, f = _layer_shapes(x, wg, bias, w1, w3, w2)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device) if y is None else y
     ws = alloc_workspace(T, d, E, k, f, x.device) if ws is None else ws
     st = load_library().mk_moe_layer(_p(x), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k, f, _p(y), _p(ws),
-                                     ws.numel(), _opts(phase_events, timeout_ns, inject), _stream(stream))
+                                     ws.numel(), _opts(phase_events, timeout_ns, inject, path, mover_ctas),
+                                     _stream(stream))
     _check(st, "mk_moe_layer")
     return y
 
 
-def mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, k, y_host, ws, phase_events=None, timeout_ns=0, stream=None):
+def mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, k, y_host, ws, phase_events=None, timeout_ns=0, stream=None,
+                      path=MK_PATH_FUSED, mover_ctas=0):
     """The layer on host buffers (pinned for asynchronous copies): x_host in, y_host out."""
     T, d, E, f = _layer_shapes(x_host, wg, bias, w1, w3, w2, device=False)
     _need(y_host, torch.bfloat16, (T, d), "y_host", device=False)
     st = load_library().mk_moe_layer_host(_p(x_host), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k, f,
-                                          _p(y_host), _p(ws), ws.numel(), _opts(phase_events, timeout_ns),
-                                          _stream(stream))
+                                          _p(y_host), _p(ws), ws.numel(),
+                                          _opts(phase_events, timeout_ns, 0, path, mover_ctas), _stream(stream))
     _check(st, "mk_moe_layer_host")
     return y_host
 

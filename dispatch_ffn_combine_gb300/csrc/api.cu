@@ -38,6 +38,7 @@ WsLayout ws_layout(int64_t T, int d, int E, int k, int f) {
     L.x_perm = take(S * d * 2);
     L.h = take(S * f * 2);
     L.P = take(S * d * 2);
+    L.sync = take(fused_sync_bytes(T, E, k));
     L.x_stage = take(static_cast<size_t>(T) * d * 2);
     L.y_stage = take(static_cast<size_t>(T) * d * 2);
     L.total = o;
@@ -252,9 +253,10 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     if (!aligned16(x) || !aligned16(wg) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(y))
         return MK_ERR_INVALID_ARG;
     if (opts != nullptr) {
-        for (int r : opts->reserved)
-            if (r != 0) return MK_ERR_INVALID_ARG;
+        if (opts->reserved != 0) return MK_ERR_INVALID_ARG;
         if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1) return MK_ERR_INVALID_ARG;
+        if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS) return MK_ERR_INVALID_ARG;
+        if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
     }
     const WsLayout L = ws_layout(T, d, E, k, ffn);
     if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
@@ -277,6 +279,45 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     bf16* x_perm = at<bf16>(ws, L.x_perm);
 
     MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    const bool fused = !(opts && (opts->path == MK_PATH_STEPS || opts->inject != 0));
+    if (fused) {
+        FusedArgs fa;
+        fa.x = static_cast<const bf16*>(x);
+        fa.wg = wg;
+        fa.bias = bias;
+        fa.w1 = static_cast<const bf16*>(w1);
+        fa.w3 = static_cast<const bf16*>(w3);
+        fa.w2 = static_cast<const bf16*>(w2);
+        fa.T = T;
+        fa.d = d;
+        fa.E = E;
+        fa.k = k;
+        fa.f = ffn;
+        fa.logits = logits;
+        fa.ids = ids;
+        fa.w = w;
+        fa.chunk_counts = chunk_counts;
+        fa.chunk_base = chunk_base;
+        fa.rank = rank;
+        fa.counts = at<int32_t>(ws, L.counts);
+        fa.offsets = offsets;
+        fa.mtile_start = mtile;
+        fa.row_token = at<int32_t>(ws, L.row_token);
+        fa.row_weight = row_weight;
+        fa.slot_row = slot_row;
+        fa.x_perm = x_perm;
+        fa.h = at<bf16>(ws, L.h);
+        fa.P = at<bf16>(ws, L.P);
+        fa.y = static_cast<bf16*>(y);
+        fa.status = status;
+        fa.sync = at<uint8_t>(ws, L.sync);
+        fa.mover_ctas = opts ? opts->mover_ctas : 0;
+        fa.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+        MK_TRY(pm.mark(0));
+        MK_TRY(launch_fused(fa, s));
+        for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
+        return MK_OK;
+    }
     MK_TRY(pm.mark(MK_PHASE_ROUTE_LOGITS));
     MK_TRY(launch_route_logits(static_cast<const bf16*>(x), wg, bias, T, d, E, logits, s));
     MK_TRY(pm.mark(MK_PHASE_TOPK));

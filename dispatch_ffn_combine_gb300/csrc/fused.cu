@@ -1,0 +1,773 @@
+// fused.cu -- the whole MoE layer as one persistent kernel whose thread blocks
+// take data-movement ("mover") or compute roles.
+//
+// The design follows the mKernel paper ("mKernel: Fast Multi-GPU, Multi-Node
+// Fused Kernels"): a persistent kernel whose blocks are assigned roles (§3,
+// Fig. 2), an on-GPU controller that sets the number of communication blocks
+// to n* = B * Rs*Cs / (Rp*Cp + Rs*Cs) from the remaining tasks R and their
+// measured per-task cycles C (§3.2, Eq. 2), blocks that re-check their role
+// between tasks, compute blocks that help communication while their input is
+// not ready (§3.2), per-chunk counters whose last finisher publishes readiness
+// (§3.1), and readiness flags per tile (§4).  On one GPU the expert-parallel
+// exchanges of the README's "MoE Dispatch + FFN + Combine" row become HBM
+// copies, so the mover role runs the router, the dispatch and the combine.
+//
+// Two task queues, each claimed in order with an atomic ticket:
+//   mover queue:   route blocks (32 tokens x 32 experts of gate logits)
+//                  -> index chunks (row of every (token, slot) of 128 tokens)
+//                  -> copy tasks (the 128 token rows of one expert M-tile)
+//                  -> combine tasks (32 tokens)
+//   compute queue: gemm1 tiles (expert M-tile x 128 h columns)
+//                  -> gemm2 tiles (expert M-tile x 256 output columns)
+// Inline chains (last finisher of a counter does the next step):
+//   last route block of a token group -> top-k of its tokens
+//   last top-k of a 128-token chunk   -> expert histogram + ranks of the chunk
+//   last chunk counted                -> scans (offsets, chunk bases, tiles)
+// Readiness: index tasks need the scans; copy tasks need every index chunk;
+// gemm1 tile (g, n) needs copy task g; gemm2 tile (g, n) needs all gemm1 tiles
+// of g; combine tasks need every gemm2 tile.  Each of the four epilogue warps
+// of a GEMM tile publishes its own 32 rows, so a tile counts 4 when done.  A block claims only tasks whose
+// inputs are ready, so claiming in order never deadlocks; every wait is
+// bounded by %globaltimer and an abort word.
+#include "gemm_impl.cuh"
+#include "layer_tasks.cuh"
+#include "route_impl.cuh"
+
+namespace mk {
+namespace {
+
+using namespace gemm_detail;
+
+constexpr int kThreads = 256;
+constexpr int kInfoSlots = 4;
+constexpr int kCombineTokens = 32;
+
+enum : int { kRoleMover = 0, kRoleCompute = 1 };
+enum : int { kActExit = 0, kActIdle = 1, kActRoute = 2, kActIndex = 3, kActCopy = 4, kActCombine = 5, kActGemm = 6 };
+
+struct TileSlot {
+    int end;
+    int mode;  // 0 gemm1, 1 gemm2
+    int g;     // expert M-tile index
+    int row0;
+    int rows;
+    int n0;
+    int kblocks;
+    int pad;
+};
+
+// Pipeline positions that persist across GEMM sessions; each role keeps its
+// own fields here between sessions (not in registers, which the router's
+// block computation needs in full).
+struct PipeState {
+    uint32_t pr_stage, pr_phase, pr_slot, pr_slot_phase, pr_issued, pr_last_par;
+    uint32_t mm_stage, mm_phase, mm_acc, mm_acc_phase, mm_slot, mm_slot_phase;
+    uint32_t ep_acc, ep_acc_phase, ep_slot, ep_slot_phase;
+    int role;
+    int pad;
+    unsigned long long last_progress;
+    long long t_start;
+};
+
+struct FusedCtl {
+    uint64_t full[STAGES];
+    uint64_t empty[STAGES];
+    uint64_t tmem_full[2];
+    uint64_t tmem_empty[2];
+    uint64_t info_full[kInfoSlots];
+    uint64_t info_empty[kInfoSlots];
+    TileSlot info[kInfoSlots];
+    PipeState ps;
+    uint32_t tmem_base;
+    uint32_t abort_local;
+    uint32_t zero;
+    int action;
+    int arg;
+    int flag;
+};
+
+constexpr size_t kUnionBytes = static_cast<size_t>(STAGES) * STAGE_BYTES;  // >= router stages
+constexpr size_t kFusedSmem = kUnionBytes + sizeof(FusedCtl) + 1024;
+
+struct FusedParams {
+    const bf16* x;
+    const float* wg;
+    const float* bias;
+    int T, d, E, k, f;
+    float* logits;
+    int32_t* ids;
+    float* w;
+    int32_t* chunk_counts;
+    int32_t* chunk_base;
+    int32_t* rank;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* mtile_start;
+    int32_t* row_token;
+    float* row_weight;
+    int32_t* slot_row;
+    bf16* x_perm;
+    bf16* h;
+    bf16* P;
+    bf16* y;
+    uint32_t* status;
+    FusedSync* sync;
+    uint32_t* route_done;  // [n_tg]
+    uint32_t* topk_done;   // [nchunks]
+    uint32_t* copy_done;   // [G_max]
+    uint32_t* h_done;      // [G_max]
+    int n_tg, n_eg, ct, nchunks;
+    int NR, NK;
+    int NT1, NT2, kb1, kb2;
+    int mover_ctas;  // 0 adaptive; > 0 blocks [0, n) prefer mover tasks; < 0 no block prefers them
+    uint64_t timeout_ns;
+};
+
+__device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+__device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
+
+// (expert, M-tile) of expert-M-tile index g: largest e with mtile_start[e] <= g.
+__device__ __forceinline__ void decode_g(const FusedParams& p, int g, int& e, int& row0, int& rows) {
+    int lo = 0, hi = p.E - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (p.mtile_start[mid] <= g)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    e = lo;
+    const int mt = g - p.mtile_start[lo];
+    const int off = p.offsets[lo];
+    row0 = off + mt * BM;
+    rows = min(BM, p.offsets[lo + 1] - off - mt * BM);
+}
+
+struct Claim {
+    int kind;
+    int arg;
+};
+
+// ------------------------------------------------------------------ claiming
+// Run by thread 0 only.  A task is claimed only when its inputs are ready.
+
+__device__ Claim try_claim_mover(const FusedParams& p) {
+    FusedSync* s = p.sync;
+    const uint32_t h = ld_acquire(&s->mover_head);
+    int kind = kActIdle, arg = 0;
+    if (h < static_cast<uint32_t>(p.NR)) {
+        kind = kActRoute;
+        arg = static_cast<int>(h);
+    } else {
+        if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
+        const int G = p.mtile_start[p.E];
+        const uint32_t b_index = p.NR, b_copy = b_index + p.nchunks, b_comb = b_copy + G, total = b_comb + p.NK;
+        if (h >= total) return {kActExit, 0};
+        if (h < b_copy) {
+            kind = kActIndex;
+            arg = static_cast<int>(h - b_index);
+        } else if (h < b_comb) {
+            if (ld_acquire(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0};
+            kind = kActCopy;
+            arg = static_cast<int>(h - b_copy);
+        } else {
+            if (ld_acquire(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0};
+            kind = kActCombine;
+            arg = static_cast<int>(h - b_comb);
+        }
+    }
+    if (atomicCAS(&s->mover_head, h, h + 1) != h) return {kActIdle, 0};
+    return {kind, arg};
+}
+
+__device__ Claim try_claim_compute(const FusedParams& p) {
+    FusedSync* s = p.sync;
+    if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
+    const int G = p.mtile_start[p.E];
+    const uint32_t n1 = static_cast<uint32_t>(G) * p.NT1, total = n1 + static_cast<uint32_t>(G) * p.NT2;
+    const uint32_t h = ld_acquire(&s->compute_head);
+    if (h >= total) return {kActExit, 0};
+    bool ready;
+    if (h < n1)
+        ready = ld_acquire(&p.copy_done[h / p.NT1]) != 0u;
+    else
+        ready = ld_acquire(&p.h_done[(h - n1) / p.NT2]) == static_cast<uint32_t>(4 * p.NT1);
+    if (!ready) return {kActIdle, 0};
+    if (atomicCAS(&s->compute_head, h, h + 1) != h) return {kActIdle, 0};
+    return {kActGemm, static_cast<int>(h)};
+}
+
+// Eq. 2 of the paper: the mover-block target that equalises the predicted
+// finishing times of the two roles.  Before the scans the compute queue is
+// empty and its size unknown, so every block is a mover.
+__device__ int controller_target(const FusedParams& p) {
+    FusedSync* s = p.sync;
+    const int B = static_cast<int>(gridDim.x);
+    if (ld_acquire(&s->scan_done) == 0u) return B;
+    const int G = p.mtile_start[p.E];
+    const double mover_total = static_cast<double>(p.NR) + p.nchunks + G + p.NK;
+    const double compute_total = static_cast<double>(G) * (p.NT1 + p.NT2);
+    const double Rs = fmax(0.0, mover_total - static_cast<double>(ld_acquire(&s->mover_head)));
+    const double Rp = fmax(0.0, compute_total - static_cast<double>(ld_acquire(&s->compute_head)));
+    const unsigned long long cs = atomicAdd(&s->cyc[0], 0ull), cp = atomicAdd(&s->cyc[1], 0ull);
+    const uint32_t ns = ld_acquire(&s->ntask[0]), np = ld_acquire(&s->ntask[1]);
+    const double Cs = ns ? static_cast<double>(cs) / ns : 1.0;
+    const double Cp = np ? static_cast<double>(cp) / np : Cs;
+    const double den = Rp * Cp + Rs * Cs;
+    if (den <= 0.0) return 0;
+    int n = static_cast<int>(B * (Rs * Cs) / den + 0.5);
+    return n < 0 ? 0 : (n > B ? B : n);
+}
+
+__device__ Claim decide(const FusedParams& p, int& role, unsigned long long& last_progress) {
+    FusedSync* s = p.sync;
+    for (;;) {
+        if (ld_acquire(&s->abort_flag) != 0u) return {kActExit, 0};
+        if (p.mover_ctas == 0) {
+            const int target = controller_target(p);
+            atomicExch(&s->target_movers, static_cast<uint32_t>(target));
+            const uint32_t cur = ld_acquire(&s->movers_active);
+            if (role == kRoleCompute && static_cast<int>(cur) < target) {
+                if (atomicCAS(&s->movers_active, cur, cur + 1) == cur) role = kRoleMover;
+            } else if (role == kRoleMover && static_cast<int>(cur) > target) {
+                if (atomicCAS(&s->movers_active, cur, cur - 1) == cur) role = kRoleCompute;
+            }
+        }
+        Claim c1 = (role == kRoleMover) ? try_claim_mover(p) : try_claim_compute(p);
+        if (c1.kind != kActIdle && c1.kind != kActExit) {
+            last_progress = globaltimer_ns();
+            return c1;
+        }
+        // The preferred queue has nothing ready: help the other role.
+        Claim c2 = (role == kRoleMover) ? try_claim_compute(p) : try_claim_mover(p);
+        if (c2.kind != kActIdle && c2.kind != kActExit) {
+            last_progress = globaltimer_ns();
+            return c2;
+        }
+        if (c1.kind == kActExit && c2.kind == kActExit) return {kActExit, 0};
+        if (globaltimer_ns() - last_progress > p.timeout_ns) {
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteFusedIdle);
+            atomicExch(&s->abort_flag, 1u);
+            return {kActExit, 0};
+        }
+        nanosleep_ns(200);
+    }
+}
+
+// Publish a finished task: the block's writes, then a release increment.
+__device__ __forceinline__ void publish_add(uint32_t* word, uint32_t v) {
+    __threadfence();
+    atomicAdd(word, v);
+}
+
+// The router's block computation needs nearly every register of a thread; as
+// a separate (not inlined) function it gets its own allocation, and the
+// persistent kernel's live state is saved around the call instead of being
+// spilled inside its FMA loop.
+template <int WT, int WE>
+__device__ __noinline__ void fused_route_block(uint8_t* smem, const FusedParams& p, int tg, int eg) {
+    route_detail::route_block<WT, WE, 8, 1>(smem, reinterpret_cast<const uint16_t*>(p.x), p.wg, p.bias, p.T, p.d,
+                                             p.E, p.logits, tg, eg);
+}
+
+// ------------------------------------------------------------------ kernel
+
+template <int WT, int WE>
+__global__ void __launch_bounds__(kThreads, 1)
+    fused_layer_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmW1,
+                       const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmA2,
+                       const __grid_constant__ CUtensorMap tmW2, const FusedParams p) {
+    using RT = route_detail::RouteTile<WT, WE, 8, 1>;
+    static_assert(RT::SMEM <= static_cast<int>(kUnionBytes), "router stages fit the shared union");
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    FusedCtl* ctl = reinterpret_cast<FusedCtl*>(smem + kUnionBytes);
+    const int tid = threadIdx.x;
+    const int warp = tid >> 5;
+    const int lane = tid & 31;
+    FusedSync* sync = p.sync;
+
+    if (tid == 0) {
+        for (int i = 0; i < STAGES; ++i) {
+            mbar_init(smem_u32(&ctl->full[i]), 1);
+            mbar_init(smem_u32(&ctl->empty[i]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tmem_full[a]), 1);
+            mbar_init(smem_u32(&ctl->tmem_empty[a]), 4);
+        }
+        for (int i = 0; i < kInfoSlots; ++i) {
+            mbar_init(smem_u32(&ctl->info_full[i]), 1);
+            mbar_init(smem_u32(&ctl->info_empty[i]), 5);  // MMA thread + 4 epilogue warps
+        }
+        ctl->abort_local = 0;
+        ctl->zero = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA1);
+        prefetch_tensormap(&tmW1);
+        prefetch_tensormap(&tmW3);
+        prefetch_tensormap(&tmA2);
+        prefetch_tensormap(&tmW2);
+    }
+    if (warp == 1) {
+        tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile uint32_t* abort_local = &ctl->abort_local;
+    const volatile uint32_t* never = &ctl->zero;
+
+    // Role of this block (thread 0 keeps it).  Adaptive mode starts with every
+    // block a mover: only route tasks exist before the scans.
+    PipeState* ps = &ctl->ps;
+    if (tid == 0) {
+        *ps = PipeState{};
+        int role = kRoleMover;
+        if (p.mover_ctas > 0) role = (static_cast<int>(blockIdx.x) < p.mover_ctas) ? kRoleMover : kRoleCompute;
+        if (p.mover_ctas < 0) role = kRoleCompute;
+        if (p.mover_ctas == 0) atomicAdd(&sync->movers_active, 1u);
+        ps->role = role;
+        ps->last_progress = globaltimer_ns();
+    }
+    __syncthreads();
+
+    for (;;) {
+        if (tid == 0) {
+            int role = ps->role;
+            unsigned long long lp = ps->last_progress;
+            const Claim c = decide(p, role, lp);
+            ps->role = role;
+            ps->last_progress = lp;
+            ctl->action = c.kind;
+            ctl->arg = c.arg;
+            ps->t_start = clock64();
+        }
+        __syncthreads();
+        const int action = ctl->action;
+        const int arg = ctl->arg;
+        __syncthreads();  // everyone has read the action before thread 0 may reuse the slot
+        if (action == kActExit) break;
+
+        if (action == kActRoute) {
+            // ---------------------------------------------- gate logits block
+            const int tg = arg / p.n_eg, eg = arg % p.n_eg;
+            fused_route_block<WT, WE>(smem, p, tg, eg);
+            __syncthreads();
+            if (tid == 0) {
+                __threadfence();
+                const uint32_t old = atomicAdd(&p.route_done[tg], 1u);
+                ctl->flag = (old == static_cast<uint32_t>(p.n_eg - 1)) ? 1 : 0;
+                __threadfence();
+            }
+            __syncthreads();
+            if (ctl->flag) {
+                // last expert group of this token group: top-k of its tokens
+                const int t0 = tg * p.ct;
+                for (int tl = warp; tl < p.ct; tl += kThreads / 32)
+                    if (t0 + tl < p.T) tasks::topk_token(p.logits, t0 + tl, p.E, p.k, p.ids, p.w);
+                __syncthreads();
+                const int c = t0 / kChunkTokens;
+                if (tid == 0) {
+                    const int nt_c = min(kChunkTokens, p.T - c * kChunkTokens);
+                    const int groups = (nt_c + p.ct - 1) / p.ct;
+                    __threadfence();
+                    const uint32_t old = atomicAdd(&p.topk_done[c], 1u);
+                    ctl->flag = (old == static_cast<uint32_t>(groups - 1)) ? 1 : 0;
+                    __threadfence();
+                }
+                __syncthreads();
+                if (ctl->flag) {
+                    // last token group of this chunk: histogram and ranks
+                    tasks::count_chunk(reinterpret_cast<uint32_t*>(smem), p.ids, p.T, p.E, p.k, c, p.chunk_counts,
+                                       p.rank);
+                    __syncthreads();
+                    if (tid == 0) {
+                        __threadfence();
+                        const uint32_t old = atomicAdd(&sync->count_done, 1u);
+                        ctl->flag = (old == static_cast<uint32_t>(p.nchunks - 1)) ? 1 : 0;
+                        __threadfence();
+                    }
+                    __syncthreads();
+                    if (ctl->flag) {
+                        // last chunk counted: the scans, then open the later queues
+                        tasks::scan_all(reinterpret_cast<int32_t*>(smem), p.chunk_counts, p.nchunks, p.E,
+                                        p.chunk_base, p.counts, p.offsets, p.mtile_start);
+                        __syncthreads();
+                        if (tid == 0) {
+                            __threadfence();
+                            atomicExch(&sync->scan_done, 1u);
+                        }
+                    }
+                }
+            }
+        } else if (action == kActIndex) {
+            tasks::index_chunk(p.ids, p.w, p.T, p.E, p.k, arg, p.offsets, p.chunk_base, p.rank, p.row_token,
+                               p.row_weight, p.slot_row);
+            __syncthreads();
+            if (tid == 0) publish_add(&sync->index_done, 1u);
+        } else if (action == kActCopy) {
+            int e, row0, rows;
+            decode_g(p, arg, e, row0, rows);
+            tasks::copy_rows(p.x, p.d, p.row_token, row0, rows, p.x_perm);
+            fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
+            __syncthreads();
+            if (tid == 0) {
+                fence_proxy_async_global();
+                __threadfence();
+                atomicExch(&p.copy_done[arg], 1u);
+            }
+        } else if (action == kActCombine) {
+            const int t0 = arg * kCombineTokens;
+            tasks::combine_tokens(p.P, p.slot_row, t0, min(kCombineTokens, p.T - t0), p.d, p.k, p.y);
+        } else if (action == kActGemm) {
+            // ---------------------------------------------- GEMM session
+            const int G = p.mtile_start[p.E];
+            const int n1 = G * p.NT1;
+            if (warp == 0) {
+                if (lane == 0) {
+                    uint32_t pr_stage = ps->pr_stage, pr_phase = ps->pr_phase, pr_slot = ps->pr_slot,
+                             pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued,
+                             pr_last_par = ps->pr_last_par;
+                    const int role = ps->role;
+                    int tile = arg;
+                    bool ok = true;
+                    int session_tiles = 0;
+                    for (;;) {
+                        TileSlot ts;
+                        ts.end = (tile < 0) ? 1 : 0;
+                        if (tile >= 0) {
+                            ts.mode = tile < n1 ? 0 : 1;
+                            const int local = ts.mode == 0 ? tile : tile - n1;
+                            const int nt_cnt = ts.mode == 0 ? p.NT1 : p.NT2;
+                            ts.g = local / nt_cnt;
+                            int e;
+                            decode_g(p, ts.g, e, ts.row0, ts.rows);
+                            ts.n0 = (local - ts.g * nt_cnt) * (ts.mode == 0 ? MMA_N / 2 : MMA_N);
+                            ts.kblocks = ts.mode == 0 ? p.kb1 : p.kb2;
+                            ts.pad = e;
+                        }
+                        if (!mbar_wait_bounded(smem_u32(&ctl->info_empty[pr_slot]), pr_slot_phase ^ 1u, abort_local,
+                                               p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        ctl->info[pr_slot] = ts;
+                        mbar_arrive(smem_u32(&ctl->info_full[pr_slot]));
+                        if (++pr_slot == kInfoSlots) {
+                            pr_slot = 0;
+                            pr_slot_phase ^= 1u;
+                        }
+                        if (ts.end) break;
+                        ++session_tiles;
+                        fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
+                        const int e = ts.pad;
+                        const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
+                        for (int kb = 0; kb < ts.kblocks; ++kb) {
+                            if (!mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u, abort_local,
+                                                   p.timeout_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            const uint32_t fb = smem_u32(&ctl->full[pr_stage]);
+                            const uint32_t sa = smem_u32(smem + pr_stage * STAGE_BYTES);
+                            const uint32_t sb = sa + A_BYTES;
+                            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                            if (ts.mode == 0) {
+                                tma_load_2d(sa, &tmA1, kb * BK, ts.row0, fb);
+                                tma_load_2d(sb, &tmW1, kb * BK, b_row, fb);
+                                tma_load_2d(sb + B_BYTES / 2, &tmW3, kb * BK, b_row, fb);
+                            } else {
+                                tma_load_2d(sa, &tmA2, kb * BK, ts.row0, fb);
+                                tma_load_2d(sb, &tmW2, kb * BK, b_row, fb);
+                            }
+                            pr_issued |= 1u << pr_stage;
+                            pr_last_par = (pr_last_par & ~(1u << pr_stage)) | (pr_phase << pr_stage);
+                            if (++pr_stage == STAGES) {
+                                pr_stage = 0;
+                                pr_phase ^= 1u;
+                            }
+                        }
+                        if (!ok) break;
+                        // next ready compute tile, unless this block should turn mover
+                        tile = -1;
+                        const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
+                                          static_cast<int>(ld_acquire(&sync->movers_active)) >=
+                                              static_cast<int>(ld_acquire(&sync->target_movers));
+                        if (stay && ld_acquire(&sync->abort_flag) == 0u) {
+                            const Claim c = try_claim_compute(p);
+                            if (c.kind == kActGemm) tile = c.arg;
+                        }
+                    }
+                    if (!ok) {
+                        *abort_local = 1u;
+                        atomicExch(&sync->abort_flag, 1u);
+                        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+                        for (int i = 0; i < STAGES; ++i)
+                            if ((pr_issued >> i) & 1u)
+                                mbar_wait_bounded(smem_u32(&ctl->full[i]), (pr_last_par >> i) & 1u, never,
+                                                  p.timeout_ns);
+                    }
+                    ps->last_progress = globaltimer_ns();
+                    ctl->arg = session_tiles;  // read back by this same thread for the cost estimate
+                    ps->pr_stage = pr_stage;
+                    ps->pr_phase = pr_phase;
+                    ps->pr_slot = pr_slot;
+                    ps->pr_slot_phase = pr_slot_phase;
+                    ps->pr_issued = pr_issued;
+                    ps->pr_last_par = pr_last_par;
+                }
+                __syncwarp();
+            } else if (warp == 1) {
+                if (lane == 0) {
+                    uint32_t mm_stage = ps->mm_stage, mm_phase = ps->mm_phase, mm_acc = ps->mm_acc,
+                             mm_acc_phase = ps->mm_acc_phase, mm_slot = ps->mm_slot, mm_slot_phase = ps->mm_slot_phase;
+                    bool ok = true;
+                    for (;;) {
+                        if (!mbar_wait_bounded(smem_u32(&ctl->info_full[mm_slot]), mm_slot_phase, abort_local,
+                                               p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        const TileSlot ts = ctl->info[mm_slot];
+                        mbar_arrive(smem_u32(&ctl->info_empty[mm_slot]));
+                        if (++mm_slot == kInfoSlots) {
+                            mm_slot = 0;
+                            mm_slot_phase ^= 1u;
+                        }
+                        if (ts.end) break;
+                        if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[mm_acc]), mm_acc_phase ^ 1u, abort_local,
+                                               p.timeout_ns)) {
+                            ok = false;
+                            break;
+                        }
+                        tc_fence_after();
+                        const uint32_t d_tmem = tmem_base + mm_acc * MMA_N;
+                        for (int kb = 0; kb < ts.kblocks; ++kb) {
+                            if (!mbar_wait_bounded(smem_u32(&ctl->full[mm_stage]), mm_phase, abort_local,
+                                                   p.timeout_ns)) {
+                                ok = false;
+                                break;
+                            }
+                            tc_fence_after();
+                            const uint32_t sa = smem_u32(smem + mm_stage * STAGE_BYTES);
+                            const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+                            for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                                mma_bf16_ss(d_tmem, sw128_kmajor_desc(sa + kk * UMMA_K * 2),
+                                            sw128_kmajor_desc(sb + kk * UMMA_K * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
+                            mma_commit(smem_u32(&ctl->empty[mm_stage]));
+                            if (++mm_stage == STAGES) {
+                                mm_stage = 0;
+                                mm_phase ^= 1u;
+                            }
+                        }
+                        if (!ok) break;
+                        mma_commit(smem_u32(&ctl->tmem_full[mm_acc]));
+                        mm_acc ^= 1u;
+                        if (mm_acc == 0) mm_acc_phase ^= 1u;
+                    }
+                    if (!ok) {
+                        *abort_local = 1u;
+                        atomicExch(&sync->abort_flag, 1u);
+                        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+                    }
+                    ps->mm_stage = mm_stage;
+                    ps->mm_phase = mm_phase;
+                    ps->mm_acc = mm_acc;
+                    ps->mm_acc_phase = mm_acc_phase;
+                    ps->mm_slot = mm_slot;
+                    ps->mm_slot_phase = mm_slot_phase;
+                }
+                __syncwarp();
+            } else if (warp >= 2 && warp <= 5) {
+                const int sub = warp & 3;
+                const int row_in_tile = sub * 32 + lane;
+                uint32_t ep_acc = ps->ep_acc, ep_acc_phase = ps->ep_acc_phase, ep_slot = ps->ep_slot,
+                         ep_slot_phase = ps->ep_slot_phase;
+                bool ok = true;
+                for (;;) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->info_full[ep_slot]), ep_slot_phase, abort_local,
+                                           p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const TileSlot ts = ctl->info[ep_slot];
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(smem_u32(&ctl->info_empty[ep_slot]));
+                    if (++ep_slot == kInfoSlots) {
+                        ep_slot = 0;
+                        ep_slot_phase ^= 1u;
+                    }
+                    if (ts.end) break;
+                    if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[ep_acc]), ep_acc_phase, abort_local,
+                                           p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + ep_acc * MMA_N;
+                    const bool row_ok = row_in_tile < ts.rows;
+                    const int64_t r = static_cast<int64_t>(ts.row0) + row_in_tile;
+                    if (ts.mode == 0) {
+                        epilogue_swiglu(tbase, row_ok, p.h + r * p.f, ts.n0, p.f);
+                    } else {
+                        const float wr = row_ok ? p.row_weight[r] : 1.0f;
+                        epilogue_weighted(tbase, row_ok, p.P + r * p.d, ts.n0, p.d, wr);
+                    }
+                    fence_proxy_async_global();  // h is read next by TMA (async proxy)
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) {
+                        mbar_arrive(smem_u32(&ctl->tmem_empty[ep_acc]));
+                        // this warp's 32 rows are stored: publish a quarter of the tile
+                        if (ts.mode == 0)
+                            publish_add(&p.h_done[ts.g], 1u);
+                        else
+                            publish_add(&sync->p_done, 1u);
+                    }
+                    ep_acc ^= 1u;
+                    if (ep_acc == 0) ep_acc_phase ^= 1u;
+                }
+                if (!ok && lane == 0) {
+                    *abort_local = 1u;
+                    atomicExch(&sync->abort_flag, 1u);
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
+                }
+                __syncwarp();
+                if (warp == 2 && lane == 0) {  // the four epilogue warps hold the same positions
+                    ps->ep_acc = ep_acc;
+                    ps->ep_acc_phase = ep_acc_phase;
+                    ps->ep_slot = ep_slot;
+                    ps->ep_slot_phase = ep_slot_phase;
+                }
+            }
+        }
+        __syncthreads();
+        if (tid == 0 && action != kActIdle) {
+            const int r = (action == kActGemm) ? 1 : 0;
+            const uint32_t n = (action == kActGemm) ? static_cast<uint32_t>(max(ctl->arg, 1)) : 1u;
+            atomicAdd(&sync->cyc[r], static_cast<unsigned long long>(clock64() - ps->t_start));
+            atomicAdd(&sync->ntask[r], n);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, TMEM_COLS);
+    }
+}
+
+template <int WT, int WE>
+cudaError_t launch_fused_shape(const FusedArgs& a, const FusedParams& p, const CUtensorMap* maps, cudaStream_t s) {
+    static int configured[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    auto fn = fused_layer_kernel<WT, WE>;
+    if (dev < 64 && !configured[dev]) {
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFusedSmem));
+        if (err != cudaSuccess) return err;
+        configured[dev] = 1;
+    }
+    int per_sm = 0;
+    err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, kFusedSmem);
+    if (err != cudaSuccess) return err;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    const int grid = device_sm_count();  // one block per SM, all co-resident
+    (void)a;
+    void* args[] = {const_cast<CUtensorMap*>(&maps[0]), const_cast<CUtensorMap*>(&maps[1]),
+                    const_cast<CUtensorMap*>(&maps[2]), const_cast<CUtensorMap*>(&maps[3]),
+                    const_cast<CUtensorMap*>(&maps[4]), const_cast<FusedParams*>(&p)};
+    err = cudaLaunchCooperativeKernel(reinterpret_cast<void*>(fn), dim3(grid), dim3(kThreads), args, kFusedSmem, s);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t fused_sync_bytes(int64_t T, int E, int k) {
+    const int64_t n_tg = (T + 31) / 32;  // upper bound over the router block shapes
+    const int64_t nch = num_chunks(T);
+    const int64_t g_max = (T * k + kTileM - 1) / kTileM + E;
+    return sizeof(FusedSync) + 4 * static_cast<size_t>(n_tg + nch + 2 * g_max);
+}
+
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
+    const int64_t T = a.T;
+    const int d = a.d, E = a.E, k = a.k, f = a.f;
+    const int64_t S = T * k;
+    CUtensorMap maps[5];
+    if (!make_map(&maps[0], a.x_perm, d, S, BM) ||
+        !make_map(&maps[1], a.w1, d, static_cast<uint64_t>(E) * f, MMA_N / 2) ||
+        !make_map(&maps[2], a.w3, d, static_cast<uint64_t>(E) * f, MMA_N / 2) || !make_map(&maps[3], a.h, f, S, BM) ||
+        !make_map(&maps[4], a.w2, f, static_cast<uint64_t>(E) * d, MMA_N))
+        return cudaErrorInvalidValue;
+    const bool wide = E >= 32;
+    const int ct = wide ? 32 : 64, ce = wide ? 32 : 16;
+    FusedParams p;
+    p.x = a.x;
+    p.wg = a.wg;
+    p.bias = a.bias;
+    p.T = static_cast<int>(T);
+    p.d = d;
+    p.E = E;
+    p.k = k;
+    p.f = f;
+    p.logits = a.logits;
+    p.ids = a.ids;
+    p.w = a.w;
+    p.chunk_counts = a.chunk_counts;
+    p.chunk_base = a.chunk_base;
+    p.rank = a.rank;
+    p.counts = a.counts;
+    p.offsets = a.offsets;
+    p.mtile_start = a.mtile_start;
+    p.row_token = a.row_token;
+    p.row_weight = a.row_weight;
+    p.slot_row = a.slot_row;
+    p.x_perm = a.x_perm;
+    p.h = a.h;
+    p.P = a.P;
+    p.y = a.y;
+    p.status = a.status;
+    uint8_t* sb = static_cast<uint8_t*>(a.sync);
+    p.sync = reinterpret_cast<FusedSync*>(sb);
+    const int64_t n_tg_max = (T + 31) / 32;
+    const int64_t nch = num_chunks(T);
+    const int64_t g_max = (S + kTileM - 1) / kTileM + E;
+    uint32_t* arr = reinterpret_cast<uint32_t*>(sb + sizeof(FusedSync));
+    p.route_done = arr;
+    p.topk_done = arr + n_tg_max;
+    p.copy_done = p.topk_done + nch;
+    p.h_done = p.copy_done + g_max;
+    p.n_tg = static_cast<int>((T + ct - 1) / ct);
+    p.n_eg = (E + ce - 1) / ce;
+    p.ct = ct;
+    p.nchunks = static_cast<int>(nch);
+    p.NR = p.n_tg * p.n_eg;
+    p.NK = static_cast<int>((T + kCombineTokens - 1) / kCombineTokens);
+    p.NT1 = (f + MMA_N / 2 - 1) / (MMA_N / 2);
+    p.NT2 = (d + MMA_N - 1) / MMA_N;
+    p.kb1 = d / BK;
+    p.kb2 = f / BK;
+    p.mover_ctas = a.mover_ctas;
+    p.timeout_ns = a.timeout_ns;
+    cudaError_t err = cudaMemsetAsync(a.sync, 0, fused_sync_bytes(T, E, k), s);
+    if (err != cudaSuccess) return err;
+    return wide ? launch_fused_shape<2, 4>(a, p, maps, s) : launch_fused_shape<4, 2>(a, p, maps, s);
+}
+
+}  // namespace mk

@@ -25,27 +25,13 @@
 // expert's end are loaded (TMA fills past the tensor end with zeros) but never
 // stored.  Every wait is bounded (see mk_device.cuh): on a timeout the CTA
 // records MK_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM, returns.
-#include "mk_device.cuh"
-#include "mk_internal.h"
-
-#include <cudaTypedefs.h>
-
-#include <mutex>
+#include "gemm_impl.cuh"
 
 namespace mk {
 namespace {
 
-constexpr int BM = 128;
-constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int UMMA_K = 16;
-constexpr int STAGES = 4;
-constexpr int MMA_N = 256;
-constexpr uint32_t A_BYTES = BM * BK * 2;
-constexpr uint32_t B_BYTES = MMA_N * BK * 2;
-constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
-constexpr uint32_t TMEM_COLS = 2 * MMA_N;
-constexpr int NUM_THREADS = 192;
-constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
+using namespace gemm_detail;
+
 
 struct SharedCtl {
     uint64_t full[STAGES];
@@ -105,8 +91,6 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmParams& p) {
     ti.n0 = nt * p.tile_n;
     return ti;
 }
-
-__device__ __forceinline__ float silu_mul(float g, float u) { return (g / (1.0f + expf(-g))) * u; }
 
 template <int MODE>  // 0: gemm1 + SwiGLU, 1: gemm2 + row weight
 __global__ void __launch_bounds__(NUM_THREADS, 1)
@@ -266,48 +250,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int64_t r = static_cast<int64_t>(ti.row0) + row_in_tile;
             bf16* orow = p.out + r * p.out_ld;
             if (MODE == 0) {
-#pragma unroll 1
-                for (int c = 0; c < 128; c += 32) {
-                    uint32_t g[32], u[32];
-                    tmem_ld_32x32b_x32(tbase + c, g);
-                    tmem_ld_32x32b_x32(tbase + 128 + c, u);
-                    tmem_ld_wait();
-                    if (row_ok) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            pk[q] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * q]), __uint_as_float(u[2 * q])),
-                                                silu_mul(__uint_as_float(g[2 * q + 1]), __uint_as_float(u[2 * q + 1])));
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int col = ti.n0 + c + 8 * v;
-                            if (col < p.n_valid)
-                                *reinterpret_cast<uint4*>(orow + col) =
-                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                        }
-                    }
-                }
+                epilogue_swiglu(tbase, row_ok, orow, ti.n0, p.n_valid);
             } else {
                 const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
-#pragma unroll 1
-                for (int c = 0; c < MMA_N; c += 32) {
-                    uint32_t a[32];
-                    tmem_ld_32x32b_x32(tbase + c, a);
-                    tmem_ld_wait();
-                    if (row_ok) {
-                        uint32_t pk[16];
-#pragma unroll
-                        for (int q = 0; q < 16; ++q)
-                            pk[q] = pack_bf16x2(__uint_as_float(a[2 * q]) * wr, __uint_as_float(a[2 * q + 1]) * wr);
-#pragma unroll
-                        for (int v = 0; v < 4; ++v) {
-                            const int col = ti.n0 + c + 8 * v;
-                            if (col < p.n_valid)
-                                *reinterpret_cast<uint4*>(orow + col) =
-                                    make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-                        }
-                    }
-                }
+                epilogue_weighted(tbase, row_ok, orow, ti.n0, p.n_valid, wr);
             }
             tc_fence_before();
             __syncwarp();
@@ -329,33 +275,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 }
 
 // ------------------------------------------------------------------ host side
-
-PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
-    });
-    return fn;
-}
-
-// 2-D bf16 tensor [rows, inner] (row-major), box {64, box_rows}, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
-    auto fn = encode_fn();
-    if (fn == nullptr) return false;
-    const cuuint64_t dims[2] = {inner, rows};
-    const cuuint64_t strides[1] = {inner * 2};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
-    const cuuint32_t estr[2] = {1, 1};
-    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
-              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
-              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
 
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const GemmParams& p,

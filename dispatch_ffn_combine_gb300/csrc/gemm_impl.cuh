@@ -1,0 +1,113 @@
+// gemm_impl.cuh -- pieces of the grouped expert GEMMs shared by the
+// stand-alone GEMM kernels and the fused persistent layer kernel: tile
+// constants, the two fused epilogues (SwiGLU for gemm1, routing weight for
+// gemm2) and the TMA tensor-map encoding.
+#pragma once
+
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "mk_device.cuh"
+#include "mk_internal.h"
+
+namespace mk {
+namespace gemm_detail {
+
+constexpr int BM = 128;
+constexpr int BK = 64;  // one 128-byte swizzle row of bf16
+constexpr int UMMA_K = 16;
+constexpr int STAGES = 4;
+constexpr int MMA_N = 256;
+constexpr uint32_t A_BYTES = BM * BK * 2;
+constexpr uint32_t B_BYTES = MMA_N * BK * 2;
+constexpr uint32_t STAGE_BYTES = A_BYTES + B_BYTES;
+constexpr uint32_t TMEM_COLS = 2 * MMA_N;
+constexpr int NUM_THREADS = 192;
+constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
+
+__device__ __forceinline__ float silu_mul(float g, float u) { return (g / (1.0f + expf(-g))) * u; }
+
+// Epilogue of one 128 x 256 accumulator for the 32 rows of this warp's TMEM
+// lane group.  Every lane of the warp must call (tcgen05.ld is warp-wide);
+// only rows with row_ok store.
+//   gemm1: columns [0,128) are gate, [128,256) up: h = bf16(silu(g) * u)
+//   gemm2: P = bf16(wr * acc)
+__device__ __forceinline__ void epilogue_swiglu(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
+#pragma unroll 1
+    for (int c = 0; c < 128; c += 32) {
+        uint32_t g[32], u[32];
+        tmem_ld_32x32b_x32(tbase + c, g);
+        tmem_ld_32x32b_x32(tbase + 128 + c, u);
+        tmem_ld_wait();
+        if (row_ok) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                pk[q] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * q]), __uint_as_float(u[2 * q])),
+                                    silu_mul(__uint_as_float(g[2 * q + 1]), __uint_as_float(u[2 * q + 1])));
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int col = n0 + c + 8 * v;
+                if (col < n_valid)
+                    *reinterpret_cast<uint4*>(orow + col) =
+                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+    }
+}
+
+__device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
+                                                  float wr) {
+#pragma unroll 1
+    for (int c = 0; c < MMA_N; c += 32) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(tbase + c, a);
+        tmem_ld_wait();
+        if (row_ok) {
+            uint32_t pk[16];
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                pk[q] = pack_bf16x2(__uint_as_float(a[2 * q]) * wr, __uint_as_float(a[2 * q + 1]) * wr);
+#pragma unroll
+            for (int v = 0; v < 4; ++v) {
+                const int col = n0 + c + 8 * v;
+                if (col < n_valid)
+                    *reinterpret_cast<uint4*>(orow + col) =
+                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+    });
+    return fn;
+}
+
+// 2-D bf16 tensor [rows, inner] (row-major), box {64, box_rows}, 128-byte swizzle.
+inline bool make_map(CUtensorMap* m, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+    auto fn = encode_fn();
+    if (fn == nullptr) return false;
+    const cuuint64_t dims[2] = {inner, rows};
+    const cuuint64_t strides[1] = {inner * 2};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(BK), box_rows};
+    const cuuint32_t estr[2] = {1, 1};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace gemm_detail
+}  // namespace mk

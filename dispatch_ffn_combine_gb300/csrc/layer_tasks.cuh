@@ -1,0 +1,237 @@
+// layer_tasks.cuh -- per-task device bodies of the layer's data-movement
+// steps, run by one block of 256 threads: top-k of a token, per-chunk expert
+// histogram and ranks, the scans over chunks and experts, the per-chunk index
+// pass, the expert-major row copy, and the combine of a token range.  The
+// fused persistent kernel strings them together with ready flags; the
+// stand-alone kernels of the unfused path have their own bodies.
+#pragma once
+
+#include <math.h>
+
+#include "mk_device.cuh"
+#include "mk_internal.h"
+
+namespace mk {
+namespace tasks {
+
+constexpr int kThreads = 256;
+
+// Top-k of one token by one warp: k rounds of a warp-wide arg-max (larger
+// logit wins, equal logits go to the lower expert id), then the softmax over
+// the chosen k in fp32.
+__device__ __forceinline__ void topk_token(const float* __restrict__ logits, int64_t t, int E, int k,
+                                           int32_t* __restrict__ ids, float* __restrict__ w) {
+    const int lane = threadIdx.x & 31;
+    constexpr int kNone = 0x7fffffff;
+    float v[kMaxExperts / 32];
+#pragma unroll
+    for (int q = 0; q < kMaxExperts / 32; ++q) {
+        const int e = lane + 32 * q;
+        v[q] = (e < E) ? logits[t * E + e] : 0.0f;
+    }
+    uint32_t taken = 0;
+    float sel_v[kMaxTopK];
+    int sel_i[kMaxTopK];
+#pragma unroll
+    for (int j = 0; j < kMaxTopK; ++j) {
+        if (j >= k) break;
+        float bv = 0.0f;
+        int bi = kNone;
+#pragma unroll
+        for (int q = 0; q < kMaxExperts / 32; ++q) {
+            const int e = lane + 32 * q;
+            if (e < E && !((taken >> q) & 1u) && (bi == kNone || v[q] > bv)) {
+                bv = v[q];
+                bi = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (oi != kNone && (bi == kNone || ov > bv || (ov == bv && oi < bi))) {
+                bv = ov;
+                bi = oi;
+            }
+        }
+        sel_v[j] = bv;
+        sel_i[j] = bi;
+        if ((bi & 31) == lane) taken |= 1u << (bi >> 5);
+    }
+    if (lane == 0) {
+        float ex[kMaxTopK];
+        float z = 0.0f;
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j >= k) break;
+            ex[j] = expf(sel_v[j] - sel_v[0]);
+            z += ex[j];
+        }
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) {
+            if (j >= k) break;
+            ids[t * k + j] = sel_i[j];
+            w[t * k + j] = ex[j] / z;
+        }
+    }
+}
+
+// Expert histogram of one 128-token chunk and each (token, slot)'s rank among
+// the chunk's rows of its expert (ascending token order).  `mask` is
+// kMaxExperts * 4 words of shared memory.  All threads of the block call.
+__device__ __forceinline__ void count_chunk(uint32_t* mask, const int32_t* __restrict__ ids, int64_t T, int E,
+                                            int k, int64_t c, int32_t* __restrict__ chunk_counts,
+                                            int32_t* __restrict__ rank) {
+    const int64_t t_begin = c * kChunkTokens;
+    const int nt = static_cast<int>((T - t_begin < kChunkTokens) ? (T - t_begin) : kChunkTokens);
+    for (int i = threadIdx.x; i < E * (kChunkTokens / 32); i += kThreads) mask[i] = 0u;
+    __syncthreads();
+    for (int q = threadIdx.x; q < nt * k; q += kThreads) {
+        const int tl = q / k;
+        const int e = ids[t_begin * k + q];
+        atomicOr(&mask[e * 4 + (tl >> 5)], 1u << (tl & 31));
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < E; e += kThreads)
+        chunk_counts[c * E + e] =
+            __popc(mask[e * 4]) + __popc(mask[e * 4 + 1]) + __popc(mask[e * 4 + 2]) + __popc(mask[e * 4 + 3]);
+    for (int q = threadIdx.x; q < nt * k; q += kThreads) {
+        const int tl = q / k;
+        const int e = ids[t_begin * k + q];
+        const int wd = tl >> 5;
+        int r = 0;
+        for (int ww = 0; ww < wd; ++ww) r += __popc(mask[e * 4 + ww]);
+        r += __popc(mask[e * 4 + wd] & ((1u << (tl & 31)) - 1u));
+        rank[t_begin * k + q] = r;
+    }
+}
+
+__device__ __forceinline__ int warp_inclusive_scan(int v, int lane) {
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, v, off);
+        if (lane >= off) v += u;
+    }
+    return v;
+}
+
+// Scans after the last chunk is counted: per expert over chunks (chunk bases),
+// then over experts (offsets) and over per-expert 128-row tile counts.
+// `s_counts` is kMaxExperts words of shared memory.  All threads call.
+__device__ __forceinline__ void scan_all(int32_t* s_counts, const int32_t* __restrict__ chunk_counts, int64_t nchunks,
+                                         int E, int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
+                                         int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_start) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    for (int e = warp; e < E; e += kThreads / 32) {
+        int running = 0;
+        for (int64_t c0 = 0; c0 < nchunks; c0 += 32) {
+            const int64_t c = c0 + lane;
+            const int v = (c < nchunks) ? chunk_counts[c * E + e] : 0;
+            const int inc = warp_inclusive_scan(v, lane);
+            if (c < nchunks) chunk_base[c * E + e] = running + inc - v;
+            running += __shfl_sync(0xffffffffu, inc, 31);
+        }
+        if (lane == 0) {
+            s_counts[e] = running;
+            counts[e] = running;
+        }
+    }
+    __syncthreads();
+    if (warp == 0) {
+        int cnt[8], til[8], sum_c = 0, sum_t = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            cnt[i] = (e < E) ? s_counts[e] : 0;
+            til[i] = (cnt[i] + kTileM - 1) / kTileM;
+            sum_c += cnt[i];
+            sum_t += til[i];
+        }
+        const int inc_c = warp_inclusive_scan(sum_c, lane);
+        const int inc_t = warp_inclusive_scan(sum_t, lane);
+        int run_c = inc_c - sum_c, run_t = inc_t - sum_t;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            const int e = lane * 8 + i;
+            if (e < E) {
+                offsets[e] = run_c;
+                mtile_start[e] = run_t;
+            }
+            run_c += cnt[i];
+            run_t += til[i];
+        }
+        if (lane == 31) {
+            offsets[E] = inc_c;
+            mtile_start[E] = inc_t;
+        }
+    }
+}
+
+// Row of every (token, slot) of one chunk, and the row -> token / weight maps.
+__device__ __forceinline__ void index_chunk(const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t T,
+                                            int E, int k, int64_t c, const int32_t* __restrict__ offsets,
+                                            const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ rank,
+                                            int32_t* __restrict__ row_token, float* __restrict__ row_weight,
+                                            int32_t* __restrict__ slot_row) {
+    const int64_t t_begin = c * kChunkTokens;
+    const int nt = static_cast<int>((T - t_begin < kChunkTokens) ? (T - t_begin) : kChunkTokens);
+    for (int q = threadIdx.x; q < nt * k; q += kThreads) {
+        const int64_t tq = t_begin * k + q;
+        const int e = ids[tq];
+        const int64_t r = static_cast<int64_t>(offsets[e]) + chunk_base[c * E + e] + rank[tq];
+        slot_row[tq] = static_cast<int32_t>(r);
+        row_token[r] = static_cast<int32_t>(t_begin + q / k);
+        row_weight[r] = w[tq];
+    }
+}
+
+// Copy rows [row0, row0 + rows) of the expert-contiguous buffer from their
+// source tokens (one 16-byte vector per thread per step).
+__device__ __forceinline__ void copy_rows(const bf16* __restrict__ x, int d, const int32_t* __restrict__ row_token,
+                                          int64_t row0, int rows, bf16* __restrict__ x_perm) {
+    const int n16 = d / 8;
+    const int total = rows * n16;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int rr = i / n16;
+        const int cc = i - rr * n16;
+        const int64_t r = row0 + rr;
+        const int64_t t = row_token[r];
+        reinterpret_cast<uint4*>(x_perm + r * d)[cc] = __ldg(reinterpret_cast<const uint4*>(x + t * d) + cc);
+    }
+}
+
+// y[t] = bf16( sum_j P[slot_row[t, j]] ), j ascending, fp32 sum, for tokens
+// [t0, t0 + nt).
+__device__ __forceinline__ void combine_tokens(const bf16* __restrict__ P, const int32_t* __restrict__ slot_row,
+                                               int64_t t0, int nt, int d, int k, bf16* __restrict__ y) {
+    const int n16 = d / 8;
+    const int total = nt * n16;
+    for (int i = threadIdx.x; i < total; i += kThreads) {
+        const int tt = i / n16;
+        const int cc = i - tt * n16;
+        const int64_t t = t0 + tt;
+        float acc[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+        for (int j = 0; j < k; ++j) {
+            const int64_t r = slot_row[t * k + j];
+            const uint4 v = reinterpret_cast<const uint4*>(P + r * d)[cc];
+            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(wv[q] << 16));
+                acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(wv[q] & 0xffff0000u));
+            }
+        }
+        uint4 o;
+        o.x = pack_bf16x2(acc[0], acc[1]);
+        o.y = pack_bf16x2(acc[2], acc[3]);
+        o.z = pack_bf16x2(acc[4], acc[5]);
+        o.w = pack_bf16x2(acc[6], acc[7]);
+        reinterpret_cast<uint4*>(y + t * d)[cc] = o;
+    }
+}
+
+}  // namespace tasks
+}  // namespace mk

@@ -28,6 +28,7 @@ enum : uint32_t {
     kSiteGemmDrain = 0x400,
     kSiteCountIds = 0x500,
     kSiteCountRepeat = 0x600,
+    kSiteFusedIdle = 0x800,
 };
 
 // Byte offsets of every region of the caller's workspace.  The first 256
@@ -50,6 +51,7 @@ struct WsLayout {
     size_t x_perm = 0;        // bf16  [S, d]
     size_t h = 0;             // bf16  [S, f]
     size_t P = 0;             // bf16  [S, d]
+    size_t sync = 0;          // fused kernel: tickets, counters and ready flags (zeroed per call)
     size_t x_stage = 0;       // bf16  [T, d]  host-buffer entry point: staged input
     size_t y_stage = 0;       // bf16  [T, d]  host-buffer entry point: staged output
     size_t total = 0;
@@ -93,6 +95,56 @@ struct FfnArgs {
     int inject;                  // MK_INJECT_STALL_GEMM1 or 0
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
+
+// Fused persistent kernel: tickets, role accounting and cost sums (followed in
+// the workspace by the per-token-group, per-chunk and per-M-tile counters).
+struct FusedSync {
+    uint32_t mover_head;      // next mover-queue ticket
+    uint32_t compute_head;    // next compute-queue ticket
+    uint32_t movers_active;   // blocks in the mover role (adaptive mode)
+    uint32_t target_movers;   // controller target (Eq. 2)
+    uint32_t count_done;      // chunks counted
+    uint32_t scan_done;       // scans finished (0/1)
+    uint32_t index_done;      // index chunks finished
+    uint32_t p_done;          // gemm2 epilogue quarters finished
+    uint32_t abort_flag;      // set by a block whose bounded wait ran out
+    uint32_t ntask[2];        // finished tasks per role (mover, compute)
+    uint32_t pad;
+    unsigned long long cyc[2];  // summed task cycles per role
+};
+
+struct FusedArgs {
+    const bf16* x;
+    const float* wg;
+    const float* bias;
+    const bf16* w1;
+    const bf16* w3;
+    const bf16* w2;
+    int64_t T;
+    int d, E, k, f;
+    float* logits;
+    int32_t* ids;
+    float* w;
+    int32_t* chunk_counts;
+    int32_t* chunk_base;
+    int32_t* rank;
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* mtile_start;
+    int32_t* row_token;
+    float* row_weight;
+    int32_t* slot_row;
+    bf16* x_perm;
+    bf16* h;
+    bf16* P;
+    bf16* y;
+    uint32_t* status;
+    void* sync;
+    int mover_ctas;   // 0 adaptive; > 0 fixed split; < 0 no block prefers mover tasks
+    uint64_t timeout_ns;
+};
+size_t fused_sync_bytes(int64_t T, int E, int k);
+cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s);
 
 int device_sm_count();      // SMs of the current device (cached per device)

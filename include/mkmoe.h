@@ -76,6 +76,8 @@ enum {
     MK_PHASE_COMBINE = 7,      /* y[t] = sum_j P[slot_row[t,j]] in j order           */
     MK_PHASE_COUNT_ALL = 8
 };
+/* On the fused path the steps overlap inside one kernel: phase_events then
+ * gets event 0 before the kernel and events 1..MK_PHASE_COUNT_ALL after it. */
 
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {
@@ -86,9 +88,20 @@ typedef struct {
     int inject;            /* test hook, 0 = off.  MK_INJECT_STALL_GEMM1: block 0 of the first
                               grouped GEMM announces one shared-memory stage but never loads
                               it, so its consumers' bounded waits run out; the call then
-                              reports MK_ERR_TIMEOUT (no fault, no hang).                    */
-    int reserved[3];       /* must be zero                                                   */
+                              reports MK_ERR_TIMEOUT (no fault, no hang).  Kernel-per-step
+                              path only.                                                     */
+    int path;              /* MK_PATH_FUSED (0, default): one persistent kernel whose blocks
+                              take mover or compute roles; MK_PATH_STEPS (1): one kernel per
+                              step.  Both give bit-identical results.                       */
+    int mover_ctas;        /* fused path: 0 = adaptive split (on-GPU controller, paper
+                              section 3.2 Eq. 2); n > 0 = fixed split, blocks [0, n) prefer
+                              mover tasks; -1 = no block prefers them (compute blocks still
+                              help when their input is not ready)                            */
+    int reserved;          /* must be zero                                                   */
 } mk_moe_opts;
+
+#define MK_PATH_FUSED 0
+#define MK_PATH_STEPS 1
 
 #define MK_INJECT_STALL_GEMM1 1
 

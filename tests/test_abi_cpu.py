@@ -86,7 +86,13 @@ def test_layer_rejects_bad_arguments(lib):
     assert call(wsb=need - 1) == mk.MK_ERR_WORKSPACE
     assert call(T=1 << 28, k=8) == mk.MK_ERR_UNSUPPORTED  # T*k >= 2^31
     opts = mk.MkMoeOpts()
-    opts.reserved[0] = 1
+    opts.reserved = 1
+    assert call(opts=ctypes.pointer(opts)) == mk.MK_ERR_INVALID_ARG
+    opts = mk.MkMoeOpts()
+    opts.path = 5
+    assert call(opts=ctypes.pointer(opts)) == mk.MK_ERR_INVALID_ARG
+    opts = mk.MkMoeOpts()
+    opts.mover_ctas = -2
     assert call(opts=ctypes.pointer(opts)) == mk.MK_ERR_INVALID_ARG
     opts = mk.MkMoeOpts()
     opts.inject = 7
