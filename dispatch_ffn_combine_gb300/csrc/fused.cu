@@ -129,6 +129,18 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
     return v;
 }
 
+__device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long long* p) {
+    unsigned long long v;
+    asm volatile("ld.relaxed.gpu.global.u64 %0, [%1];" : "=l"(v) : "l"(p) : "memory");
+    return v;
+}
+
 __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
@@ -158,35 +170,45 @@ struct Claim {
 };
 
 // ------------------------------------------------------------------ claiming
-// Run by thread 0 only.  A task is claimed only when its inputs are ready.
+// Run by thread 0 only.  A task is claimed only when its inputs are ready:
+// the head ticket's readiness is read with relaxed loads, the ticket taken
+// with a compare-and-swap (retried while the head stays ready), and an
+// acquire fence after a won claim orders the task's reads after the flags.
+
+constexpr int kClaimTries = 64;
 
 __device__ Claim try_claim_mover(const FusedParams& p) {
     FusedSync* s = p.sync;
-    const uint32_t h = ld_acquire(&s->mover_head);
-    int kind = kActIdle, arg = 0;
-    if (h < static_cast<uint32_t>(p.NR)) {
-        kind = kActRoute;
-        arg = static_cast<int>(h);
-    } else {
-        if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
-        const int G = p.mtile_start[p.E];
-        const uint32_t b_index = p.NR, b_copy = b_index + p.nchunks, b_comb = b_copy + G, total = b_comb + p.NK;
-        if (h >= total) return {kActExit, 0};
-        if (h < b_copy) {
-            kind = kActIndex;
-            arg = static_cast<int>(h - b_index);
-        } else if (h < b_comb) {
-            if (ld_acquire(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0};
-            kind = kActCopy;
-            arg = static_cast<int>(h - b_copy);
+    for (int attempt = 0; attempt < kClaimTries; ++attempt) {
+        const uint32_t h = ld_relaxed(&s->mover_head);
+        int kind, arg;
+        if (h < static_cast<uint32_t>(p.NR)) {
+            kind = kActRoute;
+            arg = static_cast<int>(h);
         } else {
-            if (ld_acquire(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0};
-            kind = kActCombine;
-            arg = static_cast<int>(h - b_comb);
+            if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
+            const int G = p.mtile_start[p.E];
+            const uint32_t b_index = p.NR, b_copy = b_index + p.nchunks, b_comb = b_copy + G, total = b_comb + p.NK;
+            if (h >= total) return {kActExit, 0};
+            if (h < b_copy) {
+                kind = kActIndex;
+                arg = static_cast<int>(h - b_index);
+            } else if (h < b_comb) {
+                if (ld_relaxed(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0};
+                kind = kActCopy;
+                arg = static_cast<int>(h - b_copy);
+            } else {
+                if (ld_relaxed(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0};
+                kind = kActCombine;
+                arg = static_cast<int>(h - b_comb);
+            }
+        }
+        if (atomicCAS(&s->mover_head, h, h + 1) == h) {
+            __threadfence();
+            return {kind, arg};
         }
     }
-    if (atomicCAS(&s->mover_head, h, h + 1) != h) return {kActIdle, 0};
-    return {kind, arg};
+    return {kActIdle, 0};
 }
 
 __device__ Claim try_claim_compute(const FusedParams& p) {
@@ -194,16 +216,21 @@ __device__ Claim try_claim_compute(const FusedParams& p) {
     if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
     const int G = p.mtile_start[p.E];
     const uint32_t n1 = static_cast<uint32_t>(G) * p.NT1, total = n1 + static_cast<uint32_t>(G) * p.NT2;
-    const uint32_t h = ld_acquire(&s->compute_head);
-    if (h >= total) return {kActExit, 0};
-    bool ready;
-    if (h < n1)
-        ready = ld_acquire(&p.copy_done[h / p.NT1]) != 0u;
-    else
-        ready = ld_acquire(&p.h_done[(h - n1) / p.NT2]) == static_cast<uint32_t>(4 * p.NT1);
-    if (!ready) return {kActIdle, 0};
-    if (atomicCAS(&s->compute_head, h, h + 1) != h) return {kActIdle, 0};
-    return {kActGemm, static_cast<int>(h)};
+    for (int attempt = 0; attempt < kClaimTries; ++attempt) {
+        const uint32_t h = ld_relaxed(&s->compute_head);
+        if (h >= total) return {kActExit, 0};
+        bool ready;
+        if (h < n1)
+            ready = ld_relaxed(&p.copy_done[h / p.NT1]) != 0u;
+        else
+            ready = ld_relaxed(&p.h_done[(h - n1) / p.NT2]) == static_cast<uint32_t>(4 * p.NT1);
+        if (!ready) return {kActIdle, 0};
+        if (atomicCAS(&s->compute_head, h, h + 1) == h) {
+            __threadfence();
+            return {kActGemm, static_cast<int>(h)};
+        }
+    }
+    return {kActIdle, 0};
 }
 
 // Eq. 2 of the paper: the mover-block target that equalises the predicted
@@ -216,10 +243,10 @@ __device__ int controller_target(const FusedParams& p) {
     const int G = p.mtile_start[p.E];
     const double mover_total = static_cast<double>(p.NR) + p.nchunks + G + p.NK;
     const double compute_total = static_cast<double>(G) * (p.NT1 + p.NT2);
-    const double Rs = fmax(0.0, mover_total - static_cast<double>(ld_acquire(&s->mover_head)));
-    const double Rp = fmax(0.0, compute_total - static_cast<double>(ld_acquire(&s->compute_head)));
-    const unsigned long long cs = atomicAdd(&s->cyc[0], 0ull), cp = atomicAdd(&s->cyc[1], 0ull);
-    const uint32_t ns = ld_acquire(&s->ntask[0]), np = ld_acquire(&s->ntask[1]);
+    const double Rs = fmax(0.0, mover_total - static_cast<double>(ld_relaxed(&s->mover_head)));
+    const double Rp = fmax(0.0, compute_total - static_cast<double>(ld_relaxed(&s->compute_head)));
+    const unsigned long long cs = ld_relaxed64(&s->cyc[0]), cp = ld_relaxed64(&s->cyc[1]);
+    const uint32_t ns = ld_relaxed(&s->ntask[0]), np = ld_relaxed(&s->ntask[1]);
     const double Cs = ns ? static_cast<double>(cs) / ns : 1.0;
     const double Cp = np ? static_cast<double>(cp) / np : Cs;
     const double den = Rp * Cp + Rs * Cs;
@@ -228,14 +255,19 @@ __device__ int controller_target(const FusedParams& p) {
     return n < 0 ? 0 : (n > B ? B : n);
 }
 
+// Thread 0's choice of the next task.  The block's role (adaptive mode) moves
+// toward the controller's published target; the preferred queue is tried
+// first, the other one when nothing preferred is ready (a stalled block helps
+// the other role); with nothing ready anywhere the thread backs off and
+// retries, up to the timeout.
 __device__ Claim decide(const FusedParams& p, int& role, unsigned long long& last_progress) {
     FusedSync* s = p.sync;
+    uint32_t backoff = 64;
     for (;;) {
-        if (ld_acquire(&s->abort_flag) != 0u) return {kActExit, 0};
+        if (ld_relaxed(&s->abort_flag) != 0u) return {kActExit, 0};
         if (p.mover_ctas == 0) {
-            const int target = controller_target(p);
-            atomicExch(&s->target_movers, static_cast<uint32_t>(target));
-            const uint32_t cur = ld_acquire(&s->movers_active);
+            const int target = static_cast<int>(ld_relaxed(&s->target_movers));
+            const uint32_t cur = ld_relaxed(&s->movers_active);
             if (role == kRoleCompute && static_cast<int>(cur) < target) {
                 if (atomicCAS(&s->movers_active, cur, cur + 1) == cur) role = kRoleMover;
             } else if (role == kRoleMover && static_cast<int>(cur) > target) {
@@ -247,7 +279,6 @@ __device__ Claim decide(const FusedParams& p, int& role, unsigned long long& las
             last_progress = globaltimer_ns();
             return c1;
         }
-        // The preferred queue has nothing ready: help the other role.
         Claim c2 = (role == kRoleMover) ? try_claim_compute(p) : try_claim_mover(p);
         if (c2.kind != kActIdle && c2.kind != kActExit) {
             last_progress = globaltimer_ns();
@@ -259,7 +290,8 @@ __device__ Claim decide(const FusedParams& p, int& role, unsigned long long& las
             atomicExch(&s->abort_flag, 1u);
             return {kActExit, 0};
         }
-        nanosleep_ns(200);
+        nanosleep_ns(backoff);
+        backoff = backoff < 2048 ? 2 * backoff : 2048;
     }
 }
 
@@ -337,7 +369,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         int role = kRoleMover;
         if (p.mover_ctas > 0) role = (static_cast<int>(blockIdx.x) < p.mover_ctas) ? kRoleMover : kRoleCompute;
         if (p.mover_ctas < 0) role = kRoleCompute;
-        if (p.mover_ctas == 0) atomicAdd(&sync->movers_active, 1u);
+        if (p.mover_ctas == 0) {
+            atomicAdd(&sync->movers_active, 1u);
+            if (blockIdx.x == 0) atomicExch(&sync->target_movers, gridDim.x);
+        }
         ps->role = role;
         ps->last_progress = globaltimer_ns();
     }
@@ -471,6 +506,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                         }
                         if (ts.end) break;
                         ++session_tiles;
+                        // claim the next ready compute tile now, unless this block should
+                        // turn mover: the claim's latency hides behind this tile's loads
+                        int next = -1;
+                        {
+                            const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
+                                              static_cast<int>(ld_relaxed(&sync->movers_active)) >=
+                                                  static_cast<int>(ld_relaxed(&sync->target_movers));
+                            if (stay && ld_relaxed(&sync->abort_flag) == 0u) {
+                                const Claim c = try_claim_compute(p);
+                                if (c.kind == kActGemm) next = c.arg;
+                            }
+                        }
                         fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
                         const int e = ts.pad;
                         const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
@@ -500,15 +547,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                             }
                         }
                         if (!ok) break;
-                        // next ready compute tile, unless this block should turn mover
-                        tile = -1;
-                        const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
-                                          static_cast<int>(ld_acquire(&sync->movers_active)) >=
-                                              static_cast<int>(ld_acquire(&sync->target_movers));
-                        if (stay && ld_acquire(&sync->abort_flag) == 0u) {
-                            const Claim c = try_claim_compute(p);
-                            if (c.kind == kActGemm) tile = c.arg;
-                        }
+                        tile = next;
                     }
                     if (!ok) {
                         *abort_local = 1u;
@@ -660,6 +699,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             const uint32_t n = (action == kActGemm) ? static_cast<uint32_t>(max(ctl->arg, 1)) : 1u;
             atomicAdd(&sync->cyc[r], static_cast<unsigned long long>(clock64() - ps->t_start));
             atomicAdd(&sync->ntask[r], n);
+            if (p.mover_ctas == 0) {  // Eq. 2 after every finished task
+                const uint32_t target = static_cast<uint32_t>(controller_target(p));
+                if (ld_relaxed(&sync->target_movers) != target) atomicExch(&sync->target_movers, target);
+            }
         }
     }
     tc_fence_before();
