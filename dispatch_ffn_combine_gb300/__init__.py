@@ -34,7 +34,7 @@ PHASES = ("route_logits", "topk", "count", "scan", "scatter", "gemm1", "gemm2", 
 ENTRY_POINTS = (
     "mk_moe_workspace_size", "mk_moe_route", "mk_moe_dispatch", "mk_moe_expert_ffn", "mk_moe_combine",
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
-    "mk_moe_layer_routing", "mk_moe_route_noalloc",
+    "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count",
 )
 
 _lock = threading.Lock()
@@ -50,7 +50,7 @@ class MoEError(RuntimeError):
 class MkMoeOpts(ctypes.Structure):
     _fields_ = [("timeout_ns", ctypes.c_uint64), ("phase_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("inject", ctypes.c_int), ("path", ctypes.c_int), ("mover_ctas", ctypes.c_int),
-                ("reserved", ctypes.c_int)]
+                ("trace_cap", ctypes.c_int), ("trace", ctypes.c_void_p)]
 
 
 MK_INJECT_STALL_GEMM1 = 1
@@ -81,6 +81,7 @@ def load_library():
         lib.mk_moe_last_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         lib.mk_moe_layer_routing.argtypes = [P, I64, I, I, I, I, P, P, P, P, P]
         lib.mk_moe_route_noalloc.argtypes = [P, P, P, I64, I, I, I, P, P, P, P]
+        lib.mk_moe_layer_trace_count.argtypes = [P, I64, I, I, I, I, P, ctypes.POINTER(ctypes.c_uint32)]
         for name in ENTRY_POINTS:
             if name not in ("mk_moe_workspace_size", "mk_moe_status_string"):
                 getattr(lib, name).restype = I
@@ -228,10 +229,16 @@ def mk_moe_combine(P, slot_row, y=None, stream=None):
     return y
 
 
-def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_FUSED, mover_ctas=0):
-    if phase_events is None and not timeout_ns and not inject and path == MK_PATH_FUSED and mover_ctas == 0:
+def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_FUSED, mover_ctas=0, trace=None):
+    if (phase_events is None and not timeout_ns and not inject and path == MK_PATH_FUSED and mover_ctas == 0
+            and trace is None):
         return None
     o = MkMoeOpts()
+    if trace is not None:
+        if trace.dtype != torch.int32 or trace.dim() != 2 or trace.shape[1] != 8 or not trace.is_cuda:
+            raise ValueError("trace must be a CUDA int32 tensor of shape [records, 8]")
+        o.trace = trace.data_ptr()
+        o.trace_cap = trace.shape[0]
     o.timeout_ns = int(timeout_ns or 0)
     o.inject = int(inject)
     o.path = int(path)
@@ -259,7 +266,7 @@ def _layer_shapes(x, wg, bias, w1, w3, w2, device=True):
 
 
 def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None, timeout_ns=0, stream=None,
-                 inject=0, path=MK_PATH_FUSED, mover_ctas=0):
+                 inject=0, path=MK_PATH_FUSED, mover_ctas=0, trace=None):
     """The whole layer on device tensors; returns y [T, d] bf16.
 
     path: MK_PATH_FUSED (one persistent kernel, default) or MK_PATH_STEPS
@@ -268,7 +275,7 @@ def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None,
     y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device) if y is None else y
     ws = alloc_workspace(T, d, E, k, f, x.device) if ws is None else ws
     st = load_library().mk_moe_layer(_p(x), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k, f, _p(y), _p(ws),
-                                     ws.numel(), _opts(phase_events, timeout_ns, inject, path, mover_ctas),
+                                     ws.numel(), _opts(phase_events, timeout_ns, inject, path, mover_ctas, trace),
                                      _stream(stream))
     _check(st, "mk_moe_layer")
     return y
@@ -291,6 +298,17 @@ def mk_moe_last_device_error(ws, stream=None):
     detail = ctypes.c_uint32(0)
     st = load_library().mk_moe_last_device_error(_p(ws), _stream(stream), ctypes.byref(detail))
     return int(st), int(detail.value)
+
+
+def mk_moe_layer_trace_count(ws, T, d, E, k, ffn, stream=None):
+    """Number of task records the last fused layer call on ws wrote (synchronises)."""
+    n = ctypes.c_uint32(0)
+    _check(load_library().mk_moe_layer_trace_count(_p(ws), T, d, E, k, ffn, _stream(stream), ctypes.byref(n)),
+           "mk_moe_layer_trace_count")
+    return int(n.value)
+
+
+TRACE_KINDS = {2: "route", 3: "index", 4: "copy", 5: "combine", 6: "gemm"}
 
 
 def mk_moe_layer_routing(ws, T, d, E, k, ffn, stream=None):

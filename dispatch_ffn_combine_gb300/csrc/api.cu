@@ -253,7 +253,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     if (!aligned16(x) || !aligned16(wg) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(y))
         return MK_ERR_INVALID_ARG;
     if (opts != nullptr) {
-        if (opts->reserved != 0) return MK_ERR_INVALID_ARG;
+        if (opts->trace_cap < 0 || (opts->trace_cap > 0 && opts->trace == nullptr)) return MK_ERR_INVALID_ARG;
         if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1) return MK_ERR_INVALID_ARG;
         if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS) return MK_ERR_INVALID_ARG;
         if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
@@ -312,6 +312,8 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
         fa.status = status;
         fa.sync = at<uint8_t>(ws, L.sync);
         fa.mover_ctas = opts ? opts->mover_ctas : 0;
+        fa.trace = (opts && opts->trace_cap > 0) ? opts->trace : nullptr;
+        fa.trace_cap = (opts && opts->trace) ? opts->trace_cap : 0;
         fa.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
         MK_TRY(pm.mark(0));
         MK_TRY(launch_fused(fa, s));
@@ -386,6 +388,20 @@ mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail) {
     if (cudaMemset(ws, 0, sizeof st) != cudaSuccess) return MK_ERR_CUDA;
     if (detail) *detail = st[1];
     return static_cast<mk_status>(st[0]);
+}
+
+mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int ffn, void* stream,
+                                   uint32_t* count) {
+    if (ws == nullptr) return MK_ERR_WORKSPACE;
+    mk_status st = check_sizes(T, d, E, k, ffn);
+    if (st != MK_OK) return st;
+    if (count == nullptr) return MK_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, ffn);
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MK_ERR_CUDA;
+    FusedSync fs;
+    if (cudaMemcpy(&fs, at<uint8_t>(ws, L.sync), sizeof fs, cudaMemcpyDeviceToHost) != cudaSuccess) return MK_ERR_CUDA;
+    *count = fs.trace_n;
+    return MK_OK;
 }
 
 mk_status mk_moe_layer_routing(const void* ws, int64_t T, int d, int E, int k, int ffn, int32_t* topk_ids,

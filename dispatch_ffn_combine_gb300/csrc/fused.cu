@@ -67,6 +67,7 @@ struct PipeState {
     int pad;
     unsigned long long last_progress;
     long long t_start;
+    unsigned long long g_start;
 };
 
 struct FusedCtl {
@@ -121,6 +122,8 @@ struct FusedParams {
     int NT1, NT2, kb1, kb2;
     int mover_ctas;  // 0 adaptive; > 0 blocks [0, n) prefer mover tasks; < 0 no block prefers them
     uint64_t timeout_ns;
+    uint32_t* trace;
+    int trace_cap;
 };
 
 __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
@@ -388,6 +391,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ctl->action = c.kind;
             ctl->arg = c.arg;
             ps->t_start = clock64();
+            ps->g_start = globaltimer_ns();
         }
         __syncthreads();
         const int action = ctl->action;
@@ -697,6 +701,21 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (tid == 0 && action != kActIdle) {
             const int r = (action == kActGemm) ? 1 : 0;
             const uint32_t n = (action == kActGemm) ? static_cast<uint32_t>(max(ctl->arg, 1)) : 1u;
+            if (p.trace != nullptr) {
+                const uint32_t idx = atomicAdd(&sync->trace_n, 1u);
+                if (idx < static_cast<uint32_t>(p.trace_cap)) {
+                    const unsigned long long g1 = globaltimer_ns();
+                    uint32_t* rec = p.trace + 8ull * idx;
+                    rec[0] = blockIdx.x;
+                    rec[1] = static_cast<uint32_t>(action);
+                    rec[2] = static_cast<uint32_t>(arg);
+                    rec[3] = (action == kActGemm) ? n : 0u;
+                    rec[4] = static_cast<uint32_t>(ps->g_start);
+                    rec[5] = static_cast<uint32_t>(ps->g_start >> 32);
+                    rec[6] = static_cast<uint32_t>(g1);
+                    rec[7] = static_cast<uint32_t>(g1 >> 32);
+                }
+            }
             atomicAdd(&sync->cyc[r], static_cast<unsigned long long>(clock64() - ps->t_start));
             atomicAdd(&sync->ntask[r], n);
             if (p.mover_ctas == 0) {  // Eq. 2 after every finished task
@@ -808,6 +827,8 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     p.kb2 = f / BK;
     p.mover_ctas = a.mover_ctas;
     p.timeout_ns = a.timeout_ns;
+    p.trace = a.trace;
+    p.trace_cap = a.trace_cap;
     cudaError_t err = cudaMemsetAsync(a.sync, 0, fused_sync_bytes(T, E, k), s);
     if (err != cudaSuccess) return err;
     return wide ? launch_fused_shape<2, 4>(a, p, maps, s) : launch_fused_shape<4, 2>(a, p, maps, s);

@@ -109,7 +109,7 @@ struct FusedSync {
     uint32_t p_done;          // gemm2 epilogue quarters finished
     uint32_t abort_flag;      // set by a block whose bounded wait ran out
     uint32_t ntask[2];        // finished tasks per role (mover, compute)
-    uint32_t pad;
+    uint32_t trace_n;         // trace records claimed
     unsigned long long cyc[2];  // summed task cycles per role
 };
 
@@ -142,6 +142,8 @@ struct FusedArgs {
     void* sync;
     int mover_ctas;   // 0 adaptive; > 0 fixed split; < 0 no block prefers mover tasks
     uint64_t timeout_ns;
+    uint32_t* trace;  // optional task trace (8 words per record)
+    int trace_cap;
 };
 size_t fused_sync_bytes(int64_t T, int E, int k);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);

@@ -97,7 +97,13 @@ typedef struct {
                               section 3.2 Eq. 2); n > 0 = fixed split, blocks [0, n) prefer
                               mover tasks; -1 = no block prefers them (compute blocks still
                               help when their input is not ready)                            */
-    int reserved;          /* must be zero                                                   */
+    int trace_cap;         /* fused path: records `trace` can hold (0 = no trace)            */
+    uint32_t* trace;       /* fused path, device buffer of trace_cap * 8 words or NULL: one
+                              record per task {block, kind, arg, tiles, start_lo, start_hi,
+                              end_lo, end_hi} (%globaltimer ns); kinds 2 route, 3 index,
+                              4 copy, 5 combine, 6 GEMM session (tiles = tiles it ran).
+                              min(trace_cap, tasks run) records are written; the task count
+                              is left in the workspace (mk_moe_layer_trace_count).          */
 } mk_moe_opts;
 
 #define MK_PATH_FUSED 0
@@ -199,6 +205,11 @@ MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const fl
  * `ws` (MK_OK if no device error).  *detail (may be NULL) receives the site
  * code of the error. */
 MK_API mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail);
+
+/* Records the last fused mk_moe_layer call on `ws` wrote into its trace buffer
+ * (synchronises `stream`).  Returns MK_ERR_WORKSPACE if ws is NULL. */
+MK_API mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int ffn, void* stream,
+                                          uint32_t* count);
 
 /* Static, human-readable name of a status code. */
 MK_API const char* mk_moe_status_string(mk_status s);

@@ -86,7 +86,7 @@ def test_layer_rejects_bad_arguments(lib):
     assert call(wsb=need - 1) == mk.MK_ERR_WORKSPACE
     assert call(T=1 << 28, k=8) == mk.MK_ERR_UNSUPPORTED  # T*k >= 2^31
     opts = mk.MkMoeOpts()
-    opts.reserved = 1
+    opts.trace_cap = 4  # a record count without a buffer
     assert call(opts=ctypes.pointer(opts)) == mk.MK_ERR_INVALID_ARG
     opts = mk.MkMoeOpts()
     opts.path = 5
