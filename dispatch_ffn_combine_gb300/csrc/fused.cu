@@ -170,6 +170,7 @@ __device__ __forceinline__ void decode_g(const FusedParams& p, int g, int& e, in
 struct Claim {
     int kind;
     int arg;
+    int n;  // compute claims: number of consecutive tiles
 };
 
 // ------------------------------------------------------------------ claiming
@@ -189,51 +190,64 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
             kind = kActRoute;
             arg = static_cast<int>(h);
         } else {
-            if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
+            if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0, 0};
             const int G = p.mtile_start[p.E];
             const uint32_t b_index = p.NR, b_copy = b_index + p.nchunks, b_comb = b_copy + G, total = b_comb + p.NK;
-            if (h >= total) return {kActExit, 0};
+            if (h >= total) return {kActExit, 0, 0};
             if (h < b_copy) {
                 kind = kActIndex;
                 arg = static_cast<int>(h - b_index);
             } else if (h < b_comb) {
-                if (ld_relaxed(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0};
+                if (ld_relaxed(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0, 0};
                 kind = kActCopy;
                 arg = static_cast<int>(h - b_copy);
             } else {
-                if (ld_relaxed(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0};
+                if (ld_relaxed(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0, 0};
                 kind = kActCombine;
                 arg = static_cast<int>(h - b_comb);
             }
         }
         if (atomicCAS(&s->mover_head, h, h + 1) == h) {
             __threadfence();
-            return {kind, arg};
+            return {kind, arg, 1};
         }
     }
-    return {kActIdle, 0};
+    return {kActIdle, 0, 0};
 }
+
+// Compute tiles are claimed in runs of up to kBatch tiles of one expert M-tile
+// (they share their readiness), which cuts the number of compare-and-swaps on
+// the queue head and keeps a block's GEMM session going.  Claim.arg is the
+// first ticket, Claim.n the run length.
+constexpr int kBatch = 4;
 
 __device__ Claim try_claim_compute(const FusedParams& p) {
     FusedSync* s = p.sync;
-    if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0};
+    if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0, 0};
     const int G = p.mtile_start[p.E];
     const uint32_t n1 = static_cast<uint32_t>(G) * p.NT1, total = n1 + static_cast<uint32_t>(G) * p.NT2;
     for (int attempt = 0; attempt < kClaimTries; ++attempt) {
         const uint32_t h = ld_relaxed(&s->compute_head);
-        if (h >= total) return {kActExit, 0};
+        if (h >= total) return {kActExit, 0, 0};
         bool ready;
-        if (h < n1)
-            ready = ld_relaxed(&p.copy_done[h / p.NT1]) != 0u;
-        else
-            ready = ld_relaxed(&p.h_done[(h - n1) / p.NT2]) == static_cast<uint32_t>(4 * p.NT1);
-        if (!ready) return {kActIdle, 0};
-        if (atomicCAS(&s->compute_head, h, h + 1) == h) {
+        uint32_t run_end;  // end of this expert M-tile's tiles
+        if (h < n1) {
+            const uint32_t g = h / p.NT1;
+            ready = ld_relaxed(&p.copy_done[g]) != 0u;
+            run_end = (g + 1) * p.NT1;
+        } else {
+            const uint32_t g = (h - n1) / p.NT2;
+            ready = ld_relaxed(&p.h_done[g]) == static_cast<uint32_t>(4 * p.NT1);
+            run_end = n1 + (g + 1) * p.NT2;
+        }
+        if (!ready) return {kActIdle, 0, 0};
+        const uint32_t n = min(static_cast<uint32_t>(kBatch), run_end - h);
+        if (atomicCAS(&s->compute_head, h, h + n) == h) {
             __threadfence();
-            return {kActGemm, static_cast<int>(h)};
+            return {kActGemm, static_cast<int>(h), static_cast<int>(n)};
         }
     }
-    return {kActIdle, 0};
+    return {kActIdle, 0, 0};
 }
 
 // Eq. 2 of the paper: the mover-block target that equalises the predicted
@@ -267,7 +281,7 @@ __device__ Claim decide(const FusedParams& p, int& role, unsigned long long& las
     FusedSync* s = p.sync;
     uint32_t backoff = 64;
     for (;;) {
-        if (ld_relaxed(&s->abort_flag) != 0u) return {kActExit, 0};
+        if (ld_relaxed(&s->abort_flag) != 0u) return {kActExit, 0, 0};
         if (p.mover_ctas == 0) {
             const int target = static_cast<int>(ld_relaxed(&s->target_movers));
             const uint32_t cur = ld_relaxed(&s->movers_active);
@@ -287,21 +301,21 @@ __device__ Claim decide(const FusedParams& p, int& role, unsigned long long& las
             last_progress = globaltimer_ns();
             return c2;
         }
-        if (c1.kind == kActExit && c2.kind == kActExit) return {kActExit, 0};
+        if (c1.kind == kActExit && c2.kind == kActExit) return {kActExit, 0, 0};
         if (globaltimer_ns() - last_progress > p.timeout_ns) {
             report_error(p.status, MK_ERR_TIMEOUT, kSiteFusedIdle);
             atomicExch(&s->abort_flag, 1u);
-            return {kActExit, 0};
+            return {kActExit, 0, 0};
         }
         nanosleep_ns(backoff);
         backoff = backoff < 2048 ? 2 * backoff : 2048;
     }
 }
 
-// Publish a finished task: the block's writes, then a release increment.
+// Publish a finished task: a release increment (orders every write of this
+// thread, and those ordered before it by a block or warp barrier, before it).
 __device__ __forceinline__ void publish_add(uint32_t* word, uint32_t v) {
-    __threadfence();
-    atomicAdd(word, v);
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(word), "r"(v) : "memory");
 }
 
 // The router's block computation needs nearly every register of a thread; as
@@ -312,6 +326,272 @@ template <int WT, int WE>
 __device__ __noinline__ void fused_route_block(uint8_t* smem, const FusedParams& p, int tg, int eg) {
     route_detail::route_block<WT, WE, 8, 1>(smem, reinterpret_cast<const uint16_t*>(p.x), p.wg, p.bias, p.T, p.d,
                                              p.E, p.logits, tg, eg);
+}
+
+// The copy and combine bodies keep many loads in flight; separate functions
+// keep their registers out of the persistent kernel's allocation too.
+__device__ __noinline__ void fused_copy(const FusedParams& p, int64_t row0, int rows) {
+    tasks::copy_rows(p.x, p.d, p.row_token, row0, rows, p.x_perm);
+}
+
+__device__ __noinline__ void fused_combine(const FusedParams& p, int64_t t0, int nt) {
+    tasks::combine_tokens(p.P, p.slot_row, t0, nt, p.d, p.k, p.y);
+}
+
+// ------------------------------------------------------------------ GEMM roles
+// The three roles of a GEMM session, each a separate function (own register
+// allocation).  `tile` / `run` are the first claimed tile and the length of
+// its claimed run; pipeline positions live in ctl->ps between sessions.
+
+struct GemmMaps {
+    const CUtensorMap* a1;
+    const CUtensorMap* w1;
+    const CUtensorMap* w3;
+    const CUtensorMap* a2;
+    const CUtensorMap* w2;
+};
+
+__device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps& m, FusedCtl* ctl, uint8_t* smem,
+                                           int arg, int arg_n) {
+    FusedSync* sync = p.sync;
+    PipeState* ps = &ctl->ps;
+    volatile uint32_t* abort_local = &ctl->abort_local;
+    const volatile uint32_t* never = &ctl->zero;
+    const int G = p.mtile_start[p.E];
+    const int n1 = G * p.NT1;
+    uint32_t pr_stage = ps->pr_stage, pr_phase = ps->pr_phase, pr_slot = ps->pr_slot,
+             pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued,
+             pr_last_par = ps->pr_last_par;
+    const int role = ps->role;
+    int tile = arg;
+    int run_left = arg_n;  // tiles left in the claimed run, this one included
+    bool ok = true;
+    int session_tiles = 0;
+    for (;;) {
+        TileSlot ts;
+        ts.end = (tile < 0) ? 1 : 0;
+        if (tile >= 0) {
+            ts.mode = tile < n1 ? 0 : 1;
+            const int local = ts.mode == 0 ? tile : tile - n1;
+            const int nt_cnt = ts.mode == 0 ? p.NT1 : p.NT2;
+            ts.g = local / nt_cnt;
+            int e;
+            decode_g(p, ts.g, e, ts.row0, ts.rows);
+            ts.n0 = (local - ts.g * nt_cnt) * (ts.mode == 0 ? MMA_N / 2 : MMA_N);
+            ts.kblocks = ts.mode == 0 ? p.kb1 : p.kb2;
+            ts.pad = e;
+        }
+        if (!mbar_wait_bounded(smem_u32(&ctl->info_empty[pr_slot]), pr_slot_phase ^ 1u, abort_local,
+                               p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        ctl->info[pr_slot] = ts;
+        mbar_arrive(smem_u32(&ctl->info_full[pr_slot]));
+        if (++pr_slot == kInfoSlots) {
+            pr_slot = 0;
+            pr_slot_phase ^= 1u;
+        }
+        if (ts.end) break;
+        ++session_tiles;
+        // next tile: the rest of the claimed run, else claim a new run now
+        // (unless this block should turn mover); the claim's latency
+        // hides behind this tile's loads
+        int next = -1;
+        if (run_left > 1) {
+            next = tile + 1;
+            --run_left;
+        } else {
+            const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
+                              static_cast<int>(ld_relaxed(&sync->movers_active)) >=
+                                  static_cast<int>(ld_relaxed(&sync->target_movers));
+            if (stay && ld_relaxed(&sync->abort_flag) == 0u) {
+                const Claim c = try_claim_compute(p);
+                if (c.kind == kActGemm) {
+                    next = c.arg;
+                    run_left = c.n;
+                }
+            }
+        }
+        fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
+        const int e = ts.pad;
+        const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
+        for (int kb = 0; kb < ts.kblocks; ++kb) {
+            if (!mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u, abort_local,
+                                   p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            const uint32_t fb = smem_u32(&ctl->full[pr_stage]);
+            const uint32_t sa = smem_u32(smem + pr_stage * STAGE_BYTES);
+            const uint32_t sb = sa + A_BYTES;
+            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            if (ts.mode == 0) {
+                tma_load_2d(sa, m.a1, kb * BK, ts.row0, fb);
+                tma_load_2d(sb, m.w1, kb * BK, b_row, fb);
+                tma_load_2d(sb + B_BYTES / 2, m.w3, kb * BK, b_row, fb);
+            } else {
+                tma_load_2d(sa, m.a2, kb * BK, ts.row0, fb);
+                tma_load_2d(sb, m.w2, kb * BK, b_row, fb);
+            }
+            pr_issued |= 1u << pr_stage;
+            pr_last_par = (pr_last_par & ~(1u << pr_stage)) | (pr_phase << pr_stage);
+            if (++pr_stage == STAGES) {
+                pr_stage = 0;
+                pr_phase ^= 1u;
+            }
+        }
+        if (!ok) break;
+        tile = next;
+    }
+    if (!ok) {
+        *abort_local = 1u;
+        atomicExch(&sync->abort_flag, 1u);
+        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+        for (int i = 0; i < STAGES; ++i)
+            if ((pr_issued >> i) & 1u)
+                mbar_wait_bounded(smem_u32(&ctl->full[i]), (pr_last_par >> i) & 1u, never,
+                                  p.timeout_ns);
+    }
+    ps->last_progress = globaltimer_ns();
+    ctl->arg = session_tiles;  // read back by this same thread for the cost estimate
+    ps->pr_stage = pr_stage;
+    ps->pr_phase = pr_phase;
+    ps->pr_slot = pr_slot;
+    ps->pr_slot_phase = pr_slot_phase;
+    ps->pr_issued = pr_issued;
+    ps->pr_last_par = pr_last_par;
+    }
+
+__device__ __noinline__ void gemm_mma(const FusedParams& p, FusedCtl* ctl, uint8_t* smem, uint32_t tmem_base) {
+    FusedSync* sync = p.sync;
+    PipeState* ps = &ctl->ps;
+    volatile uint32_t* abort_local = &ctl->abort_local;
+    uint32_t mm_stage = ps->mm_stage, mm_phase = ps->mm_phase, mm_acc = ps->mm_acc,
+             mm_acc_phase = ps->mm_acc_phase, mm_slot = ps->mm_slot, mm_slot_phase = ps->mm_slot_phase;
+    bool ok = true;
+    for (;;) {
+    if (!mbar_wait_bounded(smem_u32(&ctl->info_full[mm_slot]), mm_slot_phase, abort_local,
+                           p.timeout_ns)) {
+        ok = false;
+        break;
+    }
+    const TileSlot ts = ctl->info[mm_slot];
+    mbar_arrive(smem_u32(&ctl->info_empty[mm_slot]));
+    if (++mm_slot == kInfoSlots) {
+        mm_slot = 0;
+        mm_slot_phase ^= 1u;
+    }
+    if (ts.end) break;
+    if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[mm_acc]), mm_acc_phase ^ 1u, abort_local,
+                           p.timeout_ns)) {
+        ok = false;
+        break;
+    }
+    tc_fence_after();
+    const uint32_t d_tmem = tmem_base + mm_acc * MMA_N;
+    for (int kb = 0; kb < ts.kblocks; ++kb) {
+        if (!mbar_wait_bounded(smem_u32(&ctl->full[mm_stage]), mm_phase, abort_local,
+                               p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t sa = smem_u32(smem + mm_stage * STAGE_BYTES);
+        const uint32_t sb = sa + A_BYTES;
+#pragma unroll
+        for (int kk = 0; kk < BK / UMMA_K; ++kk)
+            mma_bf16_ss(d_tmem, sw128_kmajor_desc(sa + kk * UMMA_K * 2),
+                        sw128_kmajor_desc(sb + kk * UMMA_K * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
+        mma_commit(smem_u32(&ctl->empty[mm_stage]));
+        if (++mm_stage == STAGES) {
+            mm_stage = 0;
+            mm_phase ^= 1u;
+        }
+    }
+    if (!ok) break;
+    mma_commit(smem_u32(&ctl->tmem_full[mm_acc]));
+    mm_acc ^= 1u;
+    if (mm_acc == 0) mm_acc_phase ^= 1u;
+    }
+    if (!ok) {
+    *abort_local = 1u;
+    atomicExch(&sync->abort_flag, 1u);
+    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+    }
+    ps->mm_stage = mm_stage;
+    ps->mm_phase = mm_phase;
+    ps->mm_acc = mm_acc;
+    ps->mm_acc_phase = mm_acc_phase;
+    ps->mm_slot = mm_slot;
+    ps->mm_slot_phase = mm_slot_phase;
+    }
+
+__device__ __noinline__ void gemm_epilogue(const FusedParams& p, FusedCtl* ctl, uint32_t tmem_base, int warp,
+                                   int lane) {
+    FusedSync* sync = p.sync;
+    PipeState* ps = &ctl->ps;
+    volatile uint32_t* abort_local = &ctl->abort_local;
+    const int sub = warp & 3;
+    const int row_in_tile = sub * 32 + lane;
+    uint32_t ep_acc = ps->ep_acc, ep_acc_phase = ps->ep_acc_phase, ep_slot = ps->ep_slot,
+         ep_slot_phase = ps->ep_slot_phase;
+    bool ok = true;
+    for (;;) {
+    if (!mbar_wait_bounded(smem_u32(&ctl->info_full[ep_slot]), ep_slot_phase, abort_local,
+                           p.timeout_ns)) {
+    ok = false;
+    break;
+    }
+    const TileSlot ts = ctl->info[ep_slot];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&ctl->info_empty[ep_slot]));
+    if (++ep_slot == kInfoSlots) {
+    ep_slot = 0;
+    ep_slot_phase ^= 1u;
+    }
+    if (ts.end) break;
+    if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[ep_acc]), ep_acc_phase, abort_local,
+                       p.timeout_ns)) {
+    ok = false;
+    break;
+    }
+    tc_fence_after();
+    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + ep_acc * MMA_N;
+    const bool row_ok = row_in_tile < ts.rows;
+    const int64_t r = static_cast<int64_t>(ts.row0) + row_in_tile;
+    if (ts.mode == 0) {
+    epilogue_swiglu(tbase, row_ok, p.h + r * p.f, ts.n0, p.f);
+    } else {
+    const float wr = row_ok ? p.row_weight[r] : 1.0f;
+    epilogue_weighted(tbase, row_ok, p.P + r * p.d, ts.n0, p.d, wr);
+    }
+    fence_proxy_async_global();  // h is read next by TMA (async proxy)
+    tc_fence_before();
+    __syncwarp();
+    if (lane == 0) {
+    mbar_arrive(smem_u32(&ctl->tmem_empty[ep_acc]));
+    // this warp's 32 rows are stored: publish a quarter of the tile
+    if (ts.mode == 0)
+        publish_add(&p.h_done[ts.g], 1u);
+    else
+        publish_add(&sync->p_done, 1u);
+    }
+    ep_acc ^= 1u;
+    if (ep_acc == 0) ep_acc_phase ^= 1u;
+    }
+    if (!ok && lane == 0) {
+    *abort_local = 1u;
+    atomicExch(&sync->abort_flag, 1u);
+    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
+    }
+    __syncwarp();
+    if (warp == 2 && lane == 0) {  // the four epilogue warps hold the same positions
+    ps->ep_acc = ep_acc;
+    ps->ep_acc_phase = ep_acc_phase;
+    ps->ep_slot = ep_slot;
+    ps->ep_slot_phase = ep_slot_phase;
+    }
 }
 
 // ------------------------------------------------------------------ kernel
@@ -390,12 +670,14 @@ __global__ void __launch_bounds__(kThreads, 1)
             ps->last_progress = lp;
             ctl->action = c.kind;
             ctl->arg = c.arg;
+            ctl->flag = c.n;
             ps->t_start = clock64();
             ps->g_start = globaltimer_ns();
         }
         __syncthreads();
         const int action = ctl->action;
         const int arg = ctl->arg;
+        const int arg_n = ctl->flag;
         __syncthreads();  // everyone has read the action before thread 0 may reuse the slot
         if (action == kActExit) break;
 
@@ -459,7 +741,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         } else if (action == kActCopy) {
             int e, row0, rows;
             decode_g(p, arg, e, row0, rows);
-            tasks::copy_rows(p.x, p.d, p.row_token, row0, rows, p.x_perm);
+            fused_copy(p, row0, rows);
             fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
             __syncthreads();
             if (tid == 0) {
@@ -469,232 +751,18 @@ __global__ void __launch_bounds__(kThreads, 1)
             }
         } else if (action == kActCombine) {
             const int t0 = arg * kCombineTokens;
-            tasks::combine_tokens(p.P, p.slot_row, t0, min(kCombineTokens, p.T - t0), p.d, p.k, p.y);
+            fused_combine(p, t0, min(kCombineTokens, p.T - t0));
         } else if (action == kActGemm) {
             // ---------------------------------------------- GEMM session
-            const int G = p.mtile_start[p.E];
-            const int n1 = G * p.NT1;
+            const GemmMaps maps{&tmA1, &tmW1, &tmW3, &tmA2, &tmW2};
             if (warp == 0) {
-                if (lane == 0) {
-                    uint32_t pr_stage = ps->pr_stage, pr_phase = ps->pr_phase, pr_slot = ps->pr_slot,
-                             pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued,
-                             pr_last_par = ps->pr_last_par;
-                    const int role = ps->role;
-                    int tile = arg;
-                    bool ok = true;
-                    int session_tiles = 0;
-                    for (;;) {
-                        TileSlot ts;
-                        ts.end = (tile < 0) ? 1 : 0;
-                        if (tile >= 0) {
-                            ts.mode = tile < n1 ? 0 : 1;
-                            const int local = ts.mode == 0 ? tile : tile - n1;
-                            const int nt_cnt = ts.mode == 0 ? p.NT1 : p.NT2;
-                            ts.g = local / nt_cnt;
-                            int e;
-                            decode_g(p, ts.g, e, ts.row0, ts.rows);
-                            ts.n0 = (local - ts.g * nt_cnt) * (ts.mode == 0 ? MMA_N / 2 : MMA_N);
-                            ts.kblocks = ts.mode == 0 ? p.kb1 : p.kb2;
-                            ts.pad = e;
-                        }
-                        if (!mbar_wait_bounded(smem_u32(&ctl->info_empty[pr_slot]), pr_slot_phase ^ 1u, abort_local,
-                                               p.timeout_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        ctl->info[pr_slot] = ts;
-                        mbar_arrive(smem_u32(&ctl->info_full[pr_slot]));
-                        if (++pr_slot == kInfoSlots) {
-                            pr_slot = 0;
-                            pr_slot_phase ^= 1u;
-                        }
-                        if (ts.end) break;
-                        ++session_tiles;
-                        // claim the next ready compute tile now, unless this block should
-                        // turn mover: the claim's latency hides behind this tile's loads
-                        int next = -1;
-                        {
-                            const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
-                                              static_cast<int>(ld_relaxed(&sync->movers_active)) >=
-                                                  static_cast<int>(ld_relaxed(&sync->target_movers));
-                            if (stay && ld_relaxed(&sync->abort_flag) == 0u) {
-                                const Claim c = try_claim_compute(p);
-                                if (c.kind == kActGemm) next = c.arg;
-                            }
-                        }
-                        fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
-                        const int e = ts.pad;
-                        const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
-                        for (int kb = 0; kb < ts.kblocks; ++kb) {
-                            if (!mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u, abort_local,
-                                                   p.timeout_ns)) {
-                                ok = false;
-                                break;
-                            }
-                            const uint32_t fb = smem_u32(&ctl->full[pr_stage]);
-                            const uint32_t sa = smem_u32(smem + pr_stage * STAGE_BYTES);
-                            const uint32_t sb = sa + A_BYTES;
-                            mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                            if (ts.mode == 0) {
-                                tma_load_2d(sa, &tmA1, kb * BK, ts.row0, fb);
-                                tma_load_2d(sb, &tmW1, kb * BK, b_row, fb);
-                                tma_load_2d(sb + B_BYTES / 2, &tmW3, kb * BK, b_row, fb);
-                            } else {
-                                tma_load_2d(sa, &tmA2, kb * BK, ts.row0, fb);
-                                tma_load_2d(sb, &tmW2, kb * BK, b_row, fb);
-                            }
-                            pr_issued |= 1u << pr_stage;
-                            pr_last_par = (pr_last_par & ~(1u << pr_stage)) | (pr_phase << pr_stage);
-                            if (++pr_stage == STAGES) {
-                                pr_stage = 0;
-                                pr_phase ^= 1u;
-                            }
-                        }
-                        if (!ok) break;
-                        tile = next;
-                    }
-                    if (!ok) {
-                        *abort_local = 1u;
-                        atomicExch(&sync->abort_flag, 1u);
-                        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
-                        for (int i = 0; i < STAGES; ++i)
-                            if ((pr_issued >> i) & 1u)
-                                mbar_wait_bounded(smem_u32(&ctl->full[i]), (pr_last_par >> i) & 1u, never,
-                                                  p.timeout_ns);
-                    }
-                    ps->last_progress = globaltimer_ns();
-                    ctl->arg = session_tiles;  // read back by this same thread for the cost estimate
-                    ps->pr_stage = pr_stage;
-                    ps->pr_phase = pr_phase;
-                    ps->pr_slot = pr_slot;
-                    ps->pr_slot_phase = pr_slot_phase;
-                    ps->pr_issued = pr_issued;
-                    ps->pr_last_par = pr_last_par;
-                }
+                if (lane == 0) gemm_producer(p, maps, ctl, smem, arg, arg_n);
                 __syncwarp();
             } else if (warp == 1) {
-                if (lane == 0) {
-                    uint32_t mm_stage = ps->mm_stage, mm_phase = ps->mm_phase, mm_acc = ps->mm_acc,
-                             mm_acc_phase = ps->mm_acc_phase, mm_slot = ps->mm_slot, mm_slot_phase = ps->mm_slot_phase;
-                    bool ok = true;
-                    for (;;) {
-                        if (!mbar_wait_bounded(smem_u32(&ctl->info_full[mm_slot]), mm_slot_phase, abort_local,
-                                               p.timeout_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        const TileSlot ts = ctl->info[mm_slot];
-                        mbar_arrive(smem_u32(&ctl->info_empty[mm_slot]));
-                        if (++mm_slot == kInfoSlots) {
-                            mm_slot = 0;
-                            mm_slot_phase ^= 1u;
-                        }
-                        if (ts.end) break;
-                        if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[mm_acc]), mm_acc_phase ^ 1u, abort_local,
-                                               p.timeout_ns)) {
-                            ok = false;
-                            break;
-                        }
-                        tc_fence_after();
-                        const uint32_t d_tmem = tmem_base + mm_acc * MMA_N;
-                        for (int kb = 0; kb < ts.kblocks; ++kb) {
-                            if (!mbar_wait_bounded(smem_u32(&ctl->full[mm_stage]), mm_phase, abort_local,
-                                                   p.timeout_ns)) {
-                                ok = false;
-                                break;
-                            }
-                            tc_fence_after();
-                            const uint32_t sa = smem_u32(smem + mm_stage * STAGE_BYTES);
-                            const uint32_t sb = sa + A_BYTES;
-#pragma unroll
-                            for (int kk = 0; kk < BK / UMMA_K; ++kk)
-                                mma_bf16_ss(d_tmem, sw128_kmajor_desc(sa + kk * UMMA_K * 2),
-                                            sw128_kmajor_desc(sb + kk * UMMA_K * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
-                            mma_commit(smem_u32(&ctl->empty[mm_stage]));
-                            if (++mm_stage == STAGES) {
-                                mm_stage = 0;
-                                mm_phase ^= 1u;
-                            }
-                        }
-                        if (!ok) break;
-                        mma_commit(smem_u32(&ctl->tmem_full[mm_acc]));
-                        mm_acc ^= 1u;
-                        if (mm_acc == 0) mm_acc_phase ^= 1u;
-                    }
-                    if (!ok) {
-                        *abort_local = 1u;
-                        atomicExch(&sync->abort_flag, 1u);
-                        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
-                    }
-                    ps->mm_stage = mm_stage;
-                    ps->mm_phase = mm_phase;
-                    ps->mm_acc = mm_acc;
-                    ps->mm_acc_phase = mm_acc_phase;
-                    ps->mm_slot = mm_slot;
-                    ps->mm_slot_phase = mm_slot_phase;
-                }
+                if (lane == 0) gemm_mma(p, ctl, smem, tmem_base);
                 __syncwarp();
             } else if (warp >= 2 && warp <= 5) {
-                const int sub = warp & 3;
-                const int row_in_tile = sub * 32 + lane;
-                uint32_t ep_acc = ps->ep_acc, ep_acc_phase = ps->ep_acc_phase, ep_slot = ps->ep_slot,
-                         ep_slot_phase = ps->ep_slot_phase;
-                bool ok = true;
-                for (;;) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->info_full[ep_slot]), ep_slot_phase, abort_local,
-                                           p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    const TileSlot ts = ctl->info[ep_slot];
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(smem_u32(&ctl->info_empty[ep_slot]));
-                    if (++ep_slot == kInfoSlots) {
-                        ep_slot = 0;
-                        ep_slot_phase ^= 1u;
-                    }
-                    if (ts.end) break;
-                    if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[ep_acc]), ep_acc_phase, abort_local,
-                                           p.timeout_ns)) {
-                        ok = false;
-                        break;
-                    }
-                    tc_fence_after();
-                    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + ep_acc * MMA_N;
-                    const bool row_ok = row_in_tile < ts.rows;
-                    const int64_t r = static_cast<int64_t>(ts.row0) + row_in_tile;
-                    if (ts.mode == 0) {
-                        epilogue_swiglu(tbase, row_ok, p.h + r * p.f, ts.n0, p.f);
-                    } else {
-                        const float wr = row_ok ? p.row_weight[r] : 1.0f;
-                        epilogue_weighted(tbase, row_ok, p.P + r * p.d, ts.n0, p.d, wr);
-                    }
-                    fence_proxy_async_global();  // h is read next by TMA (async proxy)
-                    tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) {
-                        mbar_arrive(smem_u32(&ctl->tmem_empty[ep_acc]));
-                        // this warp's 32 rows are stored: publish a quarter of the tile
-                        if (ts.mode == 0)
-                            publish_add(&p.h_done[ts.g], 1u);
-                        else
-                            publish_add(&sync->p_done, 1u);
-                    }
-                    ep_acc ^= 1u;
-                    if (ep_acc == 0) ep_acc_phase ^= 1u;
-                }
-                if (!ok && lane == 0) {
-                    *abort_local = 1u;
-                    atomicExch(&sync->abort_flag, 1u);
-                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
-                }
-                __syncwarp();
-                if (warp == 2 && lane == 0) {  // the four epilogue warps hold the same positions
-                    ps->ep_acc = ep_acc;
-                    ps->ep_acc_phase = ep_acc_phase;
-                    ps->ep_slot = ep_slot;
-                    ps->ep_slot_phase = ep_slot_phase;
-                }
+                gemm_epilogue(p, ctl, tmem_base, warp, lane);
             }
         }
         __syncthreads();

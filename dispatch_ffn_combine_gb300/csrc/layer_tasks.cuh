@@ -187,49 +187,70 @@ __device__ __forceinline__ void index_chunk(const int32_t* __restrict__ ids, con
 }
 
 // Copy rows [row0, row0 + rows) of the expert-contiguous buffer from their
-// source tokens (one 16-byte vector per thread per step).
+// source tokens.  A warp per row; each lane keeps 8 independent 16-byte loads
+// in flight before it stores them, so one block moves ~32 KB at a time.
 __device__ __forceinline__ void copy_rows(const bf16* __restrict__ x, int d, const int32_t* __restrict__ row_token,
                                           int64_t row0, int rows, bf16* __restrict__ x_perm) {
+    constexpr int U = 8;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int n16 = d / 8;
-    const int total = rows * n16;
-    for (int i = threadIdx.x; i < total; i += kThreads) {
-        const int rr = i / n16;
-        const int cc = i - rr * n16;
+    for (int rr = warp; rr < rows; rr += kThreads / 32) {
         const int64_t r = row0 + rr;
         const int64_t t = row_token[r];
-        reinterpret_cast<uint4*>(x_perm + r * d)[cc] = __ldg(reinterpret_cast<const uint4*>(x + t * d) + cc);
+        const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
+        uint4* dst = reinterpret_cast<uint4*>(x_perm + r * d);
+        for (int c0 = lane; c0 < n16; c0 += 32 * U) {
+            uint4 v[U];
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < n16) v[u] = __ldg(src + c0 + 32 * u);
+#pragma unroll
+            for (int u = 0; u < U; ++u)
+                if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+        }
     }
 }
 
 // y[t] = bf16( sum_j P[slot_row[t, j]] ), j ascending, fp32 sum, for tokens
-// [t0, t0 + nt).
+// [t0, t0 + nt).  A warp per token; each lane loads its 16-byte piece of all
+// k rows before adding them in slot order.
 __device__ __forceinline__ void combine_tokens(const bf16* __restrict__ P, const int32_t* __restrict__ slot_row,
                                                int64_t t0, int nt, int d, int k, bf16* __restrict__ y) {
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
     const int n16 = d / 8;
-    const int total = nt * n16;
-    for (int i = threadIdx.x; i < total; i += kThreads) {
-        const int tt = i / n16;
-        const int cc = i - tt * n16;
+    for (int tt = warp; tt < nt; tt += kThreads / 32) {
         const int64_t t = t0 + tt;
-        float acc[8];
+        int64_t rows[kMaxTopK];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
-        for (int j = 0; j < k; ++j) {
-            const int64_t r = slot_row[t * k + j];
-            const uint4 v = reinterpret_cast<const uint4*>(P + r * d)[cc];
-            const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        for (int j = 0; j < kMaxTopK; ++j) rows[j] = (j < k) ? static_cast<int64_t>(slot_row[t * k + j]) : 0;
+        for (int cc = lane; cc < n16; cc += 32) {
+            uint4 v[kMaxTopK];
 #pragma unroll
-            for (int q = 0; q < 4; ++q) {
-                acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(wv[q] << 16));
-                acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(wv[q] & 0xffff0000u));
+            for (int j = 0; j < kMaxTopK; ++j)
+                if (j < k) v[j] = reinterpret_cast<const uint4*>(P + rows[j] * d)[cc];
+            float acc[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) acc[q] = 0.0f;
+#pragma unroll
+            for (int j = 0; j < kMaxTopK; ++j) {
+                if (j < k) {
+                    const uint32_t wv[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        acc[2 * q] = __fadd_rn(acc[2 * q], __uint_as_float(wv[q] << 16));
+                        acc[2 * q + 1] = __fadd_rn(acc[2 * q + 1], __uint_as_float(wv[q] & 0xffff0000u));
+                    }
+                }
             }
+            uint4 o;
+            o.x = pack_bf16x2(acc[0], acc[1]);
+            o.y = pack_bf16x2(acc[2], acc[3]);
+            o.z = pack_bf16x2(acc[4], acc[5]);
+            o.w = pack_bf16x2(acc[6], acc[7]);
+            reinterpret_cast<uint4*>(y + t * d)[cc] = o;
         }
-        uint4 o;
-        o.x = pack_bf16x2(acc[0], acc[1]);
-        o.y = pack_bf16x2(acc[2], acc[3]);
-        o.z = pack_bf16x2(acc[4], acc[5]);
-        o.w = pack_bf16x2(acc[6], acc[7]);
-        reinterpret_cast<uint4*>(y + t * d)[cc] = o;
     }
 }
 
