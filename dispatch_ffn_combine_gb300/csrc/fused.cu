@@ -219,7 +219,7 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
 // (they share their readiness), which cuts the number of compare-and-swaps on
 // the queue head and keeps a block's GEMM session going.  Claim.arg is the
 // first ticket, Claim.n the run length.
-constexpr int kBatch = 4;
+constexpr int kBatch = 8;
 
 __device__ Claim try_claim_compute(const FusedParams& p) {
     FusedSync* s = p.sync;
@@ -233,19 +233,18 @@ __device__ Claim try_claim_compute(const FusedParams& p) {
         uint32_t run_end;  // end of this expert M-tile's tiles
         if (h < n1) {
             const uint32_t g = h / p.NT1;
-            ready = ld_relaxed(&p.copy_done[g]) != 0u;
+            ready = ld_acquire(&p.copy_done[g]) != 0u;
             run_end = (g + 1) * p.NT1;
         } else {
             const uint32_t g = (h - n1) / p.NT2;
-            ready = ld_relaxed(&p.h_done[g]) == static_cast<uint32_t>(4 * p.NT1);
+            ready = ld_acquire(&p.h_done[g]) == static_cast<uint32_t>(4 * p.NT1);
             run_end = n1 + (g + 1) * p.NT2;
         }
         if (!ready) return {kActIdle, 0, 0};
         const uint32_t n = min(static_cast<uint32_t>(kBatch), run_end - h);
-        if (atomicCAS(&s->compute_head, h, h + n) == h) {
-            __threadfence();
-            return {kActGemm, static_cast<int>(h), static_cast<int>(n)};
-        }
+        // the acquire load of the flag orders this block's reads of the tile's
+        // inputs after their producers' releases; the CAS only takes the ticket
+        if (atomicCAS(&s->compute_head, h, h + n) == h) return {kActGemm, static_cast<int>(h), static_cast<int>(n)};
     }
     return {kActIdle, 0, 0};
 }
@@ -777,7 +776,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     rec[0] = blockIdx.x;
                     rec[1] = static_cast<uint32_t>(action);
                     rec[2] = static_cast<uint32_t>(arg);
-                    rec[3] = (action == kActGemm) ? n : 0u;
+                    rec[3] = (action == kActGemm) ? (n | ((arg >= p.mtile_start[p.E] * p.NT1) ? 0x80000000u : 0u)) : 0u;
                     rec[4] = static_cast<uint32_t>(ps->g_start);
                     rec[5] = static_cast<uint32_t>(ps->g_start >> 32);
                     rec[6] = static_cast<uint32_t>(g1);
