@@ -15,7 +15,6 @@
 // Two task queues, each claimed in order with an atomic ticket:
 //   mover queue:   route blocks (32 tokens x 32 experts of gate logits)
 //                  -> index chunks (row of every (token, slot) of 128 tokens)
-//                  -> copy tasks (the 128 token rows of one expert M-tile)
 //                  -> combine tasks (32 tokens)
 //   compute queue: gemm1 tiles (expert M-tile x 128 h columns)
 //                  -> gemm2 tiles (expert M-tile x 256 output columns)
@@ -23,9 +22,13 @@
 //   last route block of a token group -> top-k of its tokens
 //   last top-k of a 128-token chunk   -> expert histogram + ranks of the chunk
 //   last chunk counted                -> scans (offsets, chunk bases, tiles)
-// Readiness: index tasks need the scans; copy tasks need every index chunk;
-// gemm1 tile (g, n) needs copy task g; gemm2 tile (g, n) needs all gemm1 tiles
-// of g; combine tasks need every gemm2 tile.  Each of the four epilogue warps
+// The dispatch is not a copy: gemm1's producer gathers each tile's 128 token
+// rows straight from x with TMA gather4 loads, so a dispatched row exists only
+// in shared memory ("matmul'd as soon as they land", README row "MoE
+// Dispatch + GEMM").
+// Readiness: index tasks need the scans; gemm1 tiles need every index chunk;
+// gemm2 tile (g, n) needs all gemm1 tiles of g; combine tasks need every
+// gemm2 tile.  Each of the four epilogue warps
 // of a GEMM tile publishes its own 32 rows, so a tile counts 4 when done.  A block claims only tasks whose
 // inputs are ready, so claiming in order never deadlocks; every wait is
 // bounded by %globaltimer and an abort word.
@@ -43,7 +46,7 @@ constexpr int kInfoSlots = 4;
 constexpr int kCombineTokens = 32;
 
 enum : int { kRoleMover = 0, kRoleCompute = 1 };
-enum : int { kActExit = 0, kActIdle = 1, kActRoute = 2, kActIndex = 3, kActCopy = 4, kActCombine = 5, kActGemm = 6 };
+enum : int { kActExit = 0, kActIdle = 1, kActRoute = 2, kActIndex = 3, kActCombine = 5, kActGemm = 6 };
 
 struct TileSlot {
     int end;
@@ -107,7 +110,6 @@ struct FusedParams {
     int32_t* row_token;
     float* row_weight;
     int32_t* slot_row;
-    bf16* x_perm;
     bf16* h;
     bf16* P;
     bf16* y;
@@ -115,7 +117,6 @@ struct FusedParams {
     FusedSync* sync;
     uint32_t* route_done;  // [n_tg]
     uint32_t* topk_done;   // [nchunks]
-    uint32_t* copy_done;   // [G_max]
     uint32_t* h_done;      // [G_max]
     int n_tg, n_eg, ct, nchunks;
     int NR, NK;
@@ -192,15 +193,11 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
         } else {
             if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0, 0};
             const int G = p.mtile_start[p.E];
-            const uint32_t b_index = p.NR, b_copy = b_index + p.nchunks, b_comb = b_copy + G, total = b_comb + p.NK;
+            const uint32_t b_index = p.NR, b_comb = b_index + p.nchunks, total = b_comb + p.NK;
             if (h >= total) return {kActExit, 0, 0};
-            if (h < b_copy) {
+            if (h < b_comb) {
                 kind = kActIndex;
                 arg = static_cast<int>(h - b_index);
-            } else if (h < b_comb) {
-                if (ld_relaxed(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0, 0};
-                kind = kActCopy;
-                arg = static_cast<int>(h - b_copy);
             } else {
                 if (ld_relaxed(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0, 0};
                 kind = kActCombine;
@@ -233,7 +230,7 @@ __device__ Claim try_claim_compute(const FusedParams& p) {
         uint32_t run_end;  // end of this expert M-tile's tiles
         if (h < n1) {
             const uint32_t g = h / p.NT1;
-            ready = ld_acquire(&p.copy_done[g]) != 0u;
+            ready = ld_acquire(&s->index_done) == static_cast<uint32_t>(p.nchunks);
             run_end = (g + 1) * p.NT1;
         } else {
             const uint32_t g = (h - n1) / p.NT2;
@@ -257,7 +254,7 @@ __device__ int controller_target(const FusedParams& p) {
     const int B = static_cast<int>(gridDim.x);
     if (ld_acquire(&s->scan_done) == 0u) return B;
     const int G = p.mtile_start[p.E];
-    const double mover_total = static_cast<double>(p.NR) + p.nchunks + G + p.NK;
+    const double mover_total = static_cast<double>(p.NR) + p.nchunks + p.NK;
     const double compute_total = static_cast<double>(G) * (p.NT1 + p.NT2);
     const double Rs = fmax(0.0, mover_total - static_cast<double>(ld_relaxed(&s->mover_head)));
     const double Rp = fmax(0.0, compute_total - static_cast<double>(ld_relaxed(&s->compute_head)));
@@ -327,12 +324,8 @@ __device__ __noinline__ void fused_route_block(uint8_t* smem, const FusedParams&
                                              p.E, p.logits, tg, eg);
 }
 
-// The copy and combine bodies keep many loads in flight; separate functions
-// keep their registers out of the persistent kernel's allocation too.
-__device__ __noinline__ void fused_copy(const FusedParams& p, int64_t row0, int rows) {
-    tasks::copy_rows(p.x, p.d, p.row_token, row0, rows, p.x_perm);
-}
-
+// The combine body keeps many loads in flight; a separate function keeps its
+// registers out of the persistent kernel's allocation.
 __device__ __noinline__ void fused_combine(const FusedParams& p, int64_t t0, int nt) {
     tasks::combine_tokens(p.P, p.slot_row, t0, nt, p.d, p.k, p.y);
 }
@@ -343,7 +336,7 @@ __device__ __noinline__ void fused_combine(const FusedParams& p, int64_t t0, int
 // its claimed run; pipeline positions live in ctl->ps between sessions.
 
 struct GemmMaps {
-    const CUtensorMap* a1;
+    const CUtensorMap* x;   // token rows, one-row boxes (gathered)
     const CUtensorMap* w1;
     const CUtensorMap* w3;
     const CUtensorMap* a2;
@@ -351,7 +344,10 @@ struct GemmMaps {
 };
 
 __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps& m, FusedCtl* ctl, uint8_t* smem,
-                                           int arg, int arg_n) {
+                                           int arg, int arg_n, int lane) {
+    // Whole warp: lane 0 owns the barriers, the claims, the tile-info ring and
+    // the weight loads; for gemm1 every lane gathers four A rows straight from
+    // the token rows of x (rows 4*lane .. 4*lane+3 of the tile).
     FusedSync* sync = p.sync;
     PipeState* ps = &ctl->ps;
     volatile uint32_t* abort_local = &ctl->abort_local;
@@ -359,8 +355,7 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
     const int G = p.mtile_start[p.E];
     const int n1 = G * p.NT1;
     uint32_t pr_stage = ps->pr_stage, pr_phase = ps->pr_phase, pr_slot = ps->pr_slot,
-             pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued,
-             pr_last_par = ps->pr_last_par;
+             pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued, pr_last_par = ps->pr_last_par;
     const int role = ps->role;
     int tile = arg;
     int run_left = arg_n;  // tiles left in the claimed run, this one included
@@ -380,56 +375,83 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
             ts.kblocks = ts.mode == 0 ? p.kb1 : p.kb2;
             ts.pad = e;
         }
-        if (!mbar_wait_bounded(smem_u32(&ctl->info_empty[pr_slot]), pr_slot_phase ^ 1u, abort_local,
-                               p.timeout_ns)) {
+        uint32_t got = 1u;
+        if (lane == 0) {
+            got = mbar_wait_bounded(smem_u32(&ctl->info_empty[pr_slot]), pr_slot_phase ^ 1u, abort_local,
+                                    p.timeout_ns)
+                      ? 1u
+                      : 0u;
+            if (got) {
+                ctl->info[pr_slot] = ts;
+                mbar_arrive(smem_u32(&ctl->info_full[pr_slot]));
+            }
+        }
+        if (!__shfl_sync(0xffffffffu, got, 0)) {
             ok = false;
             break;
         }
-        ctl->info[pr_slot] = ts;
-        mbar_arrive(smem_u32(&ctl->info_full[pr_slot]));
         if (++pr_slot == kInfoSlots) {
             pr_slot = 0;
             pr_slot_phase ^= 1u;
         }
         if (ts.end) break;
         ++session_tiles;
-        // next tile: the rest of the claimed run, else claim a new run now
-        // (unless this block should turn mover); the claim's latency
-        // hides behind this tile's loads
+        // Next tile: the rest of the claimed run, else a new run claimed now
+        // (unless this block should turn mover); the claim's latency hides
+        // behind this tile's loads.
         int next = -1;
-        if (run_left > 1) {
-            next = tile + 1;
-            --run_left;
-        } else {
-            const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
-                              static_cast<int>(ld_relaxed(&sync->movers_active)) >=
-                                  static_cast<int>(ld_relaxed(&sync->target_movers));
-            if (stay && ld_relaxed(&sync->abort_flag) == 0u) {
-                const Claim c = try_claim_compute(p);
-                if (c.kind == kActGemm) {
-                    next = c.arg;
-                    run_left = c.n;
+        if (lane == 0) {
+            if (run_left > 1) {
+                next = tile + 1;
+                --run_left;
+            } else {
+                const bool stay = (p.mover_ctas != 0) || role == kRoleCompute ||
+                                  static_cast<int>(ld_relaxed(&sync->movers_active)) >=
+                                      static_cast<int>(ld_relaxed(&sync->target_movers));
+                if (stay && ld_relaxed(&sync->abort_flag) == 0u) {
+                    const Claim c = try_claim_compute(p);
+                    if (c.kind == kActGemm) {
+                        next = c.arg;
+                        run_left = c.n;
+                    }
                 }
             }
         }
+        next = __shfl_sync(0xffffffffu, next, 0);
         fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
         const int e = ts.pad;
         const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
+        int tok[4] = {0, 0, 0, 0};
+        if (ts.mode == 0) {
+            const int first = p.row_token[ts.row0];  // rows past the expert's end reuse a valid token
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const int r = 4 * lane + j;
+                tok[j] = (r < ts.rows) ? p.row_token[ts.row0 + r] : first;
+            }
+        }
         for (int kb = 0; kb < ts.kblocks; ++kb) {
-            if (!mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u, abort_local,
-                                   p.timeout_ns)) {
+            uint32_t free_ok = 1u;
+            if (lane == 0)
+                free_ok = mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u, abort_local,
+                                            p.timeout_ns)
+                              ? 1u
+                              : 0u;
+            if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
                 ok = false;
                 break;
             }
             const uint32_t fb = smem_u32(&ctl->full[pr_stage]);
             const uint32_t sa = smem_u32(smem + pr_stage * STAGE_BYTES);
             const uint32_t sb = sa + A_BYTES;
-            mbar_arrive_expect_tx(fb, STAGE_BYTES);
+            if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
             if (ts.mode == 0) {
-                tma_load_2d(sa, m.a1, kb * BK, ts.row0, fb);
-                tma_load_2d(sb, m.w1, kb * BK, b_row, fb);
-                tma_load_2d(sb + B_BYTES / 2, m.w3, kb * BK, b_row, fb);
-            } else {
+                tma_gather4(sa + 512u * lane, m.x, kb * BK, tok[0], tok[1], tok[2], tok[3], fb);
+                if (lane == 0) {
+                    tma_load_2d(sb, m.w1, kb * BK, b_row, fb);
+                    tma_load_2d(sb + B_BYTES / 2, m.w3, kb * BK, b_row, fb);
+                }
+            } else if (lane == 0) {
                 tma_load_2d(sa, m.a2, kb * BK, ts.row0, fb);
                 tma_load_2d(sb, m.w2, kb * BK, b_row, fb);
             }
@@ -443,24 +465,26 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
         if (!ok) break;
         tile = next;
     }
-    if (!ok) {
-        *abort_local = 1u;
-        atomicExch(&sync->abort_flag, 1u);
-        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
-        for (int i = 0; i < STAGES; ++i)
-            if ((pr_issued >> i) & 1u)
-                mbar_wait_bounded(smem_u32(&ctl->full[i]), (pr_last_par >> i) & 1u, never,
-                                  p.timeout_ns);
+    if (lane == 0) {
+        if (!ok) {
+            *abort_local = 1u;
+            atomicExch(&sync->abort_flag, 1u);
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+            for (int i = 0; i < STAGES; ++i)
+                if ((pr_issued >> i) & 1u)
+                    mbar_wait_bounded(smem_u32(&ctl->full[i]), (pr_last_par >> i) & 1u, never, p.timeout_ns);
+        }
+        ps->last_progress = globaltimer_ns();
+        ctl->arg = session_tiles;  // read back by thread 0 for the cost estimate
+        ps->pr_stage = pr_stage;
+        ps->pr_phase = pr_phase;
+        ps->pr_slot = pr_slot;
+        ps->pr_slot_phase = pr_slot_phase;
+        ps->pr_issued = pr_issued;
+        ps->pr_last_par = pr_last_par;
     }
-    ps->last_progress = globaltimer_ns();
-    ctl->arg = session_tiles;  // read back by this same thread for the cost estimate
-    ps->pr_stage = pr_stage;
-    ps->pr_phase = pr_phase;
-    ps->pr_slot = pr_slot;
-    ps->pr_slot_phase = pr_slot_phase;
-    ps->pr_issued = pr_issued;
-    ps->pr_last_par = pr_last_par;
-    }
+    __syncwarp();
+}
 
 __device__ __noinline__ void gemm_mma(const FusedParams& p, FusedCtl* ctl, uint8_t* smem, uint32_t tmem_base) {
     FusedSync* sync = p.sync;
@@ -597,7 +621,7 @@ __device__ __noinline__ void gemm_epilogue(const FusedParams& p, FusedCtl* ctl, 
 
 template <int WT, int WE>
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_layer_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmW1,
+    fused_layer_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                        const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmA2,
                        const __grid_constant__ CUtensorMap tmW2, const FusedParams p) {
     using RT = route_detail::RouteTile<WT, WE, 8, 1>;
@@ -626,7 +650,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctl->abort_local = 0;
         ctl->zero = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tmA1);
+        prefetch_tensormap(&tmX);
         prefetch_tensormap(&tmW1);
         prefetch_tensormap(&tmW3);
         prefetch_tensormap(&tmA2);
@@ -737,26 +761,14 @@ __global__ void __launch_bounds__(kThreads, 1)
                                p.row_weight, p.slot_row);
             __syncthreads();
             if (tid == 0) publish_add(&sync->index_done, 1u);
-        } else if (action == kActCopy) {
-            int e, row0, rows;
-            decode_g(p, arg, e, row0, rows);
-            fused_copy(p, row0, rows);
-            fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
-            __syncthreads();
-            if (tid == 0) {
-                fence_proxy_async_global();
-                __threadfence();
-                atomicExch(&p.copy_done[arg], 1u);
-            }
         } else if (action == kActCombine) {
             const int t0 = arg * kCombineTokens;
             fused_combine(p, t0, min(kCombineTokens, p.T - t0));
         } else if (action == kActGemm) {
             // ---------------------------------------------- GEMM session
-            const GemmMaps maps{&tmA1, &tmW1, &tmW3, &tmA2, &tmW2};
+            const GemmMaps maps{&tmX, &tmW1, &tmW3, &tmA2, &tmW2};
             if (warp == 0) {
-                if (lane == 0) gemm_producer(p, maps, ctl, smem, arg, arg_n);
-                __syncwarp();
+                gemm_producer(p, maps, ctl, smem, arg, arg_n, lane);
             } else if (warp == 1) {
                 if (lane == 0) gemm_mma(p, ctl, smem, tmem_base);
                 __syncwarp();
@@ -839,7 +851,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     const int d = a.d, E = a.E, k = a.k, f = a.f;
     const int64_t S = T * k;
     CUtensorMap maps[5];
-    if (!make_map(&maps[0], a.x_perm, d, S, BM) ||
+    if (!make_map(&maps[0], a.x, d, static_cast<uint64_t>(T), 1) ||
         !make_map(&maps[1], a.w1, d, static_cast<uint64_t>(E) * f, MMA_N / 2) ||
         !make_map(&maps[2], a.w3, d, static_cast<uint64_t>(E) * f, MMA_N / 2) || !make_map(&maps[3], a.h, f, S, BM) ||
         !make_map(&maps[4], a.w2, f, static_cast<uint64_t>(E) * d, MMA_N))
@@ -867,7 +879,6 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     p.row_token = a.row_token;
     p.row_weight = a.row_weight;
     p.slot_row = a.slot_row;
-    p.x_perm = a.x_perm;
     p.h = a.h;
     p.P = a.P;
     p.y = a.y;
@@ -880,8 +891,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     uint32_t* arr = reinterpret_cast<uint32_t*>(sb + sizeof(FusedSync));
     p.route_done = arr;
     p.topk_done = arr + n_tg_max;
-    p.copy_done = p.topk_done + nch;
-    p.h_done = p.copy_done + g_max;
+    p.h_done = p.topk_done + nch;
     p.n_tg = static_cast<int>((T + ct - 1) / ct);
     p.n_eg = (E + ce - 1) / ce;
     p.ct = ct;
