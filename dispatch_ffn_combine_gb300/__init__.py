@@ -308,7 +308,7 @@ def mk_moe_layer_trace_count(ws, T, d, E, k, ffn, stream=None):
     return int(n.value)
 
 
-TRACE_KINDS = {2: "route", 3: "index", 5: "combine", 6: "gemm"}
+TRACE_KINDS = {2: "route", 3: "dispatch", 5: "combine", 6: "gemm"}
 
 
 def mk_moe_layer_routing(ws, T, d, E, k, ffn, stream=None):

@@ -210,9 +210,6 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
     MK_TRY(launch_mtile_table(expert_offsets, E, S, mtile, status, s));
     FfnArgs a;
     a.x_perm = static_cast<const bf16*>(x_perm);
-    a.x = nullptr;
-    a.row_token = nullptr;
-    a.T = 0;
     a.offsets = expert_offsets;
     a.mtile_start = mtile;
     a.row_weight = row_weight;
@@ -332,13 +329,10 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     MK_TRY(pm.mark(MK_PHASE_SCAN));
     MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile, s));
     MK_TRY(pm.mark(MK_PHASE_SCATTER));
-    MK_TRY(launch_scatter(static_cast<const bf16*>(x), ids, w, T, d, E, k, offsets, chunk_base, rank, nullptr,
+    MK_TRY(launch_scatter(static_cast<const bf16*>(x), ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm,
                           at<int32_t>(ws, L.row_token), row_weight, slot_row, s));
     FfnArgs a;
     a.x_perm = x_perm;
-    a.x = static_cast<const bf16*>(x);
-    a.row_token = at<int32_t>(ws, L.row_token);
-    a.T = T;
     a.offsets = offsets;
     a.mtile_start = mtile;
     a.row_weight = row_weight;
@@ -355,7 +349,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     a.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.inject = opts ? opts->inject : 0;
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
-    MK_TRY(launch_gemm1_gather(a, s));
+    MK_TRY(launch_gemm1(a, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
     MK_TRY(launch_gemm2(a, s));
     MK_TRY(pm.mark(MK_PHASE_COMBINE));

@@ -195,7 +195,6 @@ __global__ void __launch_bounds__(128) scatter_kernel(const bf16* __restrict__ x
         }
     }
     __syncthreads();
-    if (x_perm == nullptr) return;  // index maps only (the GEMM gathers rows from x itself)
     const int n16 = d / 8;  // 16-byte chunks per row
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     for (int c = threadIdx.x; c < n16; c += blockDim.x) {

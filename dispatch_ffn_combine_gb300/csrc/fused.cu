@@ -14,7 +14,8 @@
 //
 // Two task queues, each claimed in order with an atomic ticket:
 //   mover queue:   route blocks (32 tokens x 32 experts of gate logits)
-//                  -> index chunks (row of every (token, slot) of 128 tokens)
+//                  -> dispatch chunks (128 tokens: rows of their slots, and the
+//                     token rows copied into those rows, each read once)
 //                  -> combine tasks (32 tokens)
 //   compute queue: gemm1 tiles (expert M-tile x 128 h columns)
 //                  -> gemm2 tiles (expert M-tile x 256 output columns)
@@ -22,13 +23,10 @@
 //   last route block of a token group -> top-k of its tokens
 //   last top-k of a 128-token chunk   -> expert histogram + ranks of the chunk
 //   last chunk counted                -> scans (offsets, chunk bases, tiles)
-// The dispatch is not a copy: gemm1's producer gathers each tile's 128 token
-// rows straight from x with TMA gather4 loads, so a dispatched row exists only
-// in shared memory ("matmul'd as soon as they land", README row "MoE
-// Dispatch + GEMM").
-// Readiness: index tasks need the scans; gemm1 tiles need every index chunk;
-// gemm2 tile (g, n) needs all gemm1 tiles of g; combine tasks need every
-// gemm2 tile.  Each of the four epilogue warps
+// Readiness: dispatch tasks need the scans; gemm1 tiles need every dispatch
+// chunk (an expert's 128-row tile draws its rows from tokens all over the
+// batch); gemm2 tile (g, n) needs all gemm1 tiles of g; combine tasks need
+// every gemm2 tile.  Each of the four epilogue warps
 // of a GEMM tile publishes its own 32 rows, so a tile counts 4 when done.  A block claims only tasks whose
 // inputs are ready, so claiming in order never deadlocks; every wait is
 // bounded by %globaltimer and an abort word.
@@ -110,6 +108,7 @@ struct FusedParams {
     int32_t* row_token;
     float* row_weight;
     int32_t* slot_row;
+    bf16* x_perm;
     bf16* h;
     bf16* P;
     bf16* y;
@@ -324,8 +323,13 @@ __device__ __noinline__ void fused_route_block(uint8_t* smem, const FusedParams&
                                              p.E, p.logits, tg, eg);
 }
 
-// The combine body keeps many loads in flight; a separate function keeps its
-// registers out of the persistent kernel's allocation.
+// The dispatch and combine bodies keep many loads in flight; separate
+// functions keep their registers out of the persistent kernel's allocation.
+__device__ __noinline__ void fused_dispatch(const FusedParams& p, int64_t c) {
+    tasks::dispatch_chunk(p.ids, p.w, p.T, p.d, p.E, p.k, c, p.offsets, p.chunk_base, p.rank, p.x, p.x_perm,
+                          p.row_token, p.row_weight, p.slot_row);
+}
+
 __device__ __noinline__ void fused_combine(const FusedParams& p, int64_t t0, int nt) {
     tasks::combine_tokens(p.P, p.slot_row, t0, nt, p.d, p.k, p.y);
 }
@@ -336,7 +340,7 @@ __device__ __noinline__ void fused_combine(const FusedParams& p, int64_t t0, int
 // its claimed run; pipeline positions live in ctl->ps between sessions.
 
 struct GemmMaps {
-    const CUtensorMap* x;   // token rows, one-row boxes (gathered)
+    const CUtensorMap* a1;  // dispatched rows (x_perm)
     const CUtensorMap* w1;
     const CUtensorMap* w3;
     const CUtensorMap* a2;
@@ -345,9 +349,8 @@ struct GemmMaps {
 
 __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps& m, FusedCtl* ctl, uint8_t* smem,
                                            int arg, int arg_n, int lane) {
-    // Whole warp: lane 0 owns the barriers, the claims, the tile-info ring and
-    // the weight loads; for gemm1 every lane gathers four A rows straight from
-    // the token rows of x (rows 4*lane .. 4*lane+3 of the tile).
+    // Whole warp, lane 0 does the work: the barriers, the claims, the
+    // tile-info ring and the TMA loads; the other lanes follow its decisions.
     FusedSync* sync = p.sync;
     PipeState* ps = &ctl->ps;
     volatile uint32_t* abort_local = &ctl->abort_local;
@@ -421,15 +424,6 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
         fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
         const int e = ts.pad;
         const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
-        int tok[4] = {0, 0, 0, 0};
-        if (ts.mode == 0) {
-            const int first = p.row_token[ts.row0];  // rows past the expert's end reuse a valid token
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int r = 4 * lane + j;
-                tok[j] = (r < ts.rows) ? p.row_token[ts.row0 + r] : first;
-            }
-        }
         for (int kb = 0; kb < ts.kblocks; ++kb) {
             uint32_t free_ok = 1u;
             if (lane == 0)
@@ -446,8 +440,8 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
             const uint32_t sb = sa + A_BYTES;
             if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
             if (ts.mode == 0) {
-                tma_gather4(sa + 512u * lane, m.x, kb * BK, tok[0], tok[1], tok[2], tok[3], fb);
                 if (lane == 0) {
+                    tma_load_2d(sa, m.a1, kb * BK, ts.row0, fb);
                     tma_load_2d(sb, m.w1, kb * BK, b_row, fb);
                     tma_load_2d(sb + B_BYTES / 2, m.w3, kb * BK, b_row, fb);
                 }
@@ -621,7 +615,7 @@ __device__ __noinline__ void gemm_epilogue(const FusedParams& p, FusedCtl* ctl, 
 
 template <int WT, int WE>
 __global__ void __launch_bounds__(kThreads, 1)
-    fused_layer_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
+    fused_layer_kernel(const __grid_constant__ CUtensorMap tmA1, const __grid_constant__ CUtensorMap tmW1,
                        const __grid_constant__ CUtensorMap tmW3, const __grid_constant__ CUtensorMap tmA2,
                        const __grid_constant__ CUtensorMap tmW2, const FusedParams p) {
     using RT = route_detail::RouteTile<WT, WE, 8, 1>;
@@ -650,7 +644,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         ctl->abort_local = 0;
         ctl->zero = 0;
         fence_mbar_init();
-        prefetch_tensormap(&tmX);
+        prefetch_tensormap(&tmA1);
         prefetch_tensormap(&tmW1);
         prefetch_tensormap(&tmW3);
         prefetch_tensormap(&tmA2);
@@ -757,16 +751,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                 }
             }
         } else if (action == kActIndex) {
-            tasks::index_chunk(p.ids, p.w, p.T, p.E, p.k, arg, p.offsets, p.chunk_base, p.rank, p.row_token,
-                               p.row_weight, p.slot_row);
+            fused_dispatch(p, arg);
+            fence_proxy_async_global();  // the rows are read next by TMA (async proxy)
             __syncthreads();
-            if (tid == 0) publish_add(&sync->index_done, 1u);
+            if (tid == 0) {
+                fence_proxy_async_global();
+                publish_add(&sync->index_done, 1u);
+            }
         } else if (action == kActCombine) {
             const int t0 = arg * kCombineTokens;
             fused_combine(p, t0, min(kCombineTokens, p.T - t0));
         } else if (action == kActGemm) {
             // ---------------------------------------------- GEMM session
-            const GemmMaps maps{&tmX, &tmW1, &tmW3, &tmA2, &tmW2};
+            const GemmMaps maps{&tmA1, &tmW1, &tmW3, &tmA2, &tmW2};
             if (warp == 0) {
                 gemm_producer(p, maps, ctl, smem, arg, arg_n, lane);
             } else if (warp == 1) {
@@ -851,7 +848,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     const int d = a.d, E = a.E, k = a.k, f = a.f;
     const int64_t S = T * k;
     CUtensorMap maps[5];
-    if (!make_map(&maps[0], a.x, d, static_cast<uint64_t>(T), 1) ||
+    if (!make_map(&maps[0], a.x_perm, d, S, BM) ||
         !make_map(&maps[1], a.w1, d, static_cast<uint64_t>(E) * f, MMA_N / 2) ||
         !make_map(&maps[2], a.w3, d, static_cast<uint64_t>(E) * f, MMA_N / 2) || !make_map(&maps[3], a.h, f, S, BM) ||
         !make_map(&maps[4], a.w2, f, static_cast<uint64_t>(E) * d, MMA_N))
@@ -879,6 +876,7 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     p.row_token = a.row_token;
     p.row_weight = a.row_weight;
     p.slot_row = a.slot_row;
+    p.x_perm = a.x_perm;
     p.h = a.h;
     p.P = a.P;
     p.y = a.y;

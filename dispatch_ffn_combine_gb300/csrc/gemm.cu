@@ -61,7 +61,6 @@ struct GemmParams {
     uint32_t* status;
     uint64_t timeout_ns;
     int stall_first_stage;  // test hook: block 0 never loads its first stage
-    const int32_t* row_token;  // MODE 2: source token of every dispatched row
 };
 
 struct TileInfo {
@@ -93,12 +92,7 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmParams& p) {
     return ti;
 }
 
-// MODE 0: gemm1 + SwiGLU, A = dispatched rows (x_perm, one TMA box per stage)
-// MODE 1: gemm2 + row weight, A = h
-// MODE 2: gemm1 + SwiGLU, A gathered straight from the token rows of x: lane i
-//         of the producer warp loads rows 4i .. 4i+3 of the tile with one
-//         TMA gather4 per stage (no dispatched copy of x is needed)
-template <int MODE>
+template <int MODE>  // 0: gemm1 + SwiGLU, 1: gemm2 + row weight
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                         const __grid_constant__ CUtensorMap tmB1, const GemmParams p) {
@@ -126,7 +120,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0 && lane == 0) {
         prefetch_tensormap(&tmA);
         prefetch_tensormap(&tmB0);
-        if (MODE != 1) prefetch_tensormap(&tmB1);
+        if (MODE == 0) prefetch_tensormap(&tmB1);
     }
     if (warp == 1) {
         tmem_alloc(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -140,54 +134,38 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const volatile uint32_t* never = &ctl->zero;
 
     if (warp == 0) {
-        // ---------------------------------------------------- TMA producer
-        // Lane 0 owns the barriers and the weight loads; in MODE 2 every lane
-        // also gathers four A rows.  All lanes track the same ring position.
-        uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
-        bool ok = true;
-        if (MODE == 2 || lane == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            bool ok = true;
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 const TileInfo ti = decode_tile(tile, p);
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
-                int tok[4] = {0, 0, 0, 0};
-                if (MODE == 2) {
-                    const int first = p.row_token[ti.row0];  // rows past the expert's end reuse a valid token
-#pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        const int r = 4 * lane + j;
-                        tok[j] = (r < ti.rows) ? p.row_token[ti.row0 + r] : first;
-                    }
-                }
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    uint32_t got = 1u;
-                    if (lane == 0)
-                        got = mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, p.timeout_ns)
-                                  ? 1u
-                                  : 0u;
-                    if (MODE == 2) got = __shfl_sync(0xffffffffu, got, 0);
-                    if (!got) {
+                    if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, p.timeout_ns)) {
                         ok = false;
                         break;
                     }
                     const uint32_t fb = smem_u32(&ctl->full[stage]);
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
-                    if (lane == 0) mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    const bool stall = p.stall_first_stage && blockIdx.x == 0 && tile == 0 && kb == 0;
-                    if (!stall) {  // injected stall: the stage is announced but never filled
-                        if (MODE == 2) {
-                            tma_gather4(sa + 512u * lane, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], fb);
-                        } else if (lane == 0) {
-                            tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
+                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                    if (p.stall_first_stage && blockIdx.x == 0 && tile == 0 && kb == 0) {
+                        // Injected stall: the stage is announced but never filled.
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                        if (++stage == STAGES) {
+                            stage = 0;
+                            phase ^= 1u;
                         }
-                        if (lane == 0) {
-                            if (MODE != 1) {
-                                tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
-                                tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
-                            } else {
-                                tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
-                            }
-                        }
+                        continue;
+                    }
+                    tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
+                    if (MODE == 0) {
+                        tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                        tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
+                    } else {
+                        tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
                     }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
@@ -197,15 +175,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
             }
-            if (!ok && lane == 0) {
+            if (!ok) {
                 *abort_word = 1u;
                 report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
             }
-            // Every copy this warp started must land before the CTA exits.
-            if (lane == 0)
-                for (int s = 0; s < STAGES; ++s)
-                    if ((issued >> s) & 1u)
-                        mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
+            // Every copy this thread started must land before the CTA exits.
+            for (int s = 0; s < STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == 1) {
@@ -272,7 +249,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool row_ok = row_in_tile < ti.rows;
             const int64_t r = static_cast<int64_t>(ti.row0) + row_in_tile;
             bf16* orow = p.out + r * p.out_ld;
-            if (MODE != 1) {
+            if (MODE == 0) {
                 epilogue_swiglu(tbase, row_ok, orow, ti.n0, p.n_valid);
             } else {
                 const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
@@ -342,33 +319,7 @@ cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
-    p.row_token = nullptr;
     return launch_mode<0>(ma, mb0, mb1, p, a.S, s);
-}
-
-cudaError_t launch_gemm1_gather(const FfnArgs& a, cudaStream_t s) {
-    CUtensorMap mx, mb0, mb1;
-    if (!make_map(&mx, a.x, a.d, static_cast<uint64_t>(a.T), 1) ||
-        !make_map(&mb0, a.w1, a.d, static_cast<uint64_t>(a.E) * a.f, MMA_N / 2) ||
-        !make_map(&mb1, a.w3, a.d, static_cast<uint64_t>(a.E) * a.f, MMA_N / 2))
-        return cudaErrorInvalidValue;
-    GemmParams p;
-    p.offsets = a.offsets;
-    p.mtile_start = a.mtile_start;
-    p.row_weight = nullptr;
-    p.out = a.h;
-    p.out_ld = a.f;
-    p.E = a.E;
-    p.tile_n = MMA_N / 2;
-    p.n_tiles = (a.f + p.tile_n - 1) / p.tile_n;
-    p.n_valid = a.f;
-    p.k_blocks = a.d / BK;
-    p.b_rows_per_expert = a.f;
-    p.status = a.status;
-    p.timeout_ns = a.timeout_ns;
-    p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
-    p.row_token = a.row_token;
-    return launch_mode<2>(mx, mb0, mb1, p, a.S, s);
 }
 
 cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s) {
@@ -390,7 +341,6 @@ cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = 0;
-    p.row_token = nullptr;
     return launch_mode<1>(ma, mb0, mb0, p, a.S, s);
 }
 

@@ -1,7 +1,7 @@
 // layer_tasks.cuh -- per-task device bodies of the layer's data-movement
 // steps, run by one block of 256 threads: top-k of a token, per-chunk expert
-// histogram and ranks, the scans over chunks and experts, the per-chunk index
-// pass, the expert-major row copy, and the combine of a token range.  The
+// histogram and ranks, the scans over chunks and experts, the dispatch of a
+// token chunk (row maps and row copies), and the combine of a token range.  The
 // fused persistent kernel strings them together with ready flags; the
 // stand-alone kernels of the unfused path have their own bodies.
 #pragma once
@@ -168,46 +168,51 @@ __device__ __forceinline__ void scan_all(int32_t* s_counts, const int32_t* __res
     }
 }
 
-// Row of every (token, slot) of one chunk, and the row -> token / weight maps.
-__device__ __forceinline__ void index_chunk(const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t T,
-                                            int E, int k, int64_t c, const int32_t* __restrict__ offsets,
-                                            const int32_t* __restrict__ chunk_base, const int32_t* __restrict__ rank,
-                                            int32_t* __restrict__ row_token, float* __restrict__ row_weight,
-                                            int32_t* __restrict__ slot_row) {
-    const int64_t t_begin = c * kChunkTokens;
-    const int nt = static_cast<int>((T - t_begin < kChunkTokens) ? (T - t_begin) : kChunkTokens);
-    for (int q = threadIdx.x; q < nt * k; q += kThreads) {
-        const int64_t tq = t_begin * k + q;
-        const int e = ids[tq];
-        const int64_t r = static_cast<int64_t>(offsets[e]) + chunk_base[c * E + e] + rank[tq];
-        slot_row[tq] = static_cast<int32_t>(r);
-        row_token[r] = static_cast<int32_t>(t_begin + q / k);
-        row_weight[r] = w[tq];
-    }
-}
-
-// Copy rows [row0, row0 + rows) of the expert-contiguous buffer from their
-// source tokens.  A warp per row; each lane keeps 8 independent 16-byte loads
-// in flight before it stores them, so one block moves ~32 KB at a time.
-__device__ __forceinline__ void copy_rows(const bf16* __restrict__ x, int d, const int32_t* __restrict__ row_token,
-                                          int64_t row0, int rows, bf16* __restrict__ x_perm) {
+// Dispatch of one 128-token chunk: the row of every (token, slot), the row ->
+// token / weight maps, and the token rows copied into their k expert rows.
+// A warp per token reads the row once (8 independent 16-byte loads in flight
+// per lane) and writes it k times.
+__device__ __forceinline__ void dispatch_chunk(const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t T,
+                                               int d, int E, int k, int64_t c, const int32_t* __restrict__ offsets,
+                                               const int32_t* __restrict__ chunk_base,
+                                               const int32_t* __restrict__ rank, const bf16* __restrict__ x,
+                                               bf16* __restrict__ x_perm, int32_t* __restrict__ row_token,
+                                               float* __restrict__ row_weight, int32_t* __restrict__ slot_row) {
     constexpr int U = 8;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int64_t t_begin = c * kChunkTokens;
+    const int nt = static_cast<int>((T - t_begin < kChunkTokens) ? (T - t_begin) : kChunkTokens);
     const int n16 = d / 8;
-    for (int rr = warp; rr < rows; rr += kThreads / 32) {
-        const int64_t r = row0 + rr;
-        const int64_t t = row_token[r];
+    for (int tt = warp; tt < nt; tt += kThreads / 32) {
+        const int64_t t = t_begin + tt;
+        int64_t r_lane = 0;
+        if (lane < k) {
+            const int64_t tq = t * k + lane;
+            const int e = ids[tq];
+            r_lane = static_cast<int64_t>(offsets[e]) + chunk_base[c * E + e] + rank[tq];
+            slot_row[tq] = static_cast<int32_t>(r_lane);
+            row_token[r_lane] = static_cast<int32_t>(t);
+            row_weight[r_lane] = w[tq];
+        }
+        int64_t rows[kMaxTopK];
+#pragma unroll
+        for (int j = 0; j < kMaxTopK; ++j) rows[j] = __shfl_sync(0xffffffffu, r_lane, j);
         const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
-        uint4* dst = reinterpret_cast<uint4*>(x_perm + r * d);
         for (int c0 = lane; c0 < n16; c0 += 32 * U) {
             uint4 v[U];
 #pragma unroll
             for (int u = 0; u < U; ++u)
                 if (c0 + 32 * u < n16) v[u] = __ldg(src + c0 + 32 * u);
 #pragma unroll
-            for (int u = 0; u < U; ++u)
-                if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+            for (int j = 0; j < kMaxTopK; ++j) {
+                if (j < k) {
+                    uint4* dst = reinterpret_cast<uint4*>(x_perm + rows[j] * d);
+#pragma unroll
+                    for (int u = 0; u < U; ++u)
+                        if (c0 + 32 * u < n16) dst[c0 + 32 * u] = v[u];
+                }
+            }
         }
     }
 }

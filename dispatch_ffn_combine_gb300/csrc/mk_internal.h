@@ -80,9 +80,6 @@ cudaError_t launch_combine(const bf16* P, const int32_t* slot_row, int64_t T, in
 
 struct FfnArgs {
     const bf16* x_perm;
-    const bf16* x;               // gather variant: token rows [T, d]
-    const int32_t* row_token;    // gather variant: source token of each row
-    int64_t T;
     const int32_t* offsets;      // [E+1]
     const int32_t* mtile_start;  // [E+1]
     const float* row_weight;     // [S] or null
@@ -98,7 +95,6 @@ struct FfnArgs {
     int inject;                  // MK_INJECT_STALL_GEMM1 or 0
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
-cudaError_t launch_gemm1_gather(const FfnArgs& a, cudaStream_t s);
 
 // Fused persistent kernel: tickets, role accounting and cost sums (followed in
 // the workspace by the per-token-group, per-chunk and per-M-tile counters).
@@ -109,7 +105,7 @@ struct FusedSync {
     uint32_t target_movers;   // controller target (Eq. 2)
     uint32_t count_done;      // chunks counted
     uint32_t scan_done;       // scans finished (0/1)
-    uint32_t index_done;      // index chunks finished
+    uint32_t index_done;      // dispatch chunks finished
     uint32_t p_done;          // gemm2 epilogue quarters finished
     uint32_t abort_flag;      // set by a block whose bounded wait ran out
     uint32_t ntask[2];        // finished tasks per role (mover, compute)

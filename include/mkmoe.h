@@ -100,7 +100,7 @@ typedef struct {
     int trace_cap;         /* fused path: records `trace` can hold (0 = no trace)            */
     uint32_t* trace;       /* fused path, device buffer of trace_cap * 8 words or NULL: one
                               record per task {block, kind, arg, tiles, start_lo, start_hi,
-                              end_lo, end_hi} (%globaltimer ns); kinds 2 route, 3 index,
+                              end_lo, end_hi} (%globaltimer ns); kinds 2 route, 3 dispatch,
                               5 combine, 6 GEMM session (tiles = tiles it ran, bit 31 set
                               when its first tile is a gemm2 tile).
                               min(trace_cap, tasks run) records are written; the task count
