@@ -211,38 +211,25 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
     return {kActIdle, 0, 0};
 }
 
-// Compute tiles are claimed in runs of up to kBatch tiles of one expert M-tile
-// (they share their readiness), which cuts the number of compare-and-swaps on
-// the queue head and keeps a block's GEMM session going.  Claim.arg is the
-// first ticket, Claim.n the run length.
-constexpr int kBatch = 8;
-
+// Compute tiles are claimed one at a time with a fetch-add on the queue head,
+// which never fails under contention and keeps the tiles in flight across the
+// grid consecutive (they share weights in L2, as a static stride would).
+// gemm1 tiles are claimable once every dispatch chunk is done, so they never
+// wait; a gemm2 tile's inputs (the four epilogue quarters of every gemm1 tile
+// of its M-tile) may still be in flight when it is claimed, and its producer
+// waits for them.  That wait cannot deadlock: every gemm1 tile was claimed
+// before any gemm2 tile, by a block that is running it, and gemm1 tiles wait
+// on nothing.
 __device__ Claim try_claim_compute(const FusedParams& p) {
     FusedSync* s = p.sync;
     if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0, 0};
+    if (ld_acquire(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0, 0};
     const int G = p.mtile_start[p.E];
-    const uint32_t n1 = static_cast<uint32_t>(G) * p.NT1, total = n1 + static_cast<uint32_t>(G) * p.NT2;
-    for (int attempt = 0; attempt < kClaimTries; ++attempt) {
-        const uint32_t h = ld_relaxed(&s->compute_head);
-        if (h >= total) return {kActExit, 0, 0};
-        bool ready;
-        uint32_t run_end;  // end of this expert M-tile's tiles
-        if (h < n1) {
-            const uint32_t g = h / p.NT1;
-            ready = ld_acquire(&s->index_done) == static_cast<uint32_t>(p.nchunks);
-            run_end = (g + 1) * p.NT1;
-        } else {
-            const uint32_t g = (h - n1) / p.NT2;
-            ready = ld_acquire(&p.h_done[g]) == static_cast<uint32_t>(4 * p.NT1);
-            run_end = n1 + (g + 1) * p.NT2;
-        }
-        if (!ready) return {kActIdle, 0, 0};
-        const uint32_t n = min(static_cast<uint32_t>(kBatch), run_end - h);
-        // the acquire load of the flag orders this block's reads of the tile's
-        // inputs after their producers' releases; the CAS only takes the ticket
-        if (atomicCAS(&s->compute_head, h, h + n) == h) return {kActGemm, static_cast<int>(h), static_cast<int>(n)};
-    }
-    return {kActIdle, 0, 0};
+    const uint32_t total = static_cast<uint32_t>(G) * (p.NT1 + p.NT2);
+    if (ld_relaxed(&s->compute_head) >= total) return {kActExit, 0, 0};
+    const uint32_t h = atomicAdd(&s->compute_head, 1u);
+    if (h >= total) return {kActExit, 0, 0};
+    return {kActGemm, static_cast<int>(h), 1};
 }
 
 // Eq. 2 of the paper: the mover-block target that equalises the predicted
@@ -421,7 +408,31 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
             }
         }
         next = __shfl_sync(0xffffffffu, next, 0);
-        fence_proxy_async_global();  // inputs acquired at claim time; TMA reads follow
+        if (ts.mode == 1) {
+            // gemm2: all gemm1 quarters of this M-tile must be published
+            uint32_t ready = 1u;
+            if (lane == 0) {
+                const uint32_t want = static_cast<uint32_t>(4 * p.NT1);
+                if (ld_acquire(&p.h_done[ts.g]) != want) {
+                    const uint64_t t0 = globaltimer_ns();
+                    uint32_t backoff = 32;
+                    while (ld_acquire(&p.h_done[ts.g]) != want) {
+                        if (*abort_local != 0u || ld_relaxed(&sync->abort_flag) != 0u ||
+                            globaltimer_ns() - t0 > p.timeout_ns) {
+                            ready = 0u;
+                            break;
+                        }
+                        nanosleep_ns(backoff);
+                        backoff = backoff < 1024 ? 2 * backoff : 1024;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, ready, 0)) {
+                ok = false;
+                break;
+            }
+        }
+        fence_proxy_async_global();  // inputs acquired above / at claim time; TMA reads follow
         const int e = ts.pad;
         const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
         for (int kb = 0; kb < ts.kblocks; ++kb) {
