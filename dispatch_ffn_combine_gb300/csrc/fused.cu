@@ -347,6 +347,7 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
     uint32_t pr_stage = ps->pr_stage, pr_phase = ps->pr_phase, pr_slot = ps->pr_slot,
              pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued, pr_last_par = ps->pr_last_par;
     const int role = ps->role;
+    if (lane == 0) fence_proxy_async_global();  // dispatched rows were acquired with the claim
     int tile = arg;
     int run_left = arg_n;  // tiles left in the claimed run, this one included
     bool ok = true;
@@ -386,9 +387,10 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
         }
         if (ts.end) break;
         ++session_tiles;
-        // Next tile: the rest of the claimed run, else a new run claimed now
-        // (unless this block should turn mover); the claim's latency hides
-        // behind this tile's loads.
+        // Next tile: the rest of the claimed run, else one claimed now (unless
+        // this block should turn mover).  The claim is issued before this
+        // tile's loads and its result used after them, so the atomic's latency
+        // overlaps the loads.
         int next = -1;
         if (lane == 0) {
             if (run_left > 1) {
@@ -407,9 +409,9 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
                 }
             }
         }
-        next = __shfl_sync(0xffffffffu, next, 0);
         if (ts.mode == 1) {
-            // gemm2: all gemm1 quarters of this M-tile must be published
+            // gemm2: all gemm1 quarters of this M-tile must be published; then a
+            // proxy fence orders the TMA reads of h after that acquire
             uint32_t ready = 1u;
             if (lane == 0) {
                 const uint32_t want = static_cast<uint32_t>(4 * p.NT1);
@@ -426,13 +428,13 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
                         backoff = backoff < 1024 ? 2 * backoff : 1024;
                     }
                 }
+                fence_proxy_async_global();
             }
             if (!__shfl_sync(0xffffffffu, ready, 0)) {
                 ok = false;
                 break;
             }
         }
-        fence_proxy_async_global();  // inputs acquired above / at claim time; TMA reads follow
         const int e = ts.pad;
         const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
         for (int kb = 0; kb < ts.kblocks; ++kb) {
@@ -468,7 +470,7 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
             }
         }
         if (!ok) break;
-        tile = next;
+        tile = __shfl_sync(0xffffffffu, next, 0);
     }
     if (lane == 0) {
         if (!ok) {
