@@ -80,6 +80,8 @@ struct FusedCtl {
     uint64_t info_empty[kInfoSlots];
     TileSlot info[kInfoSlots];
     PipeState ps;
+    int32_t s_offsets[kMaxExperts + 1];      // GEMM sessions: tile decode from shared memory
+    int32_t s_mtile_start[kMaxExperts + 1];
     uint32_t tmem_base;
     uint32_t abort_local;
     uint32_t zero;
@@ -151,20 +153,23 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
 // (expert, M-tile) of expert-M-tile index g: largest e with mtile_start[e] <= g.
-__device__ __forceinline__ void decode_g(const FusedParams& p, int g, int& e, int& row0, int& rows) {
-    int lo = 0, hi = p.E - 1;
+// `mts` / `offs` are the tile table and the expert offsets (global memory, or
+// the shared-memory copies a GEMM session makes).
+__device__ __forceinline__ void decode_g(const int32_t* mts, const int32_t* offs, int E, int g, int& e, int& row0,
+                                         int& rows) {
+    int lo = 0, hi = E - 1;
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (p.mtile_start[mid] <= g)
+        if (mts[mid] <= g)
             lo = mid;
         else
             hi = mid - 1;
     }
     e = lo;
-    const int mt = g - p.mtile_start[lo];
-    const int off = p.offsets[lo];
+    const int mt = g - mts[lo];
+    const int off = offs[lo];
     row0 = off + mt * BM;
-    rows = min(BM, p.offsets[lo + 1] - off - mt * BM);
+    rows = min(BM, offs[lo + 1] - off - mt * BM);
 }
 
 struct Claim {
@@ -230,6 +235,14 @@ __device__ Claim try_claim_compute(const FusedParams& p) {
     const uint32_t h = atomicAdd(&s->compute_head, 1u);
     if (h >= total) return {kActExit, 0, 0};
     return {kActGemm, static_cast<int>(h), 1};
+}
+
+// Inside a GEMM session the queue is known to be open (the dispatch finished
+// before the session's first claim) and its size is known: a claim is one
+// fetch-add, with no acquire load that would flush the producer's L1.
+__device__ __forceinline__ int claim_next_tile(const FusedParams& p, uint32_t total) {
+    const uint32_t h = atomicAdd(&p.sync->compute_head, 1u);
+    return h < total ? static_cast<int>(h) : -1;
 }
 
 // Eq. 2 of the paper: the mover-block target that equalises the predicted
@@ -347,6 +360,11 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
     uint32_t pr_stage = ps->pr_stage, pr_phase = ps->pr_phase, pr_slot = ps->pr_slot,
              pr_slot_phase = ps->pr_slot_phase, pr_issued = ps->pr_issued, pr_last_par = ps->pr_last_par;
     const int role = ps->role;
+    for (int i = lane; i <= p.E; i += 32) {  // tile decode from shared memory for the whole session
+        ctl->s_offsets[i] = p.offsets[i];
+        ctl->s_mtile_start[i] = p.mtile_start[i];
+    }
+    __syncwarp();
     if (lane == 0) fence_proxy_async_global();  // dispatched rows were acquired with the claim
     int tile = arg;
     int run_left = arg_n;  // tiles left in the claimed run, this one included
@@ -361,7 +379,7 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
             const int nt_cnt = ts.mode == 0 ? p.NT1 : p.NT2;
             ts.g = local / nt_cnt;
             int e;
-            decode_g(p, ts.g, e, ts.row0, ts.rows);
+            decode_g(ctl->s_mtile_start, ctl->s_offsets, p.E, ts.g, e, ts.row0, ts.rows);
             ts.n0 = (local - ts.g * nt_cnt) * (ts.mode == 0 ? MMA_N / 2 : MMA_N);
             ts.kblocks = ts.mode == 0 ? p.kb1 : p.kb2;
             ts.pad = e;
@@ -401,11 +419,8 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
                                   static_cast<int>(ld_relaxed(&sync->movers_active)) >=
                                       static_cast<int>(ld_relaxed(&sync->target_movers));
                 if (stay && ld_relaxed(&sync->abort_flag) == 0u) {
-                    const Claim c = try_claim_compute(p);
-                    if (c.kind == kActGemm) {
-                        next = c.arg;
-                        run_left = c.n;
-                    }
+                    next = claim_next_tile(p, static_cast<uint32_t>(G) * (p.NT1 + p.NT2));
+                    run_left = 1;
                 }
             }
         }
