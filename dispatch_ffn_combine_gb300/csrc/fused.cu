@@ -631,6 +631,7 @@ __device__ __noinline__ void gemm_epilogue(const FusedParams& p, FusedCtl* ctl, 
     report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
     }
     __syncwarp();
+    if (lane == 0 && p_quarters != 0u) publish_add(&sync->p_done, p_quarters);  // combine waits for all of them
     if (warp == 2 && lane == 0) {  // the four epilogue warps hold the same positions
     ps->ep_acc = ep_acc;
     ps->ep_acc_phase = ep_acc_phase;
