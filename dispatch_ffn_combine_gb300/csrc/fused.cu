@@ -573,70 +573,70 @@ __device__ __noinline__ void gemm_mma(const FusedParams& p, FusedCtl* ctl, uint8
     }
 
 __device__ __noinline__ void gemm_epilogue(const FusedParams& p, FusedCtl* ctl, uint32_t tmem_base, int warp,
-                                   int lane) {
+                                           int lane) {
     FusedSync* sync = p.sync;
     PipeState* ps = &ctl->ps;
     volatile uint32_t* abort_local = &ctl->abort_local;
-    const int sub = warp & 3;
+    const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
     const int row_in_tile = sub * 32 + lane;
     uint32_t ep_acc = ps->ep_acc, ep_acc_phase = ps->ep_acc_phase, ep_slot = ps->ep_slot,
-         ep_slot_phase = ps->ep_slot_phase;
+             ep_slot_phase = ps->ep_slot_phase;
+    uint32_t p_quarters = 0;  // gemm2 quarters stored by this warp, published once at the end
     bool ok = true;
     for (;;) {
-    if (!mbar_wait_bounded(smem_u32(&ctl->info_full[ep_slot]), ep_slot_phase, abort_local,
-                           p.timeout_ns)) {
-    ok = false;
-    break;
-    }
-    const TileSlot ts = ctl->info[ep_slot];
-    __syncwarp();
-    if (lane == 0) mbar_arrive(smem_u32(&ctl->info_empty[ep_slot]));
-    if (++ep_slot == kInfoSlots) {
-    ep_slot = 0;
-    ep_slot_phase ^= 1u;
-    }
-    if (ts.end) break;
-    if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[ep_acc]), ep_acc_phase, abort_local,
-                       p.timeout_ns)) {
-    ok = false;
-    break;
-    }
-    tc_fence_after();
-    const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + ep_acc * MMA_N;
-    const bool row_ok = row_in_tile < ts.rows;
-    const int64_t r = static_cast<int64_t>(ts.row0) + row_in_tile;
-    if (ts.mode == 0) {
-    epilogue_swiglu(tbase, row_ok, p.h + r * p.f, ts.n0, p.f);
-    } else {
-    const float wr = row_ok ? p.row_weight[r] : 1.0f;
-    epilogue_weighted(tbase, row_ok, p.P + r * p.d, ts.n0, p.d, wr);
-    }
-    fence_proxy_async_global();  // h is read next by TMA (async proxy)
-    tc_fence_before();
-    __syncwarp();
-    if (lane == 0) {
-    mbar_arrive(smem_u32(&ctl->tmem_empty[ep_acc]));
-    // this warp's 32 rows are stored: publish a quarter of the tile
-    if (ts.mode == 0)
-        publish_add(&p.h_done[ts.g], 1u);
-    else
-        publish_add(&sync->p_done, 1u);
-    }
-    ep_acc ^= 1u;
-    if (ep_acc == 0) ep_acc_phase ^= 1u;
+        if (!mbar_wait_bounded(smem_u32(&ctl->info_full[ep_slot]), ep_slot_phase, abort_local, p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        const TileSlot ts = ctl->info[ep_slot];
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->info_empty[ep_slot]));
+        if (++ep_slot == kInfoSlots) {
+            ep_slot = 0;
+            ep_slot_phase ^= 1u;
+        }
+        if (ts.end) break;
+        if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[ep_acc]), ep_acc_phase, abort_local, p.timeout_ns)) {
+            ok = false;
+            break;
+        }
+        tc_fence_after();
+        const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + ep_acc * MMA_N;
+        const bool row_ok = row_in_tile < ts.rows;
+        const int64_t r = static_cast<int64_t>(ts.row0) + row_in_tile;
+        if (ts.mode == 0) {
+            epilogue_swiglu(tbase, row_ok, p.h + r * p.f, ts.n0, p.f);
+        } else {
+            const float wr = row_ok ? p.row_weight[r] : 1.0f;
+            epilogue_weighted(tbase, row_ok, p.P + r * p.d, ts.n0, p.d, wr);
+        }
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->tmem_empty[ep_acc]));
+        if (ts.mode == 0) {
+            // h is read next by other blocks' TMA loads (async proxy): proxy
+            // fence, then this warp publishes its quarter of the tile
+            fence_proxy_async_global();
+            __syncwarp();
+            if (lane == 0) publish_add(&p.h_done[ts.g], 1u);
+        } else {
+            ++p_quarters;
+        }
+        ep_acc ^= 1u;
+        if (ep_acc == 0) ep_acc_phase ^= 1u;
     }
     if (!ok && lane == 0) {
-    *abort_local = 1u;
-    atomicExch(&sync->abort_flag, 1u);
-    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
+        *abort_local = 1u;
+        atomicExch(&sync->abort_flag, 1u);
+        report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
     }
     __syncwarp();
     if (lane == 0 && p_quarters != 0u) publish_add(&sync->p_done, p_quarters);  // combine waits for all of them
     if (warp == 2 && lane == 0) {  // the four epilogue warps hold the same positions
-    ps->ep_acc = ep_acc;
-    ps->ep_acc_phase = ep_acc_phase;
-    ps->ep_slot = ep_slot;
-    ps->ep_slot_phase = ep_slot_phase;
+        ps->ep_acc = ep_acc;
+        ps->ep_acc_phase = ep_acc_phase;
+        ps->ep_slot = ep_slot;
+        ps->ep_slot_phase = ep_slot_phase;
     }
 }
 
