@@ -54,8 +54,8 @@ class MkMoeOpts(ctypes.Structure):
 
 
 MK_INJECT_STALL_GEMM1 = 1
-MK_PATH_FUSED = 0
-MK_PATH_STEPS = 1
+MK_PATH_STEPS = 0
+MK_PATH_FUSED = 1
 
 
 def load_library():
@@ -229,8 +229,8 @@ def mk_moe_combine(P, slot_row, y=None, stream=None):
     return y
 
 
-def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_FUSED, mover_ctas=0, trace=None):
-    if (phase_events is None and not timeout_ns and not inject and path == MK_PATH_FUSED and mover_ctas == 0
+def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None):
+    if (phase_events is None and not timeout_ns and not inject and path == MK_PATH_STEPS and mover_ctas == 0
             and trace is None):
         return None
     o = MkMoeOpts()
@@ -266,11 +266,11 @@ def _layer_shapes(x, wg, bias, w1, w3, w2, device=True):
 
 
 def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None, timeout_ns=0, stream=None,
-                 inject=0, path=MK_PATH_FUSED, mover_ctas=0, trace=None):
+                 inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None):
     """The whole layer on device tensors; returns y [T, d] bf16.
 
-    path: MK_PATH_FUSED (one persistent kernel, default) or MK_PATH_STEPS
-    (one kernel per step).  mover_ctas: fused-path SM split, 0 = adaptive."""
+    path: MK_PATH_STEPS (one kernel per step, default) or MK_PATH_FUSED
+    (one persistent kernel).  mover_ctas: fused-path SM split, 0 = adaptive."""
     T, d, E, f = _layer_shapes(x, wg, bias, w1, w3, w2)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device) if y is None else y
     ws = alloc_workspace(T, d, E, k, f, x.device) if ws is None else ws
@@ -282,7 +282,7 @@ def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None,
 
 
 def mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, k, y_host, ws, phase_events=None, timeout_ns=0, stream=None,
-                      path=MK_PATH_FUSED, mover_ctas=0):
+                      path=MK_PATH_STEPS, mover_ctas=0):
     """The layer on host buffers (pinned for asynchronous copies): x_host in, y_host out."""
     T, d, E, f = _layer_shapes(x_host, wg, bias, w1, w3, w2, device=False)
     _need(y_host, torch.bfloat16, (T, d), "y_host", device=False)

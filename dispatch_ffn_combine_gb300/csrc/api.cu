@@ -279,7 +279,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     bf16* x_perm = at<bf16>(ws, L.x_perm);
 
     MK_TRY(cudaMemsetAsync(status, 0, 8, s));
-    const bool fused = !(opts && (opts->path == MK_PATH_STEPS || opts->inject != 0));
+    const bool fused = opts && opts->path == MK_PATH_FUSED && opts->inject == 0;
     if (fused) {
         FusedArgs fa;
         fa.x = static_cast<const bf16*>(x);

@@ -76,7 +76,7 @@ enum {
     MK_PHASE_COMBINE = 7,      /* y[t] = sum_j P[slot_row[t,j]] in j order           */
     MK_PHASE_COUNT_ALL = 8
 };
-/* On the fused path the steps overlap inside one kernel: phase_events then
+/* On the fused path (opts->path = MK_PATH_FUSED) the steps overlap inside one kernel: phase_events then
  * gets event 0 before the kernel and events 1..MK_PHASE_COUNT_ALL after it. */
 
 /* Optional per-call settings (pass NULL for defaults). */
@@ -90,9 +90,10 @@ typedef struct {
                               it, so its consumers' bounded waits run out; the call then
                               reports MK_ERR_TIMEOUT (no fault, no hang).  Kernel-per-step
                               path only.                                                     */
-    int path;              /* MK_PATH_FUSED (0, default): one persistent kernel whose blocks
-                              take mover or compute roles; MK_PATH_STEPS (1): one kernel per
-                              step.  Both give bit-identical results.                       */
+    int path;              /* MK_PATH_STEPS (0, default): one kernel per step, the faster
+                              path on GB300 at every workload measured; MK_PATH_FUSED (1): one
+                              persistent kernel whose blocks take mover or compute roles.
+                              Both give bit-identical results.                              */
     int mover_ctas;        /* fused path: 0 = adaptive split (on-GPU controller, paper
                               section 3.2 Eq. 2); n > 0 = fixed split, blocks [0, n) prefer
                               mover tasks; -1 = no block prefers them (compute blocks still
@@ -107,8 +108,8 @@ typedef struct {
                               is left in the workspace (mk_moe_layer_trace_count).          */
 } mk_moe_opts;
 
-#define MK_PATH_FUSED 0
-#define MK_PATH_STEPS 1
+#define MK_PATH_STEPS 0
+#define MK_PATH_FUSED 1
 
 #define MK_INJECT_STALL_GEMM1 1
 

@@ -16,6 +16,7 @@ pytestmark = pytest.mark.gpu
 
 def _layer(wl, **kw):
     c = wl.cfg
+    kw.setdefault("path", mk.MK_PATH_FUSED)
     ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
     y = mk.mk_moe_layer(wl.g["x"], wl.g["wg"], wl.g["bias"], wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k, ws=ws, **kw)
     st, site = mk.mk_moe_last_device_error(ws)
@@ -54,6 +55,6 @@ def test_fused_repeated_calls_same_workspace():
     c = wl.cfg
     ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
     args = (wl.g["x"], wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
-    ys = [mk.mk_moe_layer(*args, ws=ws).clone() for _ in range(3)]
+    ys = [mk.mk_moe_layer(*args, ws=ws, path=mk.MK_PATH_FUSED).clone() for _ in range(3)]
     assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
     assert all(torch.equal(ys[0].view(torch.int16), y.view(torch.int16)) for y in ys[1:])

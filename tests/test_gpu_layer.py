@@ -117,6 +117,11 @@ def test_layer_full_size(name, n_sample):
     toks = sample_tokens(wl.T, n_sample)
     y_ref, _, _ = wl.oracle_layer(tokens=toks)
     check_output(y.cpu()[torch.from_numpy(toks)], y_ref, name)
-    del wl, y, ws
+    # the persistent-kernel path on the same workspace: the same bits
+    y_f = mk.mk_moe_layer(wl.g["x"], wl.g["wg"], wl.g["bias"], wl.g["w1"], wl.g["w3"], wl.g["w2"], wl.cfg.k, ws=ws,
+                          path=mk.MK_PATH_FUSED)
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    assert torch.equal(y_f.view(torch.int16), y.view(torch.int16))
+    del wl, y, y_f, ws
     gc.collect()
     torch.cuda.empty_cache()
