@@ -95,6 +95,10 @@ struct FfnArgs {
     int inject;                  // MK_INJECT_STALL_GEMM1 or 0
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
+// The same GEMMs computed by CTA pairs (tcgen05 cta_group::2, 256-row tiles).
+cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_auto(const FfnArgs& a, cudaStream_t s);  // pairs when S >= 256 E
 
 // Fused persistent kernel: tickets, role accounting and cost sums (followed in
 // the workspace by the per-token-group, per-chunk and per-M-tile counters).
