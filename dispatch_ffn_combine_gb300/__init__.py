@@ -34,7 +34,7 @@ PHASES = ("route_logits", "topk", "count", "scan", "scatter", "gemm1", "gemm2", 
 ENTRY_POINTS = (
     "mk_moe_workspace_size", "mk_moe_route", "mk_moe_dispatch", "mk_moe_expert_ffn", "mk_moe_combine",
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
-    "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count",
+    "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count", "mk_moe_route_fallbacks",
 )
 
 _lock = threading.Lock()
@@ -54,6 +54,7 @@ class MkMoeOpts(ctypes.Structure):
 
 
 MK_INJECT_STALL_GEMM1 = 1
+MK_INJECT_ROUTE_ZERO_BOUND = 2
 MK_PATH_STEPS = 0
 MK_PATH_FUSED = 1
 
@@ -82,6 +83,7 @@ def load_library():
         lib.mk_moe_layer_routing.argtypes = [P, I64, I, I, I, I, P, P, P, P, P]
         lib.mk_moe_route_noalloc.argtypes = [P, P, P, I64, I, I, I, P, P, P, P]
         lib.mk_moe_layer_trace_count.argtypes = [P, I64, I, I, I, I, P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.mk_moe_route_fallbacks.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         for name in ENTRY_POINTS:
             if name not in ("mk_moe_workspace_size", "mk_moe_status_string"):
                 getattr(lib, name).restype = I
@@ -298,6 +300,14 @@ def mk_moe_last_device_error(ws, stream=None):
     detail = ctypes.c_uint32(0)
     st = load_library().mk_moe_last_device_error(_p(ws), _stream(stream), ctypes.byref(detail))
     return int(st), int(detail.value)
+
+
+def mk_moe_route_fallbacks(ws, stream=None):
+    """Tokens of the last router run on ws whose logits all took the fixed-order
+    fallback (the candidate filter's bound did not hold; synchronises)."""
+    n = ctypes.c_uint32(0)
+    _check(load_library().mk_moe_route_fallbacks(_p(ws), _stream(stream), ctypes.byref(n)), "mk_moe_route_fallbacks")
+    return int(n.value)
 
 
 def mk_moe_layer_trace_count(ws, T, d, E, k, ffn, stream=None):

@@ -24,6 +24,8 @@ WsLayout ws_layout(int64_t T, int d, int E, int k, int f) {
     };
     L.ctrl = take(256);
     L.logits = take(static_cast<size_t>(T) * E * 4);
+    L.wsplit = take(static_cast<size_t>(E) * d * 4);
+    L.wnorm = take(static_cast<size_t>(E) * 4);
     L.ids = take(S * 4);
     L.w = take(S * 4);
     L.chunk_counts = take(nch * E * 4);
@@ -153,11 +155,19 @@ mk_status mk_moe_route(const void* x, const float* wg, const float* bias, int64_
     }
     if ((st = device_ok()) != MK_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    MK_TRY(cudaMemsetAsync(at<uint8_t>(ws, L.ctrl), 0, 8, s));
+    MK_TRY(cudaMemsetAsync(at<uint8_t>(ws, L.ctrl), 0, 12, s));  // status, site, router fallbacks
     float* logits = at<float>(ws, L.logits);
-    MK_TRY(launch_route_logits(static_cast<const bf16*>(x), wg, bias, T, d, E, logits, s));
     if (expert_counts) MK_TRY(cudaMemsetAsync(expert_counts, 0, sizeof(int32_t) * E, s));
-    MK_TRY(launch_topk(logits, T, E, k, topk_ids, topk_w, expert_counts, s));
+    const bf16* xb = static_cast<const bf16*>(x);
+    if (route_tc_supported(d, E)) {
+        MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
+                                   at<uint32_t>(ws, L.ctrl), kDefaultTimeoutNs, s));
+        MK_TRY(launch_route_select(xb, wg, bias, T, d, E, k, logits, at<float>(ws, L.wnorm), topk_ids, topk_w,
+                                   expert_counts, at<uint32_t>(ws, L.ctrl) + 2, false, s));
+    } else {
+        MK_TRY(launch_route_logits(xb, wg, bias, T, d, E, logits, s));
+        MK_TRY(launch_topk(logits, T, E, k, topk_ids, topk_w, expert_counts, s));
+    }
     return MK_OK;
 }
 
@@ -254,7 +264,8 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
         return MK_ERR_INVALID_ARG;
     if (opts != nullptr) {
         if (opts->trace_cap < 0 || (opts->trace_cap > 0 && opts->trace == nullptr)) return MK_ERR_INVALID_ARG;
-        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1) return MK_ERR_INVALID_ARG;
+        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1 && opts->inject != MK_INJECT_ROUTE_ZERO_BOUND)
+            return MK_ERR_INVALID_ARG;
         if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS) return MK_ERR_INVALID_ARG;
         if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
     }
@@ -278,7 +289,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     float* row_weight = at<float>(ws, L.row_weight);
     bf16* x_perm = at<bf16>(ws, L.x_perm);
 
-    MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    MK_TRY(cudaMemsetAsync(status, 0, 12, s));  // status, site, router fallbacks
     const bool fused = opts && opts->path == MK_PATH_FUSED && opts->inject == 0;
     if (fused) {
         FusedArgs fa;
@@ -320,10 +331,25 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
         for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
         return MK_OK;
     }
+    const bf16* xb = static_cast<const bf16*>(x);
+    const uint64_t timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     MK_TRY(pm.mark(MK_PHASE_ROUTE_LOGITS));
-    MK_TRY(launch_route_logits(static_cast<const bf16*>(x), wg, bias, T, d, E, logits, s));
-    MK_TRY(pm.mark(MK_PHASE_TOPK));
-    MK_TRY(launch_topk(logits, T, E, k, ids, w, nullptr, s));
+    // The candidate filter pays off once the fixed-order work (T d E fused
+    // multiply-adds) is large and there are enough 128-token tiles to fill the
+    // GPU; below that the plain fixed-order router is faster.  Same bits.
+    const bool filter = route_tc_supported(d, E) && T >= 2048 &&
+                        static_cast<double>(T) * d * E >= 4294967296.0;
+    if (filter || (opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND && route_tc_supported(d, E))) {
+        MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
+                                   status, timeout_ns, s));
+        MK_TRY(pm.mark(MK_PHASE_TOPK));
+        MK_TRY(launch_route_select(xb, wg, bias, T, d, E, k, logits, at<float>(ws, L.wnorm), ids, w, nullptr,
+                                   status + 2, opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND, s));
+    } else {
+        MK_TRY(launch_route_logits(xb, wg, bias, T, d, E, logits, s));
+        MK_TRY(pm.mark(MK_PHASE_TOPK));
+        MK_TRY(launch_topk(logits, T, E, k, ids, w, nullptr, s));
+    }
     MK_TRY(pm.mark(MK_PHASE_COUNT));
     MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s));
     MK_TRY(pm.mark(MK_PHASE_SCAN));
@@ -347,7 +373,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     a.P = at<bf16>(ws, L.P);
     a.status = status;
     a.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
-    a.inject = opts ? opts->inject : 0;
+    a.inject = opts ? opts->inject : 0;  // only MK_INJECT_STALL_GEMM1 acts in the GEMMs
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
     MK_TRY(launch_gemm1(a, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
@@ -388,6 +414,16 @@ mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail) {
     if (cudaMemset(ws, 0, sizeof st) != cudaSuccess) return MK_ERR_CUDA;
     if (detail) *detail = st[1];
     return static_cast<mk_status>(st[0]);
+}
+
+mk_status mk_moe_route_fallbacks(void* ws, void* stream, uint32_t* count) {
+    if (ws == nullptr) return MK_ERR_WORKSPACE;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MK_ERR_CUDA;
+    uint32_t n = 0;
+    if (cudaMemcpy(&n, static_cast<uint8_t*>(ws) + 8, sizeof n, cudaMemcpyDeviceToHost) != cudaSuccess)
+        return MK_ERR_CUDA;
+    if (count) *count = n;
+    return MK_OK;
 }
 
 mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int ffn, void* stream,

@@ -36,7 +36,9 @@ enum : uint32_t {
 // status[1] = its site.
 struct WsLayout {
     size_t ctrl = 0;
-    size_t logits = 0;        // fp32 [T, E]
+    size_t logits = 0;        // fp32 [T, E]  gate logits (approximate ones on the candidate-filter path)
+    size_t wsplit = 0;        // bf16 [E, 2d]  gate rows split in two bf16 parts, interleaved by 64 columns
+    size_t wnorm = 0;         // fp32 [E]      gate row norms, rounded up
     size_t ids = 0;           // int32 [T, k]
     size_t w = 0;             // fp32 [T, k]
     size_t chunk_counts = 0;  // int32 [nchunks, E]
@@ -64,6 +66,17 @@ inline int64_t num_chunks(int64_t T) { return (T + kChunkTokens - 1) / kChunkTok
 // ----------------------------------------------------------------- launchers
 cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* logits, cudaStream_t s);
+// Router with the tensor-core candidate filter (route_tc.cu): approximate
+// logits with an error bound, then the fixed-order fp32 logits of the
+// candidates only, top-k and softmax.  Same outputs as launch_route_logits +
+// launch_topk, bit for bit.
+bool route_tc_supported(int d, int E);
+cudaError_t launch_route_approx(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
+                                float* approx, bf16* wsplit, float* wnorm, uint32_t* status, uint64_t timeout_ns,
+                                cudaStream_t s);
+cudaError_t launch_route_select(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E, int k,
+                                const float* approx, const float* wnorm, int32_t* ids, float* w, int32_t* counts,
+                                uint32_t* fallbacks, bool zero_bound, cudaStream_t s);
 cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
                         int32_t* counts_or_null, cudaStream_t s);
 cudaError_t launch_count(const int32_t* ids, int64_t T, int E, int k, int32_t* chunk_counts, int32_t* rank,

@@ -37,6 +37,11 @@
  *   logits are chosen, ties to the lower expert id; slot j holds the j-th
  *   largest.  weight_j = exp(l_j - l_0) / sum_j' exp(l_j' - l_0) (softmax over
  *   the chosen k, equal to the full softmax renormalised over the k).
+ *   How it is computed (same bits either way): approximate logits with a
+ *   rigorous-by-construction error interval come from the tensor cores; only
+ *   experts whose interval reaches the k-th largest lower end are candidates,
+ *   and only their logits are computed in the fixed order (see
+ *   mk_moe_route_fallbacks for the safety net).
  */
 #ifndef MKMOE_H
 #define MKMOE_H
@@ -112,6 +117,10 @@ typedef struct {
 #define MK_PATH_FUSED 1
 
 #define MK_INJECT_STALL_GEMM1 1
+#define MK_INJECT_ROUTE_ZERO_BOUND 2  /* test hook: the router's candidate filter runs with a zero
+                                         error bound, so (almost) every token takes the exact
+                                         fallback (all E logits in the fixed order); the results
+                                         are unchanged.  Kernel-per-step path only.          */
 
 /* Bytes of workspace mk_moe_layer needs for these sizes (also enough for
  * mk_moe_route, mk_moe_dispatch and mk_moe_expert_ffn on the same sizes).
@@ -207,6 +216,14 @@ MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const fl
  * `ws` (MK_OK if no device error).  *detail (may be NULL) receives the site
  * code of the error. */
 MK_API mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail);
+
+/* Router diagnostics: *count receives the number of tokens of the last router
+ * run on `ws` (mk_moe_route, or mk_moe_layer on the kernel-per-step path)
+ * whose logits were all computed in the fixed order because the tensor-core
+ * candidate filter's error bound did not hold for one of them (expected 0;
+ * the routing is exact either way).  Synchronises `stream`.  Returns
+ * MK_ERR_WORKSPACE if ws is NULL. */
+MK_API mk_status mk_moe_route_fallbacks(void* ws, void* stream, uint32_t* count);
 
 /* Records the last fused mk_moe_layer call on `ws` wrote into its trace buffer
  * (synchronises `stream`).  Returns MK_ERR_WORKSPACE if ws is NULL. */

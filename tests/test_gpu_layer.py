@@ -90,6 +90,22 @@ def test_layer_host_buffers_match_device_call():
     assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
 
 
+def test_layer_route_fallback_path_is_exact():
+    """With the candidate filter's bound forced to zero, (almost) every token
+    takes the exact fallback (all E logits in the fixed order): the layer's
+    output is bit-identical to the normal call."""
+    wl = Workload("ragged_skew")
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    args = (wl.g["x"], wl.g["wg"], wl.g["bias"], wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
+    y0 = mk.mk_moe_layer(*args, ws=ws).clone()
+    assert mk.mk_moe_route_fallbacks(ws) == 0
+    y1 = mk.mk_moe_layer(*args, ws=ws, inject=mk.MK_INJECT_ROUTE_ZERO_BOUND)
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    assert mk.mk_moe_route_fallbacks(ws) > wl.T // 2
+    assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
+
+
 def test_layer_bounded_wait_times_out_cleanly():
     """A grouped-GEMM stage that is announced but never filled: the waits on it
     run out after the given limit, the call reports MK_ERR_TIMEOUT, nothing

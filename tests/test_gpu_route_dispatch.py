@@ -22,8 +22,10 @@ ROUTE_CONFIGS = ["tiny", "ragged", "ragged_skew", "single", "mid", "skewed", "de
 def test_route_bit_exact(name):
     wl = Workload(name, experts=False)
     E, k = wl.cfg.E, wl.cfg.k
-    ids, w, counts = mk.mk_moe_route(wl.g["x"], wl.g["wg"], wl.g["bias"], k)
-    torch.cuda.synchronize()
+    ws = mk.alloc_workspace(wl.T, wl.cfg.d, E, k, 64, wl.dev)
+    ids, w, counts = mk.mk_moe_route(wl.g["x"], wl.g["wg"], wl.g["bias"], k, ws=ws)
+    # the candidate filter's error bound held for every logit it was checked on
+    assert mk.mk_moe_route_fallbacks(ws) == 0
     _, ids_ref, w_ref = wl.oracle_routing()
     ids_g = ids.cpu().numpy()
     mismatch = np.nonzero(np.any(ids_g != ids_ref, axis=1))[0]
@@ -31,6 +33,62 @@ def test_route_bit_exact(name):
                                f"near-ties in fp64: {wl.near_ties(ids_ref)}"
     np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-6, atol=1e-7)
     np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(ids_ref.ravel(), minlength=E))
+
+
+def _route_vs_oracle(x, wg, bias, k, expect_fallbacks=0):
+    dev = torch.device("cuda:0")
+    T, d = x.shape
+    E = wg.shape[0]
+    ws = mk.alloc_workspace(T, d, E, k, 64, dev)
+    ids, w, counts = mk.mk_moe_route(x.to(dev), wg.to(dev), None if bias is None else bias.to(dev), k, ws=ws)
+    assert mk.mk_moe_route_fallbacks(ws) == expect_fallbacks
+    from dispatch_ffn_combine_gb300.workloads import bf16_bits
+    logits = oracle.router_logits(bf16_bits(x), wg.numpy(), None if bias is None else bias.numpy())
+    ids_ref, w_ref = oracle.topk(logits, k)
+    np.testing.assert_array_equal(ids.cpu().numpy(), ids_ref)
+    np.testing.assert_allclose(w.cpu().numpy(), w_ref, rtol=1e-6, atol=1e-7)
+    np.testing.assert_array_equal(counts.cpu().numpy(), np.bincount(ids_ref.ravel(), minlength=E))
+    return ids_ref
+
+
+def test_route_exact_and_near_ties():
+    """Gate rows that tie exactly (duplicates: the lower id must win) or differ
+    by one ulp in one element, scaled up so that they compete for the top
+    slots: the tensor-core filter cannot separate them, every one is a
+    candidate, and the fixed-order logits decide as in the oracle."""
+    T, d, E, k = 512, 512, 64, 8
+    g = torch.Generator().manual_seed(11)
+    x = torch.randn((T, d), generator=g).to(torch.bfloat16)
+    wg = torch.randn((E, d), generator=g) * d ** -0.5
+    wg[5] *= 3.0
+    wg[6] = wg[5]                                   # exact duplicate of 5
+    wg[8] = wg[5]
+    wg[8, 17] = torch.nextafter(wg[8, 17], torch.tensor(10.0))   # one ulp away in one element
+    wg[9] = wg[8]
+    wg[40] = wg[5] * (1.0 + 2.0 ** -23)             # a relative hair above 5
+    wg[41] = wg[40]
+    ids_ref = _route_vs_oracle(x, wg, None, k)
+    # the tied rows really did compete: 5 beats its duplicates 6 in every token choosing both
+    both = (ids_ref == 5).any(1) & (ids_ref == 6).any(1)
+    assert both.sum() > T // 4
+    pos5 = np.argmax(ids_ref == 5, axis=1)[both]
+    pos6 = np.argmax(ids_ref == 6, axis=1)[both]
+    assert np.all(pos5 < pos6)
+
+
+def test_route_wide_dynamic_range_and_cancellation():
+    """Token rows with a few huge entries of both signs and gate rows spanning
+    many binades: large cancellation inside each logit, and a bias."""
+    T, d, E, k = 300, 1024, 32, 4
+    g = torch.Generator().manual_seed(12)
+    x = torch.randn((T, d), generator=g)
+    x[:, ::97] *= 512.0
+    x = x.to(torch.bfloat16)
+    scale = torch.pow(2.0, torch.randint(-20, 6, (E, d), generator=g).float())
+    wg = torch.randn((E, d), generator=g) * scale * d ** -0.5
+    wg[:, 1::97] = -wg[:, ::97][:, : wg[:, 1::97].shape[1]]
+    bias = torch.randn(E, generator=g)
+    _route_vs_oracle(x, wg, bias, k)
 
 
 def test_route_fixed_order_decides_weights():
