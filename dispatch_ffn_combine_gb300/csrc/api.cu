@@ -187,13 +187,14 @@ mk_status mk_moe_dispatch(const void* x, const int32_t* topk_ids, const float* t
     }
     if ((st = device_ok()) != MK_OK) return st;
     uint32_t* status = at<uint32_t>(ws, L.ctrl);
-    MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    MK_TRY(cudaMemsetAsync(status, 0, 8, s));       // status, site
+    MK_TRY(cudaMemsetAsync(status + 3, 0, 4, s));   // scan ticket
     int32_t* chunk_counts = at<int32_t>(ws, L.chunk_counts);
     int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
     int32_t* rank = at<int32_t>(ws, L.rank);
     MK_TRY(launch_count(topk_ids, T, E, k, chunk_counts, rank, status, s));
     MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), expert_offsets,
-                       at<int32_t>(ws, L.mtile_start), s));
+                       at<int32_t>(ws, L.mtile_start), status + 3, s));
     MK_TRY(launch_scatter(static_cast<const bf16*>(x), topk_ids, topk_w, T, d, E, k, expert_offsets, chunk_base, rank,
                           static_cast<bf16*>(x_perm), row_token, row_weight, slot_row, s));
     return MK_OK;
@@ -216,7 +217,8 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     uint32_t* status = at<uint32_t>(ws, 0);
     int32_t* mtile = at<int32_t>(ws, 256);
-    MK_TRY(cudaMemsetAsync(status, 0, 8, s));
+    MK_TRY(cudaMemsetAsync(status, 0, 8, s));          // status, site
+    MK_TRY(cudaMemsetAsync(status + 4, 0, 16, s));     // GEMM tile tickets
     MK_TRY(launch_mtile_table(expert_offsets, E, S, mtile, status, s));
     FfnArgs a;
     a.x_perm = static_cast<const bf16*>(x_perm);
@@ -235,6 +237,7 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
     a.status = status;
     a.timeout_ns = kDefaultTimeoutNs;
     a.inject = 0;
+    a.tickets = status + 4;
     MK_TRY(launch_gemm1(a, s));
     MK_TRY(launch_gemm2_auto(a, s));
     return MK_OK;
@@ -289,7 +292,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     float* row_weight = at<float>(ws, L.row_weight);
     bf16* x_perm = at<bf16>(ws, L.x_perm);
 
-    MK_TRY(cudaMemsetAsync(status, 0, 12, s));  // status, site, router fallbacks
+    MK_TRY(cudaMemsetAsync(status, 0, 32, s));  // status, site, router fallbacks, scan ticket, GEMM tickets
     const bool fused = opts && opts->path == MK_PATH_FUSED && opts->inject == 0;
     if (fused) {
         FusedArgs fa;
@@ -353,7 +356,8 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     MK_TRY(pm.mark(MK_PHASE_COUNT));
     MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s));
     MK_TRY(pm.mark(MK_PHASE_SCAN));
-    MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile, s));
+    MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile,
+                       status + 3, s));
     MK_TRY(pm.mark(MK_PHASE_SCATTER));
     MK_TRY(launch_scatter(static_cast<const bf16*>(x), ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm,
                           at<int32_t>(ws, L.row_token), row_weight, slot_row, s));
@@ -374,6 +378,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     a.status = status;
     a.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.inject = opts ? opts->inject : 0;  // only MK_INJECT_STALL_GEMM1 acts in the GEMMs
+    a.tickets = status + 4;
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
     MK_TRY(launch_gemm1(a, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));

@@ -102,30 +102,57 @@ __device__ void expert_scan_warp(const int32_t* s_counts, int E, int lane, int32
     }
 }
 
+// Scans after counting.  Block g takes experts [32 g, 32 g + 32), one per lane
+// (loads coalesced across experts); warp w takes a contiguous segment of the
+// chunks.  Per expert: segment sums, an exclusive scan over the segments, then
+// the chunk bases.  The last block to finish (ticket in `done`, reset by that
+// block) scans over experts: offsets and the 128-row tile table.
 __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ chunk_counts, int64_t nchunks, int E,
                                                     int32_t* __restrict__ chunk_base, int32_t* __restrict__ counts,
-                                                    int32_t* __restrict__ offsets,
-                                                    int32_t* __restrict__ mtile_start) {
+                                                    int32_t* __restrict__ offsets, int32_t* __restrict__ mtile_start,
+                                                    uint32_t* done) {
+    __shared__ int32_t s_part[32][33];
     __shared__ int32_t s_counts[kMaxExperts];
+    __shared__ int s_last;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int nwarps = blockDim.x >> 5;
-    for (int e = warp; e < E; e += nwarps) {
-        int running = 0;
-        for (int64_t c0 = 0; c0 < nchunks; c0 += 32) {
-            const int64_t c = c0 + lane;
-            const int v = (c < nchunks) ? chunk_counts[c * E + e] : 0;
-            const int inc = warp_inclusive_scan(v, lane);
-            if (c < nchunks) chunk_base[c * E + e] = running + inc - v;
-            running += __shfl_sync(0xffffffffu, inc, 31);
+    const int e = blockIdx.x * 32 + lane;
+    const bool valid = e < E;
+    const int64_t seg = (nchunks + 31) / 32;
+    const int64_t c0 = warp * seg;
+    const int64_t c1 = (c0 + seg < nchunks) ? c0 + seg : nchunks;
+    int sum = 0;
+    for (int64_t c = c0; c < c1; ++c) sum += valid ? __ldg(chunk_counts + c * E + e) : 0;
+    s_part[warp][lane] = sum;
+    __syncthreads();
+    if (warp == 0) {  // exclusive scan over the 32 segments of expert `lane`
+        int run = 0;
+        for (int w = 0; w < 32; ++w) {
+            const int v = s_part[w][lane];
+            s_part[w][lane] = run;
+            run += v;
         }
-        if (lane == 0) {
-            s_counts[e] = running;
-            counts[e] = running;
-        }
+        if (valid) counts[e] = run;
     }
     __syncthreads();
+    int run = s_part[warp][lane];
+    for (int64_t c = c0; c < c1; ++c) {
+        if (valid) {
+            const int v = __ldg(chunk_counts + c * E + e);
+            chunk_base[c * E + e] = run;
+            run += v;
+        }
+    }
+    __threadfence();
+    __syncthreads();
+    if (threadIdx.x == 0) s_last = (atomicAdd(done, 1u) == gridDim.x - 1) ? 1 : 0;
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
+    for (int i = threadIdx.x; i < E; i += blockDim.x) s_counts[i] = __ldcg(counts + i);
+    __syncthreads();
     if (warp == 0) expert_scan_warp(s_counts, E, lane, offsets, mtile_start);
+    if (threadIdx.x == 0) *done = 0u;  // ready for the next call
 }
 
 // Tile table for caller-supplied offsets (expert FFN entry point).  Offsets
@@ -215,8 +242,9 @@ cudaError_t launch_count(const int32_t* ids, int64_t T, int E, int k, int32_t* c
 }
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int64_t nchunks, int E, int32_t* chunk_base, int32_t* counts,
-                        int32_t* offsets, int32_t* mtile_start, cudaStream_t s) {
-    scan_kernel<<<1, 1024, 0, s>>>(chunk_counts, nchunks, E, chunk_base, counts, offsets, mtile_start);
+                        int32_t* offsets, int32_t* mtile_start, uint32_t* done, cudaStream_t s) {
+    scan_kernel<<<(E + 31) / 32, 1024, 0, s>>>(chunk_counts, nchunks, E, chunk_base, counts, offsets, mtile_start,
+                                                 done);
     return cudaGetLastError();
 }
 

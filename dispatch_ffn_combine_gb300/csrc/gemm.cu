@@ -19,12 +19,19 @@
 //               32 TMEM lanes its warp index allows), fused SwiGLU or weight
 //               scaling, bf16 stores of the valid rows
 // Two 256-column accumulators (all 512 TMEM columns) let the epilogue of one
-// tile overlap the main loop of the next.  One CTA per SM walks a static
-// stride over the tile list; a tile is (expert, 128-row block, N block), found
-// from the per-expert tile prefix table with a binary search.  Rows past the
-// expert's end are loaded (TMA fills past the tensor end with zeros) but never
-// stored.  Every wait is bounded (see mk_device.cuh): on a timeout the CTA
-// records MK_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM, returns.
+// tile overlap the main loop of the next.  A tile is (expert, 128-row block,
+// N block), found from the per-expert tile prefix table with a binary search;
+// rows past the expert's end are loaded (TMA fills past the tensor end with
+// zeros) but never stored.
+//   schedule  persistent CTAs claim tiles in list order, one atomic ticket
+//             per tile (decode_tile gives the order: it keeps the readers of a
+//             weight block and of a row block close together in time, so both
+//             are served from L2).  The producer hands each claimed tile to the
+//             MMA and epilogue roles through a small ring of tile slots in
+//             shared memory.  Which CTA takes which tile never affects the
+//             result.
+// Every wait is bounded (see mk_device.cuh): on a timeout the CTA records
+// MK_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM, returns.
 #include "gemm_impl.cuh"
 
 namespace mk {
@@ -39,10 +46,15 @@ struct SharedCtl {
     uint64_t tmem_full[2];
     uint64_t tmem_empty[2];
     uint64_t drain;
+    uint64_t slot_full[4];   // tile slots: producer -> MMA issuer and epilogue
+    uint64_t slot_empty[4];  // MMA thread + 4 epilogue warps release a slot
+    int4 slot[4];            // {e, row0, rows, n0}; e < 0 ends the CTA's list
     uint32_t tmem_base;
     uint32_t abort_flag;
     uint32_t zero;
 };
+
+constexpr int kSlots = 4;
 
 constexpr size_t SMEM_BYTES = static_cast<size_t>(STAGES) * STAGE_BYTES + sizeof(SharedCtl) + 1024;
 
@@ -60,7 +72,8 @@ struct GemmParams {
     int b_rows_per_expert;
     uint32_t* status;
     uint64_t timeout_ns;
-    int stall_first_stage;  // test hook: block 0 never loads its first stage
+    int stall_first_stage;  // test hook: the CTA that claims tile 0 never loads its first stage
+    uint32_t* ticket;       // a zeroed word: tiles claimed so far
 };
 
 struct TileInfo {
@@ -70,9 +83,17 @@ struct TileInfo {
     int n0;
 };
 
+// Tile t -> (expert, 128-row block, N block).  An expert's tiles occupy
+// [mtile_start[e] * n_tiles, mtile_start[e + 1] * n_tiles); inside, they run
+// in groups of kNGroup N blocks, each group over all of the expert's row
+// blocks, N fastest:  (N group, row block, N block in group).  Tiles claimed
+// one after another then share a weight block (read by the expert's row blocks
+// within a few tile claims) and a row block (read by the group's N blocks
+// back to back), so both are still in L2 when their next reader comes.
+constexpr int kNGroup = 4;
+
 __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmParams& p) {
     const int g = tile / p.n_tiles;
-    const int nt = tile - g * p.n_tiles;
     int lo = 0, hi = p.E - 1;  // largest e with mtile_start[e] <= g
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
@@ -81,7 +102,13 @@ __device__ __forceinline__ TileInfo decode_tile(int tile, const GemmParams& p) {
         else
             hi = mid - 1;
     }
-    const int mt = g - p.mtile_start[lo];
+    const int m_e = p.mtile_start[lo + 1] - p.mtile_start[lo];  // row blocks of the expert
+    const int l = tile - p.mtile_start[lo] * p.n_tiles;
+    const int q = l / (m_e * kNGroup);
+    const int nb = min(kNGroup, p.n_tiles - q * kNGroup);  // N blocks in this group
+    const int r = l - q * m_e * kNGroup;
+    const int mt = r / nb;
+    const int nt = q * kNGroup + (r - mt * nb);
     const int off = p.offsets[lo];
     const int cnt = p.offsets[lo + 1] - off;
     TileInfo ti;
@@ -112,6 +139,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             mbar_init(smem_u32(&ctl->tmem_full[a]), 1);
             mbar_init(smem_u32(&ctl->tmem_empty[a]), 4);
         }
+        for (int i = 0; i < kSlots; ++i) {
+            mbar_init(smem_u32(&ctl->slot_full[i]), 1);
+            mbar_init(smem_u32(&ctl->slot_empty[i]), 5);
+        }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
         ctl->zero = 0;
@@ -135,11 +166,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     if (warp == 0) {
         if (lane == 0) {
-            // ------------------------------------------------ TMA producer
-            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
+            // ------------------------------------------------ tile claims + TMA producer
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
-                const TileInfo ti = decode_tile(tile, p);
+            for (;;) {
+                // one ticket per tile, claimed when the producer is ready for it
+                const uint32_t tk = atomicAdd(p.ticket, 1u);
+                const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
+                int4 info = make_int4(-1, 0, 0, 0);
+                TileInfo ti{};
+                if (tile >= 0) {
+                    ti = decode_tile(tile, p);
+                    info = make_int4(ti.e, ti.row0, ti.rows, ti.n0);
+                }
+                if (!mbar_wait_bounded(smem_u32(&ctl->slot_empty[slot]), slot_phase ^ 1u, abort_word, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                ctl->slot[slot] = info;
+                mbar_arrive(smem_u32(&ctl->slot_full[slot]));
+                if (++slot == kSlots) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+                if (tile < 0) break;
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, p.timeout_ns)) {
@@ -150,30 +200,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                     const uint32_t sb = sa + A_BYTES;
                     mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    if (p.stall_first_stage && blockIdx.x == 0 && tile == 0 && kb == 0) {
-                        // Injected stall: the stage is announced but never filled.
-                        issued |= 1u << stage;
-                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                        if (++stage == STAGES) {
-                            stage = 0;
-                            phase ^= 1u;
-                        }
-                        continue;
-                    }
-                    tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
-                    if (MODE == 0) {
-                        tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
-                        tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
-                    } else {
-                        tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
-                    }
                     issued |= 1u << stage;
                     last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    const bool stall = p.stall_first_stage && tile == 0 && kb == 0;
+                    if (!stall) {  // injected stall: the stage is announced but never filled
+                        tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
+                        if (MODE == 0) {
+                            tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                            tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
+                        } else {
+                            tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                        }
+                    }
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
+                if (!ok) break;
             }
             if (!ok) {
                 *abort_word = 1u;
@@ -188,9 +232,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == 1) {
         if (lane == 0) {
             // ------------------------------------------------ MMA issuer
-            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0, slot_phase = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (;;) {
+                if (!mbar_wait_bounded(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word, p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int tile_e = ctl->slot[slot].x;
+                mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
+                if (++slot == kSlots) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+                if (tile_e < 0) break;
                 if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, abort_word, p.timeout_ns)) {
                     ok = false;
                     break;
@@ -236,24 +291,35 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // ---------------------------------------------------- epilogue
         const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
         const int row_in_tile = sub * 32 + lane;
-        uint32_t acc = 0, acc_phase = 0;
+        uint32_t acc = 0, acc_phase = 0, slot = 0, slot_phase = 0;
         bool ok = true;
-        for (int tile = blockIdx.x; tile < total_tiles; tile += gridDim.x) {
-            const TileInfo ti = decode_tile(tile, p);
+        for (;;) {
+            if (!mbar_wait_bounded(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            const int4 info = ctl->slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
+            if (++slot == kSlots) {
+                slot = 0;
+                slot_phase ^= 1u;
+            }
+            if (info.x < 0) break;
             if (!mbar_wait_bounded(smem_u32(&ctl->tmem_full[acc]), acc_phase, abort_word, p.timeout_ns)) {
                 ok = false;
                 break;
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * MMA_N;
-            const bool row_ok = row_in_tile < ti.rows;
-            const int64_t r = static_cast<int64_t>(ti.row0) + row_in_tile;
-            bf16* orow = p.out + r * p.out_ld;
+            const bool row_ok = row_in_tile < info.z;
+            const int64_t r = static_cast<int64_t>(info.y) + row_in_tile;
+            bf16* orow = p.out + (row_ok ? r : 0) * p.out_ld;
             if (MODE == 0) {
-                epilogue_swiglu(tbase, row_ok, orow, ti.n0, p.n_valid);
+                epilogue_swiglu(tbase, row_ok, orow, info.w, p.n_valid);
             } else {
                 const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
-                epilogue_weighted(tbase, row_ok, orow, ti.n0, p.n_valid, wr);
+                epilogue_weighted(tbase, row_ok, orow, info.w, p.n_valid, wr);
             }
             tc_fence_before();
             __syncwarp();
@@ -319,6 +385,7 @@ cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
+    p.ticket = a.tickets;
     return launch_mode<0>(ma, mb0, mb1, p, a.S, s);
 }
 
@@ -341,6 +408,7 @@ cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s) {
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = 0;
+    p.ticket = a.tickets + 1;
     return launch_mode<1>(ma, mb0, mb0, p, a.S, s);
 }
 

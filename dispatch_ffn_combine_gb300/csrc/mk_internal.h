@@ -81,8 +81,9 @@ cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* i
                         int32_t* counts_or_null, cudaStream_t s);
 cudaError_t launch_count(const int32_t* ids, int64_t T, int E, int k, int32_t* chunk_counts, int32_t* rank,
                          uint32_t* status, cudaStream_t s);
+// `done`: a zeroed word (left zero again) that picks the last block for the expert scan.
 cudaError_t launch_scan(const int32_t* chunk_counts, int64_t nchunks, int E, int32_t* chunk_base, int32_t* counts,
-                        int32_t* offsets, int32_t* mtile_start, cudaStream_t s);
+                        int32_t* offsets, int32_t* mtile_start, uint32_t* done, cudaStream_t s);
 cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, int64_t T, int d, int E, int k,
                            const int32_t* offsets, const int32_t* chunk_base, const int32_t* rank, bf16* x_perm,
                            int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s);
@@ -106,6 +107,7 @@ struct FfnArgs {
     uint32_t* status;
     uint64_t timeout_ns;
     int inject;                  // MK_INJECT_STALL_GEMM1 or 0
+    uint32_t* tickets;           // 2 zeroed words: tile tickets of gemm1 [0] and gemm2 [1]
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
 // The same GEMMs computed by CTA pairs (tcgen05 cta_group::2, 256-row tiles).

@@ -90,8 +90,9 @@ typedef struct {
     void** phase_events;   /* NULL, or MK_PHASE_COUNT_ALL + 1 cudaEvent_t handles created by
                               the caller; event i is recorded on `stream` before phase i and
                               the last one after the final phase (for per-phase timing)      */
-    int inject;            /* test hook, 0 = off.  MK_INJECT_STALL_GEMM1: block 0 of the first
-                              grouped GEMM announces one shared-memory stage but never loads
+    int inject;            /* test hook, 0 = off.  MK_INJECT_STALL_GEMM1: in the first grouped
+                              GEMM, the block that takes tile 0 announces one shared-memory
+                              stage but never loads
                               it, so its consumers' bounded waits run out; the call then
                               reports MK_ERR_TIMEOUT (no fault, no hang).  Kernel-per-step
                               path only.                                                     */
