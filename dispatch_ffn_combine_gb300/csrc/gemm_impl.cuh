@@ -28,17 +28,21 @@ constexpr uint32_t IDESC = idesc_bf16_f32(BM, MMA_N);
 
 __device__ __forceinline__ float silu_mul(float g, float u) { return (g / (1.0f + expf(-g))) * u; }
 
-// Epilogue of one 128 x 256 accumulator for the 32 rows of this warp's TMEM
-// lane group.  Every lane of the warp must call (tcgen05.ld is warp-wide);
-// only rows with row_ok store.
-//   gemm1: columns [0,128) are gate, [128,256) up: h = bf16(silu(g) * u)
-//   gemm2: P = bf16(wr * acc)
-__device__ __forceinline__ void epilogue_swiglu(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
+// Epilogues for the TMEM lane this thread reads (every lane of the warp must
+// call: tcgen05.ld is warp-wide); only rows with row_ok store.
+//   SwiGLU, G gate columns at tbase, the matching G up columns at tbase + G:
+//     h[n0 + c] = bf16(silu(g_c) * u_c), c < G
+//   weighted, C columns at tbase:  P[n0 + c] = bf16(wr * acc_c), c < C
+// A 128 x 256 single-CTA or 256 x 256 pair accumulator gives each lane
+// G = 128 (gate | up) or C = 256; the 128-row pair tile folds its upper output
+// columns into lanes 64..127, giving each lane G = 64 or C = 128.
+template <int G>
+__device__ __forceinline__ void epilogue_swiglu_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
 #pragma unroll 1
-    for (int c = 0; c < 128; c += 32) {
+    for (int c = 0; c < G; c += 32) {
         uint32_t g[32], u[32];
         tmem_ld_32x32b_x32(tbase + c, g);
-        tmem_ld_32x32b_x32(tbase + 128 + c, u);
+        tmem_ld_32x32b_x32(tbase + G + c, u);
         tmem_ld_wait();
         if (row_ok) {
             uint32_t pk[16];
@@ -57,10 +61,11 @@ __device__ __forceinline__ void epilogue_swiglu(uint32_t tbase, bool row_ok, bf1
     }
 }
 
-__device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
-                                                  float wr) {
+template <int C>
+__device__ __forceinline__ void epilogue_weighted_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
+                                                    float wr) {
 #pragma unroll 1
-    for (int c = 0; c < MMA_N; c += 32) {
+    for (int c = 0; c < C; c += 32) {
         uint32_t a[32];
         tmem_ld_32x32b_x32(tbase + c, a);
         tmem_ld_wait();
@@ -78,6 +83,15 @@ __device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, b
             }
         }
     }
+}
+
+__device__ __forceinline__ void epilogue_swiglu(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
+    epilogue_swiglu_w<128>(tbase, row_ok, orow, n0, n_valid);
+}
+
+__device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
+                                                  float wr) {
+    epilogue_weighted_w<MMA_N>(tbase, row_ok, orow, n0, n_valid, wr);
 }
 
 // ------------------------------------------------------------------ host side

@@ -110,8 +110,7 @@ struct FfnArgs {
     uint32_t* tickets;           // 2 zeroed words: tile tickets of gemm1 [0] and gemm2 [1]
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
-// The same GEMMs computed by CTA pairs (tcgen05 cta_group::2, 256-row tiles).
-cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s);
+// gemm2 computed by CTA pairs (tcgen05 cta_group::2, 256-row and 128-row tiles).
 cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2_auto(const FfnArgs& a, cudaStream_t s);  // pairs when S >= 256 E
 

@@ -66,7 +66,7 @@ CONFIGS = {
     "ragged": MoEConfig("ragged", 1000, 384, 12, 3, 320),
     "ragged_skew": MoEConfig("ragged_skew", 777, 512, 20, 5, 192, zipf_s=1.2),
     "single": MoEConfig("single", 300, 256, 1, 1, 384),
-    # >= 256 rows per expert on average (gemm2 on CTA pairs), ragged tails
+    # ~500 rows per expert: several row blocks per expert, ragged in every tile dimension
     "ragged_pair": MoEConfig("ragged_pair", 1500, 384, 6, 2, 320),
     # profiling shape: the large layer's d and ffn with 16 experts (about 2.5 GB
     # on the device), small enough for multi-pass counter captures

@@ -67,11 +67,11 @@ def test_ffn_tile_edges():
     _check_ffn([0, 1, 127, 128, 129, 0, 255, 256, 300], d=320, f=192, seed=10)
 
 
-def test_ffn_pair_tile_edges():
-    """Enough rows per expert (S >= 256 E) for gemm2 on CTA pairs: experts with
-    0, 1, 255, 256, 257, 511, 513, 600 rows (pair blocks with an empty, a
-    partial and a full second half); d = 384 leaves half of the last 256-column
-    tile outside the output."""
+def test_ffn_tile_edges_many_rows():
+    """Experts with 0, 1, 255, 256, 257, 511, 513, 600 rows (tiles claimed in
+    expert-local N groups; groups with one, several and a partial last row
+    block); d = 384 leaves half of the last 256-column gemm2 tile outside the
+    output."""
     _check_ffn([0, 1, 255, 256, 257, 600, 511, 513, 129], d=384, f=320, seed=60)
 
 

@@ -106,11 +106,12 @@ def test_layer_route_fallback_path_is_exact():
     assert torch.equal(y0.view(torch.int16), y1.view(torch.int16))
 
 
-def test_layer_bounded_wait_times_out_cleanly():
+@pytest.mark.parametrize("name", ["ragged", "ragged_pair"])
+def test_layer_bounded_wait_times_out_cleanly(name):
     """A grouped-GEMM stage that is announced but never filled: the waits on it
     run out after the given limit, the call reports MK_ERR_TIMEOUT, nothing
     faults or hangs, and the next call on the same context is correct."""
-    wl = Workload("ragged")
+    wl = Workload(name)
     c = wl.cfg
     ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
     args = (wl.g["x"], wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
