@@ -239,7 +239,7 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
     a.inject = 0;
     a.tickets = status + 4;
     MK_TRY(launch_gemm1(a, s));
-    MK_TRY(launch_gemm2_auto(a, s));
+    MK_TRY(launch_gemm2(a, s));
     return MK_OK;
 }
 
@@ -382,7 +382,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
     MK_TRY(launch_gemm1(a, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
-    MK_TRY(launch_gemm2_auto(a, s));
+    MK_TRY(launch_gemm2(a, s));
     MK_TRY(pm.mark(MK_PHASE_COMBINE));
     MK_TRY(launch_combine(a.P, slot_row, T, d, k, static_cast<bf16*>(y), s));
     MK_TRY(pm.mark(MK_PHASE_COUNT_ALL));

@@ -110,9 +110,6 @@ struct FfnArgs {
     uint32_t* tickets;           // 2 zeroed words: tile tickets of gemm1 [0] and gemm2 [1]
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
-// gemm2 computed by CTA pairs (tcgen05 cta_group::2, 256-row and 128-row tiles).
-cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s);
-cudaError_t launch_gemm2_auto(const FfnArgs& a, cudaStream_t s);  // pairs when S >= 256 E
 
 // Fused persistent kernel: tickets, role accounting and cost sums (followed in
 // the workspace by the per-token-group, per-chunk and per-M-tile counters).
