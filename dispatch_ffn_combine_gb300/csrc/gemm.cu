@@ -169,9 +169,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             // ------------------------------------------------ tile claims + TMA producer
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
+            // One ticket per tile.  The next ticket is taken before this tile's
+            // loads and used after them, so the atomic's latency hides behind them.
+            uint32_t tk = atomicAdd(p.ticket, 1u);
             for (;;) {
-                // one ticket per tile, claimed when the producer is ready for it
-                const uint32_t tk = atomicAdd(p.ticket, 1u);
                 const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
                 int4 info = make_int4(-1, 0, 0, 0);
                 TileInfo ti{};
@@ -190,6 +191,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     slot_phase ^= 1u;
                 }
                 if (tile < 0) break;
+                tk = atomicAdd(p.ticket, 1u);
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, p.timeout_ns)) {
