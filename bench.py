@@ -133,6 +133,19 @@ class ClockSampler:
                 "samples": len(sm), "power_w_max": max(power)}
 
 
+def launches_per_step(cfg, path) -> int:
+    """Kernels one mk_moe_layer call launches.  The fused path is one kernel.
+    The kernel-per-step path runs route (plain: logits + top-k; with the
+    tensor-core candidate filter, which the library picks when T >= 2048,
+    T*d*E >= 2^32 and the token row fits its staging: prep + approximate
+    logits + select), count, scan, scatter, gemm1, gemm2, combine."""
+    import dispatch_ffn_combine_gb300 as mk
+    if path == mk.MK_PATH_FUSED:
+        return 1
+    filt = (cfg.T >= 2048 and cfg.T * cfg.d * cfg.E >= 2 ** 32 and 2 * cfg.d + 8 * cfg.E <= 160 * 1024)
+    return (3 if filt else 2) + 6
+
+
 def flops_bytes(cfg, offsets):
     """Algorithmic work per layer call and per phase."""
     T, d, E, k, f = cfg.T, cfg.d, cfg.E, cfg.k, cfg.f
@@ -405,7 +418,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
-        "gpu_launches": (1 if args.path == mk.MK_PATH_FUSED else len(mk.PHASES)) * args.steps,
+        "gpu_launches": launches_per_step(cfg, args.path) * args.steps,
         "path": "fused persistent kernel" if args.path == mk.MK_PATH_FUSED else "one kernel per step",
         "mover_ctas": args.mover_ctas,
         "other_path": {"path": "fused persistent kernel" if other == mk.MK_PATH_FUSED else "one kernel per step",
