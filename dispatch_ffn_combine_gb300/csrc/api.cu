@@ -256,28 +256,19 @@ mk_status mk_moe_combine(const void* P, const int32_t* slot_row, int64_t T, int 
     return MK_OK;
 }
 
-mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const void* w1, const void* w3,
-                       const void* w2, int64_t T, int d, int E, int k, int ffn, void* y, void* ws, size_t ws_bytes,
-                       const mk_moe_opts* opts, void* stream) {
-    mk_status st = check_sizes(T, d, E, k, ffn);
-    if (st != MK_OK) return st;
-    if (T == 0) return MK_OK;  // empty batch: nothing to read or write
-    if (!x || !wg || !w1 || !w3 || !w2 || !y) return MK_ERR_INVALID_ARG;
-    if (!aligned16(x) || !aligned16(wg) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2) || !aligned16(y))
-        return MK_ERR_INVALID_ARG;
-    if (opts != nullptr) {
-        if (opts->trace_cap < 0 || (opts->trace_cap > 0 && opts->trace == nullptr)) return MK_ERR_INVALID_ARG;
-        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1 && opts->inject != MK_INJECT_ROUTE_ZERO_BOUND)
-            return MK_ERR_INVALID_ARG;
-        if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS) return MK_ERR_INVALID_ARG;
-        if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
-    }
-    const WsLayout L = ws_layout(T, d, E, k, ffn);
-    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
-    if (T == 0) return MK_OK;
-    if ((st = device_ok()) != MK_OK) return st;
+}  // extern "C"
 
-    cudaStream_t s = static_cast<cudaStream_t>(stream);
+namespace {
+
+// Hooks for the host-buffer entry point's pipelined copies (kernel-per-step path).
+struct LayerHooks {
+    cudaEvent_t after_scatter = nullptr;  // recorded once x has been read for the last time
+    bool skip_combine = false;            // the caller runs the combine itself (in chunks)
+};
+
+mk_status layer_impl(const void* x, const float* wg, const float* bias, const void* w1, const void* w3,
+                     const void* w2, int64_t T, int d, int E, int k, int ffn, void* y, void* ws,
+                     const WsLayout& L, const mk_moe_opts* opts, cudaStream_t s, const LayerHooks& hk) {
     const PhaseMarks pm{opts ? opts->phase_events : nullptr, s};
     uint32_t* status = at<uint32_t>(ws, L.ctrl);
     int32_t* ids = at<int32_t>(ws, L.ids);
@@ -361,6 +352,7 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     MK_TRY(pm.mark(MK_PHASE_SCATTER));
     MK_TRY(launch_scatter(static_cast<const bf16*>(x), ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm,
                           at<int32_t>(ws, L.row_token), row_weight, slot_row, s));
+    if (hk.after_scatter != nullptr) MK_TRY(cudaEventRecord(hk.after_scatter, s));
     FfnArgs a;
     a.x_perm = x_perm;
     a.offsets = offsets;
@@ -384,31 +376,186 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
     MK_TRY(launch_gemm2(a, s));
     MK_TRY(pm.mark(MK_PHASE_COMBINE));
+    if (hk.skip_combine) return MK_OK;
     MK_TRY(launch_combine(a.P, slot_row, T, d, k, static_cast<bf16*>(y), s));
     MK_TRY(pm.mark(MK_PHASE_COUNT_ALL));
     return MK_OK;
 }
 
+mk_status validate_layer(const void* x, const float* wg, const void* w1, const void* w3, const void* w2, int64_t T,
+                         int d, int E, int k, int ffn, const void* y, void* ws, size_t ws_bytes,
+                         const mk_moe_opts* opts, bool device_xy) {
+    mk_status st = check_sizes(T, d, E, k, ffn);
+    if (st != MK_OK) return st;
+    if (!x || !wg || !w1 || !w3 || !w2 || !y) return MK_ERR_INVALID_ARG;
+    if (!aligned16(wg) || !aligned16(w1) || !aligned16(w3) || !aligned16(w2)) return MK_ERR_INVALID_ARG;
+    if (device_xy && (!aligned16(x) || !aligned16(y))) return MK_ERR_INVALID_ARG;
+    if (opts != nullptr) {
+        if (opts->trace_cap < 0 || (opts->trace_cap > 0 && opts->trace == nullptr)) return MK_ERR_INVALID_ARG;
+        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1 && opts->inject != MK_INJECT_ROUTE_ZERO_BOUND)
+            return MK_ERR_INVALID_ARG;
+        if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS) return MK_ERR_INVALID_ARG;
+        if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
+    }
+    if ((st = check_ws(ws, ws_bytes, ws_layout(T, d, E, k, ffn))) != MK_OK) return st;
+    return device_ok();
+}
+
+// Copy streams and events of the host-buffer entry point, one set per
+// (device, workspace), created on first use and kept (a few sets, least
+// recently used replaced after its copies have drained).
+constexpr int kHostChunks = 8;
+constexpr int kHostPipes = 8;
+
+struct HostPipe {
+    int dev = -1;
+    const void* ws = nullptr;
+    uint64_t used = 0;
+    cudaStream_t h2d = nullptr, d2h[2] = {nullptr, nullptr};  // output chunks alternate between two copy streams
+    cudaEvent_t x_free = nullptr;               // the last read of the staged x (after the scatter)
+    cudaEvent_t x_ready = nullptr;              // staged x uploaded
+    cudaEvent_t y_ready[kHostChunks] = {};      // combine of output chunk c done
+    cudaEvent_t y_done[kHostChunks] = {};       // download of output chunk c done
+};
+
+std::mutex g_pipe_mu;
+HostPipe g_pipes[kHostPipes];
+uint64_t g_pipe_clock = 0;
+
+void release_pipe(HostPipe& p) {
+    if (p.h2d) cudaStreamSynchronize(p.h2d);
+    for (cudaStream_t q : p.d2h)
+        if (q) cudaStreamSynchronize(q);
+    cudaEvent_t* evs[] = {&p.x_free, &p.x_ready};
+    for (cudaEvent_t* e : evs)
+        if (*e) cudaEventDestroy(*e);
+    for (int c = 0; c < kHostChunks; ++c) {
+        if (p.y_ready[c]) cudaEventDestroy(p.y_ready[c]);
+        if (p.y_done[c]) cudaEventDestroy(p.y_done[c]);
+    }
+    if (p.h2d) cudaStreamDestroy(p.h2d);
+    for (cudaStream_t q : p.d2h)
+        if (q) cudaStreamDestroy(q);
+    p = HostPipe{};
+}
+
+cudaError_t get_pipe(const void* ws, HostPipe** out) {
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    std::lock_guard<std::mutex> lock(g_pipe_mu);
+    HostPipe* victim = &g_pipes[0];
+    for (HostPipe& p : g_pipes) {
+        if (p.dev == dev && p.ws == ws) {
+            p.used = ++g_pipe_clock;
+            *out = &p;
+            return cudaSuccess;
+        }
+        if (p.used < victim->used) victim = &p;
+    }
+    release_pipe(*victim);
+    HostPipe& p = *victim;
+    const unsigned ef = cudaEventDisableTiming;
+    if ((err = cudaStreamCreateWithFlags(&p.h2d, cudaStreamNonBlocking)) != cudaSuccess) return err;
+    for (cudaStream_t& q : p.d2h)
+        if ((err = cudaStreamCreateWithFlags(&q, cudaStreamNonBlocking)) != cudaSuccess) return err;
+    if ((err = cudaEventCreateWithFlags(&p.x_free, ef)) != cudaSuccess) return err;
+    if ((err = cudaEventCreateWithFlags(&p.x_ready, ef)) != cudaSuccess) return err;
+    for (int c = 0; c < kHostChunks; ++c) {
+        if ((err = cudaEventCreateWithFlags(&p.y_ready[c], ef)) != cudaSuccess) return err;
+        if ((err = cudaEventCreateWithFlags(&p.y_done[c], ef)) != cudaSuccess) return err;
+    }
+    p.dev = dev;
+    p.ws = ws;
+    p.used = ++g_pipe_clock;
+    *out = &p;
+    return cudaSuccess;
+}
+
+}  // namespace
+
+extern "C" {
+
+mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const void* w1, const void* w3,
+                       const void* w2, int64_t T, int d, int E, int k, int ffn, void* y, void* ws, size_t ws_bytes,
+                       const mk_moe_opts* opts, void* stream) {
+    if (T == 0 && check_sizes(T, d, E, k, ffn) == MK_OK) return MK_OK;  // empty batch: nothing to read or write
+    mk_status st = validate_layer(x, wg, w1, w3, w2, T, d, E, k, ffn, y, ws, ws_bytes, opts, true);
+    if (st != MK_OK) return st;
+    return layer_impl(x, wg, bias, w1, w3, w2, T, d, E, k, ffn, y, ws, ws_layout(T, d, E, k, ffn), opts,
+                      static_cast<cudaStream_t>(stream), LayerHooks{});
+}
+
 mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bias, const void* w1, const void* w3,
                             const void* w2, int64_t T, int d, int E, int k, int ffn, void* y_host, void* ws,
                             size_t ws_bytes, const mk_moe_opts* opts, void* stream) {
-    mk_status st = check_sizes(T, d, E, k, ffn);
+    if (T == 0 && check_sizes(T, d, E, k, ffn) == MK_OK) return MK_OK;
+    mk_status st = validate_layer(x_host, wg, w1, w3, w2, T, d, E, k, ffn, y_host, ws, ws_bytes, opts, false);
     if (st != MK_OK) return st;
-    if (T == 0) return MK_OK;
-    if (!x_host || !y_host) return MK_ERR_INVALID_ARG;
     const WsLayout L = ws_layout(T, d, E, k, ffn);
-    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
-    if (T == 0) return MK_OK;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const size_t bytes = static_cast<size_t>(T) * d * 2;
-    void* xd = at<uint8_t>(ws, L.x_stage);
-    void* yd = at<uint8_t>(ws, L.y_stage);
-    MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
-    st = mk_moe_layer(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, ws_bytes, opts, stream);
+    bf16* xd = at<bf16>(ws, L.x_stage);
+    bf16* yd = at<bf16>(ws, L.y_stage);
+    HostPipe* hp = nullptr;
+    MK_TRY(get_pipe(ws, &hp));
+    if (opts && opts->path == MK_PATH_FUSED) {
+        // plain sequence around the persistent kernel, ordered after any
+        // earlier call's use of the staging buffers and before any later one
+        MK_TRY(cudaStreamWaitEvent(s, hp->x_free, 0));
+        for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+        MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
+        st = layer_impl(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, L, opts, s, LayerHooks{});
+        if (st != MK_OK) return st;
+        MK_TRY(cudaEventRecord(hp->x_free, s));
+        MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+        for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaEventRecord(hp->y_done[c], s));
+        return MK_OK;
+    }
+    // Kernel-per-step path, pipelined copies on the workspace's copy streams:
+    //  - the upload of x waits only for the previous call on this workspace to
+    //    have read the staged x (its scatter), so it overlaps that call's GEMMs;
+    //  - the combine runs in chunks of tokens and each chunk is downloaded as
+    //    soon as it is combined, alternating between two copy streams (a chunk
+    //    of the staged y is rewritten only once the previous call's download
+    //    of it is done);
+    //  - `stream` waits for the last download, so the output is in y_host once
+    //    the stream reaches this point, as for the plain sequence.
+    MK_TRY(cudaStreamWaitEvent(hp->h2d, hp->x_free, 0));
+    MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
+    MK_TRY(cudaEventRecord(hp->x_ready, hp->h2d));
+    MK_TRY(cudaStreamWaitEvent(s, hp->x_ready, 0));
+    LayerHooks hk;
+    hk.after_scatter = hp->x_free;
+    hk.skip_combine = true;
+    st = layer_impl(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, L, opts, s, hk);
     if (st != MK_OK) return st;
-    MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, s));
+    const bf16* P = at<bf16>(ws, L.P);
+    const int32_t* slot_row = at<int32_t>(ws, L.slot_row);
+    const int64_t tc = (T + kHostChunks - 1) / kHostChunks;
+    int last = -1;
+    for (int c = 0; c < kHostChunks; ++c) {
+        const int64_t t0 = c * tc;
+        const int64_t nt = std::min<int64_t>(tc, T - t0);
+        if (nt <= 0) break;
+        MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+        MK_TRY(launch_combine(P, slot_row + t0 * k, nt, d, k, yd + t0 * d, s, T * k));
+        MK_TRY(cudaEventRecord(hp->y_ready[c], s));
+        cudaStream_t q = hp->d2h[c & 1];
+        MK_TRY(cudaStreamWaitEvent(q, hp->y_ready[c], 0));
+        MK_TRY(cudaMemcpyAsync(static_cast<bf16*>(y_host) + t0 * d, yd + t0 * d, static_cast<size_t>(nt) * d * 2,
+                               cudaMemcpyDeviceToHost, q));
+        MK_TRY(cudaEventRecord(hp->y_done[c], q));
+        last = c;
+    }
+    if (opts && opts->phase_events && opts->phase_events[MK_PHASE_COUNT_ALL])
+        MK_TRY(cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[MK_PHASE_COUNT_ALL]), s));
+    for (int c = std::max(0, last - 1); c <= last; ++c)  // the last chunk of each copy stream
+        MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
     return MK_OK;
 }
+
+
 
 mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail) {
     if (ws == nullptr) return MK_ERR_WORKSPACE;

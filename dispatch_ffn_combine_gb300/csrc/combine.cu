@@ -15,10 +15,9 @@ namespace mk {
 namespace {
 
 __global__ void __launch_bounds__(128) combine_kernel(const bf16* __restrict__ P, const int32_t* __restrict__ slot_row,
-                                                      int64_t T, int d, int k, bf16* __restrict__ y) {
+                                                      int64_t S, int d, int k, bf16* __restrict__ y) {
     __shared__ int64_t rows[kMaxTopK];
     const int64_t t = blockIdx.x;
-    const int64_t S = T * k;
     if (threadIdx.x < k) {
         const int64_t r = slot_row[t * k + threadIdx.x];
         rows[threadIdx.x] = (r >= 0 && r < S) ? r : -1;
@@ -53,8 +52,9 @@ __global__ void __launch_bounds__(128) combine_kernel(const bf16* __restrict__ P
 }  // namespace
 
 cudaError_t launch_combine(const bf16* P, const int32_t* slot_row, int64_t T, int d, int k, bf16* y,
-                           cudaStream_t s) {
-    combine_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(P, slot_row, T, d, k, y);
+                           cudaStream_t s, int64_t p_rows) {
+    // P has p_rows rows (T * k unless the tokens are a chunk of a larger batch)
+    combine_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(P, slot_row, p_rows >= 0 ? p_rows : T * k, d, k, y);
     return cudaGetLastError();
 }
 

@@ -89,8 +89,9 @@ cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, in
                            int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s);
 cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t* mtile_start, uint32_t* status,
                                cudaStream_t s);
+// y[t] = sum_j P[slot_row[t, j]] for t < T; p_rows = rows of P (-1: T * k).
 cudaError_t launch_combine(const bf16* P, const int32_t* slot_row, int64_t T, int d, int k, bf16* y,
-                           cudaStream_t s);
+                           cudaStream_t s, int64_t p_rows = -1);
 
 struct FfnArgs {
     const bf16* x_perm;

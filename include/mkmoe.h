@@ -206,7 +206,13 @@ MK_API mk_status mk_moe_layer(const void* x, const float* wg, const float* bias,
 /* The layer on HOST buffers: copies x_host (T*d bf16, pinned for an
  * asynchronous copy) into a staging region of `ws`, runs mk_moe_layer, and
  * copies y back into y_host.  Weights stay on the device.  Asynchronous on
- * `stream`; the result is in y_host once the stream has reached this point. */
+ * `stream`; the result is in y_host once the stream has reached this point.
+ * On the kernel-per-step path the copies run on two copy streams the library
+ * keeps per (device, workspace): the upload of x waits only until the
+ * previous call on `ws` has read its staged x, so it overlaps that call's
+ * GEMMs, and y is combined and downloaded in 8 token chunks.  The library
+ * creates those streams and events on a workspace's first call (and keeps a
+ * few sets); device memory is still only the caller's. */
 MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bias,
                             const void* w1, const void* w3, const void* w2,
                             int64_t T, int d, int E, int k, int ffn,

@@ -90,6 +90,30 @@ def test_layer_host_buffers_match_device_call():
     assert torch.equal(y_host.view(torch.int16), y_dev.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("T", [7, 1000])
+def test_layer_host_calls_back_to_back(T):
+    """Host-buffer calls issued back to back on one workspace (their copies
+    overlap the previous call's kernels), alternating paths and inputs: every
+    y_host equals the device-buffer result for its own input."""
+    wl = Workload("ragged", T=T)
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    g = torch.Generator().manual_seed(7)
+    xs = [wl.g["x"].cpu()] + [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(3)]
+    xs_host = [x.pin_memory() for x in xs]
+    ys_host = [torch.empty((wl.T, c.d), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    paths = [mk.MK_PATH_STEPS, mk.MK_PATH_STEPS, mk.MK_PATH_FUSED, mk.MK_PATH_STEPS]
+    args = (wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
+    for xh, yh, path in zip(xs_host, ys_host, paths):
+        mk.mk_moe_layer_host(xh, *args, yh, ws, path=path)
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    ws2 = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    for x, yh in zip(xs, ys_host):
+        y_dev = mk.mk_moe_layer(x.to(wl.dev), *args, ws=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+
 def test_layer_route_fallback_path_is_exact():
     """With the candidate filter's bound forced to zero, (almost) every token
     takes the exact fallback (all E logits in the fixed order): the layer's
