@@ -515,10 +515,10 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     // Kernel-per-step path, pipelined copies on the workspace's copy streams:
     //  - the upload of x waits only for the previous call on this workspace to
     //    have read the staged x (its scatter), so it overlaps that call's GEMMs;
-    //  - the combine runs in chunks of tokens and each chunk is downloaded as
-    //    soon as it is combined, alternating between two copy streams (a chunk
-    //    of the staged y is rewritten only once the previous call's download
-    //    of it is done);
+    //  - the combine runs in chunks of tokens (about 16 MB of output each, at
+    //    most kHostChunks) and each chunk is downloaded as soon as it is
+    //    combined, alternating between two copy streams (the staged y is
+    //    rewritten only once the previous call's downloads are done);
     //  - `stream` waits for the last download, so the output is in y_host once
     //    the stream reaches this point, as for the plain sequence.
     MK_TRY(cudaStreamWaitEvent(hp->h2d, hp->x_free, 0));
@@ -532,13 +532,18 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     if (st != MK_OK) return st;
     const bf16* P = at<bf16>(ws, L.P);
     const int32_t* slot_row = at<int32_t>(ws, L.slot_row);
-    const int64_t tc = (T + kHostChunks - 1) / kHostChunks;
+    // about 16 MB of output per chunk (1 to kHostChunks chunks): small layers
+    // gain nothing from splitting and would pay a launch and a copy per chunk
+    const int chunks = static_cast<int>(std::min<int64_t>(kHostChunks, std::max<int64_t>(1, bytes >> 24)));
+    const int64_t tc = (T + chunks - 1) / chunks;
+    // the staged y is rewritten only after every download of an earlier call
+    // (which may have cut it into other chunks) has finished
+    for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
     int last = -1;
-    for (int c = 0; c < kHostChunks; ++c) {
+    for (int c = 0; c < chunks; ++c) {
         const int64_t t0 = c * tc;
         const int64_t nt = std::min<int64_t>(tc, T - t0);
         if (nt <= 0) break;
-        MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
         MK_TRY(launch_combine(P, slot_row + t0 * k, nt, d, k, yd + t0 * d, s, T * k));
         MK_TRY(cudaEventRecord(hp->y_ready[c], s));
         cudaStream_t q = hp->d2h[c & 1];
