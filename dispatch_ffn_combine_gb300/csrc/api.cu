@@ -238,8 +238,8 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
     a.timeout_ns = kDefaultTimeoutNs;
     a.inject = 0;
     a.tickets = status + 4;
-    MK_TRY(launch_gemm1(a, s));
-    MK_TRY(launch_gemm2(a, s));
+    MK_TRY(launch_gemm1_auto(a, s));
+    MK_TRY(launch_gemm2_auto(a, s));
     return MK_OK;
 }
 
@@ -372,9 +372,9 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
     a.inject = opts ? opts->inject : 0;  // only MK_INJECT_STALL_GEMM1 acts in the GEMMs
     a.tickets = status + 4;
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
-    MK_TRY(launch_gemm1(a, s));
+    MK_TRY(launch_gemm1_auto(a, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
-    MK_TRY(launch_gemm2(a, s));
+    MK_TRY(launch_gemm2_auto(a, s));
     MK_TRY(pm.mark(MK_PHASE_COMBINE));
     if (hk.skip_combine) return MK_OK;
     MK_TRY(launch_combine(a.P, slot_row, T, d, k, static_cast<bf16*>(y), s));

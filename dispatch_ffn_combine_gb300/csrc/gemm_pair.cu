@@ -1,0 +1,558 @@
+// gemm_pair.cu -- the grouped expert GEMMs on CTA pairs (tcgen05 cta_group::2).
+//
+// The same two GEMMs as the single-CTA kernel of gemm.cu (the expert FFN of
+// the mKernel README's "MoE Dispatch + FFN + Combine" row: gemm1 -> SwiGLU ->
+// gemm2), each output tile computed by a cluster of two CTAs on two SMs:
+//
+//   pair tile   256 rows of one expert x 256 accumulator columns.  CTA r holds
+//               A rows [128 r, 128 r + 128) and half of the 256 B rows
+//               (gemm1: CTA 0 the 128 gate rows of W1, CTA 1 the matching up
+//               rows of W3; gemm2: W2 rows n0 + 128 r ...) and receives its
+//               128 rows x 256 columns of the accumulator in its own TMEM.
+//               One thread of CTA 0 issues the MMAs (M = 256, N = 256, K = 16).
+//   half tile   an expert with an odd number of 128-row blocks ends in a pair
+//               block of at most 128 rows, run as an M = 128 pair MMA: each CTA
+//               holds 64 rows, and TMEM lanes 0-63 get output columns 0-127 of
+//               those rows, lanes 64-127 columns 128-255.  For gemm1 each CTA
+//               then loads 64 gate rows of W1 and the same 64 rows of W3, so
+//               every lane holds matching gate and up columns.  The pair thus
+//               computes no more rows than the single-CTA kernel.
+//   why         per SM and k-block, 32 KB of operands cross L2 and shared
+//               memory instead of 48 KB (B is split, not duplicated), so six
+//               stages (3072 cycles of MMA work) fit instead of four.
+//   copies      each CTA loads its own A and B halves with TMA; all four
+//               copies of a stage complete on CTA 0's `full` barrier, which
+//               CTA 0 arms with both CTAs' bytes.
+//   schedule    CTA 0's producer claims tiles in list order (one atomic ticket
+//               each; the list keeps an expert's tiles in groups of 4 N blocks
+//               over its pair blocks, so tiles claimed together share weight
+//               and row blocks in L2) and writes each tile into both CTAs'
+//               tile-slot rings (the peer's through distributed shared
+//               memory).  The 10 consumers of a slot (both CTAs' epilogue
+//               warps, CTA 0's MMA thread, CTA 1's producer) release it on
+//               CTA 0's barrier.
+//   release     the MMA commits arrive on both CTAs' `empty` and `tmem_full`
+//               barriers (multicast); the 8 epilogue warps release an
+//               accumulator on CTA 0's `tmem_empty` barrier.
+//
+// Every wait is bounded.  A CTA whose wait runs out records MK_ERR_TIMEOUT and
+// raises the abort word of both CTAs; both leave through one cluster barrier,
+// so neither exits while the other may still touch its shared memory.
+#include <algorithm>
+
+#include "gemm_impl.cuh"
+
+namespace mk {
+namespace {
+
+using namespace gemm_detail;
+
+constexpr int PSTAGES = 6;
+constexpr int PAIR_M = 2 * BM;                          // rows per pair tile
+constexpr uint32_t PA_BYTES = BM * BK * 2;              // this CTA's 128 A rows, one k-block
+constexpr uint32_t PB_BYTES = (MMA_N / 2) * BK * 2;     // this CTA's 128 of the 256 B rows
+constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;  // 32 KB
+constexpr uint32_t PTX_BYTES = 2 * PSTAGE_BYTES;        // both CTAs' copies of one stage
+constexpr uint32_t PIDESC = idesc_bf16_f32(PAIR_M, MMA_N);
+constexpr uint32_t PIDESC_HALF = idesc_bf16_f32(BM, MMA_N);  // 128-row pair tile, 64 rows per CTA
+constexpr int kPairNGroup = 4;
+constexpr int kPairSlots = 4;
+constexpr uint32_t kSlotConsumers = 10;  // CTA 0: MMA + 4 epilogue warps; CTA 1: producer + 4 epilogue warps
+
+struct PairCtl {
+    uint64_t full[PSTAGES];   // CTA 0: both CTAs' copies of the stage landed
+    uint64_t empty[PSTAGES];  // each CTA: the pair MMAs that read the stage are done
+    uint64_t tmem_full[2];    // each CTA: accumulator complete
+    uint64_t tmem_empty[2];   // CTA 0: all 8 epilogue warps have read the accumulator
+    uint64_t drain;           // CTA 0: every MMA issued has completed
+    uint64_t slot_full[kPairSlots];   // each CTA: CTA 0 wrote the tile slot
+    uint64_t slot_empty[kPairSlots];  // CTA 0: the slot's 10 consumers have read it
+    int4 slot[kPairSlots];            // {e, row0, rows, n0}; e < 0 ends the list
+    uint32_t tmem_base;
+    uint32_t abort_flag;
+    uint32_t zero;
+    int32_t off[kMaxExperts + 1];     // expert row offsets
+    int32_t pstart[kMaxExperts + 1];  // prefix over experts of their pair blocks
+};
+
+constexpr size_t PSMEM_BYTES = static_cast<size_t>(PSTAGES) * PSTAGE_BYTES + sizeof(PairCtl) + 1024;
+
+struct PairParams {
+    const int32_t* offsets;      // [E+1]
+    const int32_t* mtile_start;  // [E+1] prefix of ceil(rows / 128); all zero when offsets were rejected
+    const float* row_weight;     // gemm2 only, may be null
+    bf16* out;
+    int64_t out_ld;
+    int E;
+    int n_tiles;        // N blocks per pair block
+    int tile_n;         // output columns per tile (128 gemm1, 256 gemm2)
+    int n_valid;        // output columns of the whole GEMM
+    int k_blocks;       // K / 64
+    int b_rows_per_expert;
+    int b_half_rows;    // row offset of CTA 1's half of B in a full tile (gemm1 0: own map; gemm2 128)
+    uint32_t* status;
+    uint64_t timeout_ns;
+    int stall_first_stage;  // test hook: CTA 0 of the pair that claims tile 0 never loads its first stage
+    uint32_t* ticket;       // a zeroed word: tiles claimed so far
+};
+
+struct PairTile {
+    int e;
+    int row0;  // first row of the pair block
+    int rows;  // valid rows of the pair block (1..256); <= 128 makes it a half tile
+    int n0;
+};
+
+// Tile t -> (expert, pair block, N block): an expert's tiles occupy
+// [pstart[e] * n_tiles, pstart[e + 1] * n_tiles), in groups of kPairNGroup N
+// blocks, each group over all the expert's pair blocks, N fastest.
+__device__ __forceinline__ PairTile decode_pair_tile(int tile, const PairCtl* ctl, const PairParams& p) {
+    const int g = tile / p.n_tiles;
+    int lo = 0, hi = p.E - 1;  // largest e with pstart[e] <= g
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (ctl->pstart[mid] <= g)
+            lo = mid;
+        else
+            hi = mid - 1;
+    }
+    const int p_e = ctl->pstart[lo + 1] - ctl->pstart[lo];
+    const int l = tile - ctl->pstart[lo] * p.n_tiles;
+    const int q = l / (p_e * kPairNGroup);
+    const int nb = min(kPairNGroup, p.n_tiles - q * kPairNGroup);
+    const int r = l - q * p_e * kPairNGroup;
+    const int j = r / nb;
+    const int nt = q * kPairNGroup + (r - j * nb);
+    const int off = ctl->off[lo];
+    const int cnt = ctl->off[lo + 1] - off;
+    PairTile t;
+    t.e = lo;
+    t.row0 = off + j * PAIR_M;
+    t.rows = min(PAIR_M, cnt - j * PAIR_M);
+    t.n0 = nt * p.tile_n;
+    return t;
+}
+
+__device__ __forceinline__ void raise_abort(PairCtl* ctl, uint32_t peer) {
+    ctl->abort_flag = 1u;
+    st_shared_cluster_u32(mapa_shared(smem_u32(&ctl->abort_flag), peer), 1u);
+}
+
+template <int MODE>  // 0: gemm1 + SwiGLU, 1: gemm2 + row weight
+__global__ void __launch_bounds__(NUM_THREADS, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
+                             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0h,
+                             const __grid_constant__ CUtensorMap tmB1h, const PairParams p) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    PairCtl* ctl = reinterpret_cast<PairCtl*>(smem + PSTAGES * PSTAGE_BYTES);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+
+    // Tile tables in shared memory: row offsets, and the pair-block prefix
+    // (an expert with t 128-row blocks has ceil(t / 2) pair blocks).
+    for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) ctl->off[i] = p.offsets[i];
+    if (warp == 0) {
+        int cnt[kMaxExperts / 32], sum = 0;
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane * (kMaxExperts / 32) + i;
+            cnt[i] = (e < p.E) ? (p.mtile_start[e + 1] - p.mtile_start[e] + 1) / 2 : 0;
+            sum += cnt[i];
+        }
+        int inc = sum;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int u = __shfl_up_sync(0xffffffffu, inc, o);
+            if (lane >= o) inc += u;
+        }
+        int run = inc - sum;
+#pragma unroll
+        for (int i = 0; i < kMaxExperts / 32; ++i) {
+            const int e = lane * (kMaxExperts / 32) + i;
+            if (e < p.E) ctl->pstart[e] = run;
+            run += cnt[i];
+        }
+        if (lane == 31) ctl->pstart[p.E] = inc;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < PSTAGES; ++s) {
+            mbar_init(smem_u32(&ctl->full[s]), 1);
+            mbar_init(smem_u32(&ctl->empty[s]), 1);
+        }
+        for (int a = 0; a < 2; ++a) {
+            mbar_init(smem_u32(&ctl->tmem_full[a]), 1);
+            mbar_init(smem_u32(&ctl->tmem_empty[a]), 8);
+        }
+        for (int i = 0; i < kPairSlots; ++i) {
+            mbar_init(smem_u32(&ctl->slot_full[i]), 1);
+            mbar_init(smem_u32(&ctl->slot_empty[i]), kSlotConsumers);
+        }
+        mbar_init(smem_u32(&ctl->drain), 1);
+        ctl->abort_flag = 0;
+        ctl->zero = 0;
+        fence_mbar_init();
+        prefetch_tensormap(&tmA);
+        prefetch_tensormap(&tmB0);
+        if (MODE == 0) {
+            prefetch_tensormap(&tmB1);
+            prefetch_tensormap(&tmB0h);
+            prefetch_tensormap(&tmB1h);
+        }
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
+        tmem_relinquish_pair();
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers exist before any copy, commit or arrive targets them
+    tc_fence_after();
+    const uint32_t tmem_base = ctl->tmem_base;
+    volatile uint32_t* abort_word = &ctl->abort_flag;
+    const volatile uint32_t* never = &ctl->zero;
+    const int total_tiles = ctl->pstart[p.E] * p.n_tiles;
+    const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);  // CTA 0's barriers
+
+    if (warp == 0) {
+        if (lane == 0) {
+            // ------------------------------------------------ claims (CTA 0) + TMA producer (both)
+            const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);
+            const uint32_t peer_slot0 = mapa_shared(smem_u32(&ctl->slot[0]), peer);
+            const uint32_t peer_slot_full0 = mapa_shared(smem_u32(&ctl->slot_full[0]), peer);
+            const CUtensorMap* mb = (MODE == 0 && rank == 1) ? &tmB1 : &tmB0;
+            uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
+            bool ok = true;
+            uint32_t tk = (rank == 0) ? atomicAdd(p.ticket, 1u) : 0u;
+            for (;;) {
+                int4 info;
+                int cur_tile = -1;  // CTA 0 only: the claimed tile's index
+                if (rank == 0) {
+                    const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
+                    cur_tile = tile;
+                    info = make_int4(-1, 0, 0, 0);
+                    if (tile >= 0) {
+                        const PairTile ti = decode_pair_tile(tile, ctl, p);
+                        info = make_int4(ti.e, ti.row0, ti.rows, ti.n0);
+                    }
+                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]), slot_phase ^ 1u, abort_word,
+                                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    ctl->slot[slot] = info;
+                    st_shared_cluster_v4(peer_slot0 + slot * static_cast<uint32_t>(sizeof(int4)), info);
+                    mbar_arrive(smem_u32(&ctl->slot_full[slot]));
+                    mbar_arrive_cluster(peer_slot_full0 + slot * 8u);
+                    if (tile >= 0) tk = atomicAdd(p.ticket, 1u);  // used after this tile's loads
+                } else {
+                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word,
+                                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    info = ctl->slot[slot];
+                    mbar_arrive_cluster(slot_empty0 + slot * 8u);
+                }
+                if (++slot == kPairSlots) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+                if (info.x < 0) break;
+                const bool half = info.z <= BM;
+                const int a_row = info.y + static_cast<int>(rank) * (half ? BM / 2 : BM);
+                // gemm1 half tile: W1 rows [n0 + 64 r, +64) then the same rows of W3
+                const int b_row = info.x * p.b_rows_per_expert + info.w +
+                                  static_cast<int>(rank) * ((MODE == 0 && half) ? BM / 2 : p.b_half_rows);
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word,
+                                                   p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
+                    const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
+                    const uint32_t sb = sa + PA_BYTES;
+                    if (rank == 0) {
+                        mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), PTX_BYTES);
+                        issued |= 1u << stage;
+                        last_par = (last_par & ~(1u << stage)) | (phase << stage);
+                    }
+                    const bool stall = p.stall_first_stage && rank == 0 && cur_tile == 0 && kb == 0;
+                    if (!stall) {  // injected stall: the stage is armed but this CTA's half never comes
+                        tma_load_2d_pair(sa, &tmA, kb * BK, a_row, fb);
+                        if (MODE == 0 && half) {
+                            tma_load_2d_pair(sb, &tmB0h, kb * BK, b_row, fb);
+                            tma_load_2d_pair(sb + PB_BYTES / 2, &tmB1h, kb * BK, b_row, fb);
+                        } else {
+                            tma_load_2d_pair(sb, mb, kb * BK, b_row, fb);
+                        }
+                    }
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+            }
+            if (!ok) {
+                raise_abort(ctl, peer);
+                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+            }
+            // CTA 0: every stage it armed completes (or times out) before the CTA exits.
+            for (int s = 0; s < PSTAGES; ++s)
+                if ((issued >> s) & 1u)
+                    mbar_wait_bounded_cluster(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
+        }
+        __syncwarp();
+    } else if (warp == 1) {
+        if (lane == 0 && rank == 0) {
+            // ------------------------------------------------ MMA issuer (CTA 0 only)
+            uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0, slot_phase = 0;
+            bool ok = true;
+            for (;;) {
+                if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word,
+                                               p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                const int4 info = ctl->slot[slot];
+                mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
+                if (++slot == kPairSlots) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+                if (info.x < 0) break;
+                const uint32_t idesc = info.z <= BM ? PIDESC_HALF : PIDESC;
+                if (!mbar_wait_bounded_cluster(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, abort_word,
+                                               p.timeout_ns)) {
+                    ok = false;
+                    break;
+                }
+                tc_fence_after();
+                const uint32_t d_tmem = tmem_base + acc * MMA_N;
+                for (int kb = 0; kb < p.k_blocks; ++kb) {
+                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->full[stage]), phase, abort_word, p.timeout_ns)) {
+                        ok = false;
+                        break;
+                    }
+                    tc_fence_after();
+                    const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
+                    const uint32_t sb = sa + PA_BYTES;
+#pragma unroll
+                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                        const uint64_t ad = sw128_kmajor_desc(sa + kk * UMMA_K * 2);
+                        const uint64_t bd = sw128_kmajor_desc(sb + kk * UMMA_K * 2);
+                        mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                    }
+                    mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), 0x3);
+                    if (++stage == PSTAGES) {
+                        stage = 0;
+                        phase ^= 1u;
+                    }
+                }
+                if (!ok) break;
+                mma_commit_pair_mc(smem_u32(&ctl->tmem_full[acc]), 0x3);
+                acc ^= 1u;
+                if (acc == 0) acc_phase ^= 1u;
+            }
+            if (!ok) {
+                raise_abort(ctl, peer);
+                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+            }
+            // All MMAs issued complete before either CTA frees TMEM or shared memory.
+            mma_commit_pair_mc(smem_u32(&ctl->drain), 0x1);
+            if (!mbar_wait_bounded_cluster(smem_u32(&ctl->drain), 0u, never, p.timeout_ns))
+                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmDrain);
+        }
+        __syncwarp();
+    } else {
+        // ---------------------------------------------------- epilogue (both CTAs)
+        const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
+        const int lane_in_tile = sub * 32 + lane;
+        const uint32_t tmem_empty0 = mapa_shared(smem_u32(&ctl->tmem_empty[0]), 0);
+        uint32_t acc = 0, acc_phase = 0, slot = 0, slot_phase = 0;
+        bool ok = true;
+        for (;;) {
+            if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            const int4 info = ctl->slot[slot];
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(slot_empty0 + slot * 8u);
+            if (++slot == kPairSlots) {
+                slot = 0;
+                slot_phase ^= 1u;
+            }
+            if (info.x < 0) break;
+            if (!mbar_wait_bounded_cluster(smem_u32(&ctl->tmem_full[acc]), acc_phase, abort_word, p.timeout_ns)) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * MMA_N;
+            const bool half = info.z <= BM;
+            // full tile: TMEM lane = row of this CTA's 128; half tile: lane & 63 =
+            // row of this CTA's 64, lane >> 6 = which half of the output columns
+            const int rows_per_cta = half ? BM / 2 : BM;
+            const int row_here = half ? (lane_in_tile & 63) : lane_in_tile;
+            const int col_half = half ? (lane_in_tile >> 6) : 0;
+            const bool row_ok = static_cast<int>(rank) * rows_per_cta + row_here < info.z;
+            const int64_t r = static_cast<int64_t>(info.y) + static_cast<int>(rank) * rows_per_cta + row_here;
+            bf16* orow = p.out + (row_ok ? r : 0) * p.out_ld;
+            if (MODE == 0) {
+                if (half)
+                    epilogue_swiglu_w<64>(tbase, row_ok, orow, info.w + 64 * col_half, p.n_valid);
+                else
+                    epilogue_swiglu(tbase, row_ok, orow, info.w, p.n_valid);
+            } else {
+                const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
+                if (half)
+                    epilogue_weighted_w<MMA_N / 2>(tbase, row_ok, orow, info.w + (MMA_N / 2) * col_half, p.n_valid,
+                                                   wr);
+                else
+                    epilogue_weighted(tbase, row_ok, orow, info.w, p.n_valid, wr);
+            }
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive_cluster(tmem_empty0 + acc * 8u);
+            acc ^= 1u;
+            if (acc == 0) acc_phase ^= 1u;
+        }
+        if (!ok && lane == 0) {
+            raise_abort(ctl, peer);
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmEpilogue);
+        }
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // neither CTA leaves while the other may still use its shared memory
+    if (*abort_word != 0u && threadIdx.x == 0) {
+        // After a timeout, copies the peer started may still complete on CTA 0's
+        // barriers: keep both CTAs resident a little longer (bounded) before exit.
+        const uint64_t t0 = globaltimer_ns();
+        while (globaltimer_ns() - t0 < 200000ull) {
+        }
+    }
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc_pair(tmem_base, TMEM_COLS);
+    }
+}
+
+// ------------------------------------------------------------------ host side
+
+template <int MODE>
+cudaError_t launch_pair_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
+                             const CUtensorMap& b0h, const CUtensorMap& b1h, const PairParams& p, int64_t S,
+                             cudaStream_t s) {
+    static int configured[64] = {0};
+    static int max_clusters[64] = {0};
+    int dev = 0;
+    cudaError_t err = cudaGetDevice(&dev);
+    if (err != cudaSuccess) return err;
+    const int slot = dev < 64 ? dev : 0;
+    auto fn = grouped_gemm_pair_kernel<MODE>;
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.dynamicSmemBytes = PSMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (dev >= 64 || !configured[dev]) {
+        err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PSMEM_BYTES));
+        if (err != cudaSuccess) return err;
+        cfg.gridDim = dim3(2 * std::max(1, device_sm_count() / 2));
+        int n = 0;
+        err = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
+        if (err != cudaSuccess) return err;
+        if (n < 1) return cudaErrorInvalidConfiguration;
+        max_clusters[slot] = n;
+        if (dev < 64) configured[dev] = 1;
+    }
+    // Upper bound on the pair tiles: every expert adds at most one partial block.
+    const int64_t max_tiles = ((S + PAIR_M - 1) / PAIR_M + p.E) * static_cast<int64_t>(p.n_tiles);
+    const int clusters = static_cast<int>(std::min<int64_t>(max_clusters[slot], std::max<int64_t>(max_tiles, 1)));
+    cfg.gridDim = dim3(2 * clusters);
+    err = cudaLaunchKernelEx(&cfg, fn, a, b0, b1, b0h, b1h, p);
+    if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s) {
+    CUtensorMap ma, mb0, mb1, mb0h, mb1h;
+    const uint64_t wrows = static_cast<uint64_t>(a.E) * a.f;
+    if (!make_map(&ma, a.x_perm, a.d, a.S, BM) || !make_map(&mb0, a.w1, a.d, wrows, MMA_N / 2) ||
+        !make_map(&mb1, a.w3, a.d, wrows, MMA_N / 2) || !make_map(&mb0h, a.w1, a.d, wrows, MMA_N / 4) ||
+        !make_map(&mb1h, a.w3, a.d, wrows, MMA_N / 4))
+        return cudaErrorInvalidValue;
+    PairParams p;
+    p.offsets = a.offsets;
+    p.mtile_start = a.mtile_start;
+    p.row_weight = nullptr;
+    p.out = a.h;
+    p.out_ld = a.f;
+    p.E = a.E;
+    p.tile_n = MMA_N / 2;
+    p.n_tiles = (a.f + p.tile_n - 1) / p.tile_n;
+    p.n_valid = a.f;
+    p.k_blocks = a.d / BK;
+    p.b_rows_per_expert = a.f;
+    p.b_half_rows = 0;  // full tiles: CTA 1 reads the same rows of W3 through its own map
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
+    p.ticket = a.tickets;
+    return launch_pair_mode<0>(ma, mb0, mb1, mb0h, mb1h, p, a.S, s);
+}
+
+cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s) {
+    CUtensorMap ma, mb0;
+    if (!make_map(&ma, a.h, a.f, a.S, BM) ||
+        !make_map(&mb0, a.w2, a.f, static_cast<uint64_t>(a.E) * a.d, MMA_N / 2))
+        return cudaErrorInvalidValue;
+    PairParams p;
+    p.offsets = a.offsets;
+    p.mtile_start = a.mtile_start;
+    p.row_weight = a.row_weight;
+    p.out = a.P;
+    p.out_ld = a.d;
+    p.E = a.E;
+    p.tile_n = MMA_N;
+    p.n_tiles = (a.d + p.tile_n - 1) / p.tile_n;
+    p.n_valid = a.d;
+    p.k_blocks = a.f / BK;
+    p.b_rows_per_expert = a.d;
+    p.b_half_rows = MMA_N / 2;
+    p.status = a.status;
+    p.timeout_ns = a.timeout_ns;
+    p.stall_first_stage = 0;
+    p.ticket = a.tickets + 1;
+    return launch_pair_mode<1>(ma, mb0, mb0, mb0, mb0, p, a.S, s);
+}
+
+// CTA pairs when experts hold 256 rows or more on average, single CTAs below:
+// with a few rows per expert the layer streams weights from HBM and the pair
+// tiles' extra rows cost more than the split operands save (same GPU,
+// alternating builds: large -6%, skewed -6%, mid -3%, decode +5% on pairs).
+bool use_pairs(const FfnArgs& a) { return a.S >= static_cast<int64_t>(PAIR_M) * a.E; }
+
+cudaError_t launch_gemm1_auto(const FfnArgs& a, cudaStream_t s) {
+    return use_pairs(a) ? launch_gemm1_pair(a, s) : launch_gemm1(a, s);
+}
+
+cudaError_t launch_gemm2_auto(const FfnArgs& a, cudaStream_t s) {
+    return use_pairs(a) ? launch_gemm2_pair(a, s) : launch_gemm2(a, s);
+}
+
+}  // namespace mk

@@ -111,6 +111,12 @@ struct FfnArgs {
     uint32_t* tickets;           // 2 zeroed words: tile tickets of gemm1 [0] and gemm2 [1]
 };
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
+// The same GEMMs on CTA pairs (tcgen05 cta_group::2; gemm_pair.cu).
+cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s);
+// Pairs when S >= 256 E (experts of 256+ rows on average), else single CTAs.
+cudaError_t launch_gemm1_auto(const FfnArgs& a, cudaStream_t s);
+cudaError_t launch_gemm2_auto(const FfnArgs& a, cudaStream_t s);
 
 // Fused persistent kernel: tickets, role accounting and cost sums (followed in
 // the workspace by the per-token-group, per-chunk and per-M-tile counters).
