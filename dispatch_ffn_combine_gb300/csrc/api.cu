@@ -532,6 +532,17 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     if (st != MK_OK) return st;
     const bf16* P = at<bf16>(ws, L.P);
     const int32_t* slot_row = at<int32_t>(ws, L.slot_row);
+    // y_host page-locked and mapped for the device: the combine writes it
+    // directly over the host link, no staging and no separate download
+    cudaPointerAttributes ya{};
+    if (cudaPointerGetAttributes(&ya, y_host) == cudaSuccess && ya.type == cudaMemoryTypeHost &&
+        ya.devicePointer != nullptr) {
+        MK_TRY(launch_combine(P, slot_row, T, d, k, static_cast<bf16*>(ya.devicePointer), s));
+        if (opts && opts->phase_events && opts->phase_events[MK_PHASE_COUNT_ALL])
+            MK_TRY(cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[MK_PHASE_COUNT_ALL]), s));
+        return MK_OK;
+    }
+    cudaGetLastError();  // a pointer unknown to CUDA (pageable memory) is not an error here
     // about 16 MB of output per chunk (1 to kHostChunks chunks): small layers
     // gain nothing from splitting and would pay a launch and a copy per chunk
     const int chunks = static_cast<int>(std::min<int64_t>(kHostChunks, std::max<int64_t>(1, bytes >> 24)));

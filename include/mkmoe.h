@@ -210,8 +210,10 @@ MK_API mk_status mk_moe_layer(const void* x, const float* wg, const float* bias,
  * On the kernel-per-step path the copies run on two copy streams the library
  * keeps per (device, workspace): the upload of x waits only until the
  * previous call on `ws` has read its staged x, so it overlaps that call's
- * GEMMs, and y is combined and downloaded in token chunks (~16 MB each, up
- * to 8) while later chunks are still being combined.  The library
+ * GEMMs.  If y_host is page-locked memory mapped for the device, the combine
+ * writes y straight into it; otherwise y is combined and downloaded in token
+ * chunks (~16 MB each, up to 8) while later chunks are still being combined.
+ * The library
  * creates those streams and events on a workspace's first call (and keeps a
  * few sets); device memory is still only the caller's. */
 MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bias,
