@@ -93,15 +93,18 @@ def test_layer_host_buffers_match_device_call():
 @pytest.mark.parametrize("T", [7, 1000])
 def test_layer_host_calls_back_to_back(T):
     """Host-buffer calls issued back to back on one workspace (their copies
-    overlap the previous call's kernels), alternating paths and inputs: every
-    y_host equals the device-buffer result for its own input."""
+    overlap the previous call's kernels), alternating paths, inputs and
+    pinned / pageable outputs: every y_host equals the device-buffer result
+    for its own input."""
     wl = Workload("ragged", T=T)
     c = wl.cfg
     ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
     g = torch.Generator().manual_seed(7)
     xs = [wl.g["x"].cpu()] + [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(3)]
     xs_host = [x.pin_memory() for x in xs]
-    ys_host = [torch.empty((wl.T, c.d), dtype=torch.bfloat16).pin_memory() for _ in xs]
+    # pinned outputs take the direct write, pageable ones the chunked downloads
+    ys_host = [torch.empty((wl.T, c.d), dtype=torch.bfloat16) for _ in xs]
+    ys_host = [y.pin_memory() if i % 2 == 0 else y for i, y in enumerate(ys_host)]
     paths = [mk.MK_PATH_STEPS, mk.MK_PATH_STEPS, mk.MK_PATH_FUSED, mk.MK_PATH_STEPS]
     args = (wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
     for xh, yh, path in zip(xs_host, ys_host, paths):
