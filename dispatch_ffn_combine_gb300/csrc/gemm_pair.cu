@@ -18,8 +18,8 @@
 //               every lane holds matching gate and up columns.  The pair thus
 //               computes no more rows than the single-CTA kernel.
 //   why         per SM and k-block, 32 KB of operands cross L2 and shared
-//               memory instead of 48 KB (B is split, not duplicated), so six
-//               stages (3072 cycles of MMA work) fit instead of four.
+//               memory instead of 48 KB (B is split, not duplicated), so seven
+//               stages (3584 cycles of MMA work) fit instead of four.
 //   copies      each CTA loads its own A and B halves with TMA; all four
 //               copies of a stage complete on CTA 0's `full` barrier, which
 //               CTA 0 arms with both CTAs' bytes.
@@ -47,7 +47,7 @@ namespace {
 
 using namespace gemm_detail;
 
-constexpr int PSTAGES = 6;
+constexpr int PSTAGES = 7;  // 224 KB: the most 32 KB stages that fit beside the control block
 constexpr int PAIR_M = 2 * BM;                          // rows per pair tile
 constexpr uint32_t PA_BYTES = BM * BK * 2;              // this CTA's 128 A rows, one k-block
 constexpr uint32_t PB_BYTES = (MMA_N / 2) * BK * 2;     // this CTA's 128 of the 256 B rows
@@ -71,11 +71,12 @@ struct PairCtl {
     uint32_t tmem_base;
     uint32_t abort_flag;
     uint32_t zero;
-    int32_t off[kMaxExperts + 1];     // expert row offsets
     int32_t pstart[kMaxExperts + 1];  // prefix over experts of their pair blocks
 };
 
+// + 1024: the stages start at the first 1024-byte boundary (128-byte swizzle atoms)
 constexpr size_t PSMEM_BYTES = static_cast<size_t>(PSTAGES) * PSTAGE_BYTES + sizeof(PairCtl) + 1024;
+static_assert(PSMEM_BYTES <= 227u * 1024u, "pair GEMM shared memory exceeds the per-CTA limit");
 
 struct PairParams {
     const int32_t* offsets;      // [E+1]
@@ -123,8 +124,8 @@ __device__ __forceinline__ PairTile decode_pair_tile(int tile, const PairCtl* ct
     const int r = l - q * p_e * kPairNGroup;
     const int j = r / nb;
     const int nt = q * kPairNGroup + (r - j * nb);
-    const int off = ctl->off[lo];
-    const int cnt = ctl->off[lo + 1] - off;
+    const int off = __ldg(p.offsets + lo);
+    const int cnt = __ldg(p.offsets + lo + 1) - off;
     PairTile t;
     t.e = lo;
     t.row0 = off + j * PAIR_M;
@@ -151,9 +152,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t rank = cluster_ctarank();
     const uint32_t peer = rank ^ 1u;
 
-    // Tile tables in shared memory: row offsets, and the pair-block prefix
-    // (an expert with t 128-row blocks has ceil(t / 2) pair blocks).
-    for (int i = threadIdx.x; i <= p.E; i += NUM_THREADS) ctl->off[i] = p.offsets[i];
+    // Tile table in shared memory: the pair-block prefix (an expert with t
+    // 128-row blocks has ceil(t / 2) pair blocks).
     if (warp == 0) {
         int cnt[kMaxExperts / 32], sum = 0;
 #pragma unroll
