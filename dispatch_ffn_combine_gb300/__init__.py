@@ -35,7 +35,9 @@ ENTRY_POINTS = (
     "mk_moe_workspace_size", "mk_moe_route", "mk_moe_dispatch", "mk_moe_expert_ffn", "mk_moe_combine",
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
     "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count", "mk_moe_route_fallbacks",
+    "mk_moe_grouped_gemm", "mk_moe_dispatch_gemm_workspace_size", "mk_moe_dispatch_gemm",
 )
+_SIZE_RESULT = ("mk_moe_workspace_size", "mk_moe_dispatch_gemm_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -84,8 +86,12 @@ def load_library():
         lib.mk_moe_route_noalloc.argtypes = [P, P, P, I64, I, I, I, P, P, P, P]
         lib.mk_moe_layer_trace_count.argtypes = [P, I64, I, I, I, I, P, ctypes.POINTER(ctypes.c_uint32)]
         lib.mk_moe_route_fallbacks.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
+        lib.mk_moe_grouped_gemm.argtypes = [P, P, P, P, I64, I, I, I, P, P, SZ, P]
+        lib.mk_moe_dispatch_gemm_workspace_size.restype = SZ
+        lib.mk_moe_dispatch_gemm_workspace_size.argtypes = [I64, I, I, I]
+        lib.mk_moe_dispatch_gemm.argtypes = [P, P, P, P, I64, I, I, I, I, P, P, P, P, P, SZ, P]
         for name in ENTRY_POINTS:
-            if name not in ("mk_moe_workspace_size", "mk_moe_status_string"):
+            if name not in _SIZE_RESULT + ("mk_moe_status_string",):
                 getattr(lib, name).restype = I
         _lib = lib
         return lib
@@ -217,6 +223,67 @@ def mk_moe_expert_ffn(x_perm, expert_offsets, row_weight, w1, w3, w2, h=None, P=
                                           S, d, E, f, _p(h), _p(P), _p(ws), ws.numel(), _stream(stream))
     _check(st, "mk_moe_expert_ffn")
     return h, P
+
+
+def mk_moe_grouped_gemm(x_perm, expert_offsets, w, row_weight=None, out=None, ws=None, stream=None):
+    """Grouped GEMM on dispatched rows: out[r] = row_weight[r] * x_perm[r] @ w[e].T for the
+    rows r of expert e (row_weight None = 1); returns out [S, n] bf16."""
+    S, d = x_perm.shape
+    E, n, _ = w.shape
+    _need(x_perm, torch.bfloat16, (S, d), "x_perm")
+    _need(expert_offsets, torch.int32, (E + 1,), "expert_offsets")
+    _need(w, torch.bfloat16, (E, n, d), "w")
+    if row_weight is not None:
+        _need(row_weight, torch.float32, (S,), "row_weight")
+    dev = x_perm.device
+    out = torch.empty((S, n), dtype=torch.bfloat16, device=dev) if out is None else out
+    _need(out, torch.bfloat16, (S, n), "out")
+    ws = torch.empty(256 + 4 * (E + 1), dtype=torch.uint8, device=dev) if ws is None else ws
+    st = load_library().mk_moe_grouped_gemm(_p(x_perm), _p(expert_offsets), _p(row_weight), _p(w), S, d, E, n,
+                                            _p(out), _p(ws), ws.numel(), _stream(stream))
+    _check(st, "mk_moe_grouped_gemm")
+    return out
+
+
+def dispatch_gemm_workspace_size(T: int, d: int, E: int, k: int) -> int:
+    return int(load_library().mk_moe_dispatch_gemm_workspace_size(T, d, E, k))
+
+
+def alloc_dispatch_gemm_workspace(T: int, d: int, E: int, k: int, device="cuda") -> torch.Tensor:
+    n = dispatch_gemm_workspace_size(T, d, E, k)
+    if n == 0:
+        raise ValueError("invalid sizes for Dispatch + GEMM")
+    return torch.empty(n, dtype=torch.uint8, device=device)
+
+
+def mk_moe_dispatch_gemm(x, wg, bias, w, k, out=None, ws=None, stream=None, row_weight=True):
+    """MoE Dispatch + GEMM: route, dispatch, and each expert's GEMM on its rows.
+
+    Returns dict(out [T*k, n] bf16 rows grouped by expert, expert_offsets [E+1],
+    row_token [T*k], row_weight [T*k] fp32 or None when row_weight=False)."""
+    T, d = x.shape
+    E, n, _ = w.shape
+    _need(x, torch.bfloat16, (T, d), "x")
+    _need(wg, torch.float32, (E, d), "wg")
+    if bias is not None:
+        _need(bias, torch.float32, (E,), "bias")
+    _need(w, torch.bfloat16, (E, n, d), "w")
+    dev = x.device
+    o = out or {}
+    res = {
+        "out": o.get("out", torch.empty((T * k, n), dtype=torch.bfloat16, device=dev)),
+        "expert_offsets": o.get("expert_offsets", torch.empty(E + 1, dtype=torch.int32, device=dev)),
+        "row_token": o.get("row_token", torch.empty(T * k, dtype=torch.int32, device=dev)),
+        "row_weight": (o.get("row_weight", torch.empty(T * k, dtype=torch.float32, device=dev))
+                       if row_weight else None),
+    }
+    _need(res["out"], torch.bfloat16, (T * k, n), "out")
+    ws = alloc_dispatch_gemm_workspace(T, d, E, k, dev) if ws is None else ws
+    st = load_library().mk_moe_dispatch_gemm(_p(x), _p(wg), _p(bias), _p(w), T, d, E, k, n, _p(res["out"]),
+                                             _p(res["expert_offsets"]), _p(res["row_token"]), _p(res["row_weight"]),
+                                             _p(ws), ws.numel(), _stream(stream))
+    _check(st, "mk_moe_dispatch_gemm")
+    return res
 
 
 def mk_moe_combine(P, slot_row, y=None, stream=None):

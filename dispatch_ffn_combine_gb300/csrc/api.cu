@@ -12,7 +12,10 @@ constexpr size_t kAlign = 256;
 size_t align_up(size_t v) { return (v + kAlign - 1) & ~(kAlign - 1); }
 }  // namespace
 
-WsLayout ws_layout(int64_t T, int d, int E, int k, int f) {
+namespace {
+// full: the layer's regions after x_perm (h, P, the fused kernel's flags, the
+// host-buffer staging) are laid out too.
+WsLayout make_layout(int64_t T, int d, int E, int k, int f, bool full) {
     WsLayout L;
     const size_t S = static_cast<size_t>(T) * k;
     const size_t nch = static_cast<size_t>(num_chunks(T));
@@ -38,6 +41,10 @@ WsLayout ws_layout(int64_t T, int d, int E, int k, int f) {
     L.row_weight = take(S * 4);
     L.slot_row = take(S * 4);
     L.x_perm = take(S * d * 2);
+    if (!full) {
+        L.total = o;
+        return L;
+    }
     L.h = take(S * f * 2);
     L.P = take(S * d * 2);
     L.sync = take(fused_sync_bytes(T, E, k));
@@ -46,6 +53,11 @@ WsLayout ws_layout(int64_t T, int d, int E, int k, int f) {
     L.total = o;
     return L;
 }
+}  // namespace
+
+WsLayout ws_layout(int64_t T, int d, int E, int k, int f) { return make_layout(T, d, E, k, f, true); }
+
+WsLayout ws_layout_dispatch(int64_t T, int d, int E, int k) { return make_layout(T, d, E, k, 64, false); }
 
 int device_sm_count() {
     static int cache[64] = {0};
@@ -108,6 +120,29 @@ Tp* at(void* ws, size_t off) {
         const cudaError_t _e = (expr);               \
         if (_e != cudaSuccess) return MK_ERR_CUDA;   \
     } while (0)
+
+// out[r] = row_weight[r] * (x_perm[r] W_e^T): the second GEMM's kernel with
+// K = d and N = n (gemm2 of the FFN is the case K = ffn, N = d).
+cudaError_t launch_grouped_gemm(const bf16* x_perm, const int32_t* offsets, const int32_t* mtile,
+                                const float* row_weight, const bf16* w, int64_t S, int d, int E, int n, bf16* out,
+                                uint32_t* status, cudaStream_t s) {
+    FfnArgs a{};
+    a.offsets = offsets;
+    a.mtile_start = mtile;
+    a.row_weight = row_weight;
+    a.h = const_cast<bf16*>(x_perm);  // the A operand; only read
+    a.w2 = w;
+    a.S = S;
+    a.f = d;
+    a.d = n;
+    a.E = E;
+    a.P = out;
+    a.status = status;
+    a.timeout_ns = kDefaultTimeoutNs;
+    a.inject = 0;
+    a.tickets = status + 4;
+    return launch_gemm2_auto(a, s);
+}
 
 struct PhaseMarks {
     void** ev;
@@ -243,6 +278,28 @@ mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_offsets, c
     return MK_OK;
 }
 
+mk_status mk_moe_grouped_gemm(const void* x_perm, const int32_t* expert_offsets, const float* row_weight, const void* w,
+                              int64_t S, int d, int E, int n, void* out, void* ws, size_t ws_bytes, void* stream) {
+    mk_status st = check_sizes(S, d, E, 1, n);
+    if (st != MK_OK) return st;
+    if (S == 0) return MK_OK;
+    if (!x_perm || !expert_offsets || !w || !out) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x_perm) || !aligned16(w) || !aligned16(out)) return MK_ERR_INVALID_ARG;
+    // Needs only the control block and the tile table that follows it.
+    if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < 256 + 4 * (size_t(E) + 1))
+        return MK_ERR_WORKSPACE;
+    if ((st = device_ok()) != MK_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    uint32_t* status = at<uint32_t>(ws, 0);
+    int32_t* mtile = at<int32_t>(ws, 256);
+    MK_TRY(cudaMemsetAsync(status, 0, 8, s));       // status, site
+    MK_TRY(cudaMemsetAsync(status + 4, 0, 16, s));  // GEMM tile tickets
+    MK_TRY(launch_mtile_table(expert_offsets, E, S, mtile, status, s));
+    MK_TRY(launch_grouped_gemm(static_cast<const bf16*>(x_perm), expert_offsets, mtile, row_weight,
+                               static_cast<const bf16*>(w), S, d, E, n, static_cast<bf16*>(out), status, s));
+    return MK_OK;
+}
+
 mk_status mk_moe_combine(const void* P, const int32_t* slot_row, int64_t T, int d, int k, void* y, void* stream) {
     mk_status st = check_sizes(T, d, k, k, 64);
     if (st != MK_OK) return st;
@@ -265,6 +322,57 @@ struct LayerHooks {
     cudaEvent_t after_scatter = nullptr;  // recorded once x has been read for the last time
     bool skip_combine = false;            // the caller runs the combine itself (in chunks)
 };
+
+// Where the dispatch step writes (the layer's workspace, or the caller's buffers).
+struct DispatchOut {
+    int32_t* offsets;    // [E+1]
+    int32_t* row_token;  // [S]
+    float* row_weight;   // [S]
+    int32_t* slot_row;   // [T, k]
+    bf16* x_perm;        // [S, d]
+};
+
+// Route, count, scan and scatter, one kernel each on `s`: the steps the layer
+// and the Dispatch + GEMM entry point share.  The control block is zeroed by
+// the caller.
+mk_status route_dispatch_steps(const bf16* xb, const float* wg, const float* bias, int64_t T, int d, int E, int k,
+                               void* ws, const WsLayout& L, const DispatchOut& o, const mk_moe_opts* opts,
+                               const PhaseMarks& pm, cudaStream_t s) {
+    uint32_t* status = at<uint32_t>(ws, L.ctrl);
+    int32_t* ids = at<int32_t>(ws, L.ids);
+    float* w = at<float>(ws, L.w);
+    float* logits = at<float>(ws, L.logits);
+    int32_t* chunk_counts = at<int32_t>(ws, L.chunk_counts);
+    int32_t* chunk_base = at<int32_t>(ws, L.chunk_base);
+    int32_t* rank = at<int32_t>(ws, L.rank);
+    const uint64_t timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+    MK_TRY(pm.mark(MK_PHASE_ROUTE_LOGITS));
+    // The candidate filter pays off once the fixed-order work (T d E fused
+    // multiply-adds) is large and there are enough 128-token tiles to fill the
+    // GPU; below that the plain fixed-order router is faster.  Same bits.
+    const bool filter = route_tc_supported(d, E) && T >= 2048 &&
+                        static_cast<double>(T) * d * E >= 4294967296.0;
+    if (filter || (opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND && route_tc_supported(d, E))) {
+        MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
+                                   status, timeout_ns, s));
+        MK_TRY(pm.mark(MK_PHASE_TOPK));
+        MK_TRY(launch_route_select(xb, wg, bias, T, d, E, k, logits, at<float>(ws, L.wnorm), ids, w, nullptr,
+                                   status + 2, opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND, s));
+    } else {
+        MK_TRY(launch_route_logits(xb, wg, bias, T, d, E, logits, s));
+        MK_TRY(pm.mark(MK_PHASE_TOPK));
+        MK_TRY(launch_topk(logits, T, E, k, ids, w, nullptr, s));
+    }
+    MK_TRY(pm.mark(MK_PHASE_COUNT));
+    MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s));
+    MK_TRY(pm.mark(MK_PHASE_SCAN));
+    MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), o.offsets,
+                       at<int32_t>(ws, L.mtile_start), status + 3, s));
+    MK_TRY(pm.mark(MK_PHASE_SCATTER));
+    MK_TRY(launch_scatter(xb, ids, w, T, d, E, k, o.offsets, chunk_base, rank, o.x_perm, o.row_token, o.row_weight,
+                          o.slot_row, s));
+    return MK_OK;
+}
 
 mk_status layer_impl(const void* x, const float* wg, const float* bias, const void* w1, const void* w3,
                      const void* w2, int64_t T, int d, int E, int k, int ffn, void* y, void* ws,
@@ -325,33 +433,9 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
         for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
         return MK_OK;
     }
-    const bf16* xb = static_cast<const bf16*>(x);
-    const uint64_t timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
-    MK_TRY(pm.mark(MK_PHASE_ROUTE_LOGITS));
-    // The candidate filter pays off once the fixed-order work (T d E fused
-    // multiply-adds) is large and there are enough 128-token tiles to fill the
-    // GPU; below that the plain fixed-order router is faster.  Same bits.
-    const bool filter = route_tc_supported(d, E) && T >= 2048 &&
-                        static_cast<double>(T) * d * E >= 4294967296.0;
-    if (filter || (opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND && route_tc_supported(d, E))) {
-        MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
-                                   status, timeout_ns, s));
-        MK_TRY(pm.mark(MK_PHASE_TOPK));
-        MK_TRY(launch_route_select(xb, wg, bias, T, d, E, k, logits, at<float>(ws, L.wnorm), ids, w, nullptr,
-                                   status + 2, opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND, s));
-    } else {
-        MK_TRY(launch_route_logits(xb, wg, bias, T, d, E, logits, s));
-        MK_TRY(pm.mark(MK_PHASE_TOPK));
-        MK_TRY(launch_topk(logits, T, E, k, ids, w, nullptr, s));
-    }
-    MK_TRY(pm.mark(MK_PHASE_COUNT));
-    MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s));
-    MK_TRY(pm.mark(MK_PHASE_SCAN));
-    MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile,
-                       status + 3, s));
-    MK_TRY(pm.mark(MK_PHASE_SCATTER));
-    MK_TRY(launch_scatter(static_cast<const bf16*>(x), ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm,
-                          at<int32_t>(ws, L.row_token), row_weight, slot_row, s));
+    const DispatchOut dout{offsets, at<int32_t>(ws, L.row_token), row_weight, slot_row, x_perm};
+    mk_status st = route_dispatch_steps(static_cast<const bf16*>(x), wg, bias, T, d, E, k, ws, L, dout, opts, pm, s);
+    if (st != MK_OK) return st;
     if (hk.after_scatter != nullptr) MK_TRY(cudaEventRecord(hk.after_scatter, s));
     FfnArgs a;
     a.x_perm = x_perm;
@@ -484,6 +568,38 @@ mk_status mk_moe_layer(const void* x, const float* wg, const float* bias, const 
     if (st != MK_OK) return st;
     return layer_impl(x, wg, bias, w1, w3, w2, T, d, E, k, ffn, y, ws, ws_layout(T, d, E, k, ffn), opts,
                       static_cast<cudaStream_t>(stream), LayerHooks{});
+}
+
+size_t mk_moe_dispatch_gemm_workspace_size(int64_t T, int d, int E, int k) {
+    if (check_sizes(T, d, E, k, 64) != MK_OK) return 0;
+    return ws_layout_dispatch(T, d, E, k).total;
+}
+
+mk_status mk_moe_dispatch_gemm(const void* x, const float* wg, const float* bias, const void* w, int64_t T, int d,
+                               int E, int k, int n, void* out, int32_t* expert_offsets, int32_t* row_token,
+                               float* row_weight, void* ws, size_t ws_bytes, void* stream) {
+    mk_status st = check_sizes(T, d, E, k, n);
+    if (st != MK_OK) return st;
+    const WsLayout L = ws_layout_dispatch(T, d, E, k);
+    if ((st = check_ws(ws, ws_bytes, L)) != MK_OK) return st;
+    if (!expert_offsets) return MK_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T == 0) {  // x, out and row_token are empty (and may be NULL)
+        MK_TRY(cudaMemsetAsync(expert_offsets, 0, sizeof(int32_t) * (E + 1), s));
+        return MK_OK;
+    }
+    if (!x || !wg || !w || !out || !row_token) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wg) || !aligned16(w) || !aligned16(out)) return MK_ERR_INVALID_ARG;
+    if ((st = device_ok()) != MK_OK) return st;
+    uint32_t* status = at<uint32_t>(ws, L.ctrl);
+    MK_TRY(cudaMemsetAsync(status, 0, 32, s));  // status, site, router fallbacks, scan ticket, GEMM tickets
+    const DispatchOut dout{expert_offsets, row_token, row_weight, at<int32_t>(ws, L.slot_row), at<bf16>(ws, L.x_perm)};
+    const PhaseMarks pm{nullptr, s};
+    st = route_dispatch_steps(static_cast<const bf16*>(x), wg, bias, T, d, E, k, ws, L, dout, nullptr, pm, s);
+    if (st != MK_OK) return st;
+    MK_TRY(launch_grouped_gemm(dout.x_perm, expert_offsets, at<int32_t>(ws, L.mtile_start), nullptr,
+                               static_cast<const bf16*>(w), T * k, d, E, n, static_cast<bf16*>(out), status, s));
+    return MK_OK;
 }
 
 mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bias, const void* w1, const void* w3,

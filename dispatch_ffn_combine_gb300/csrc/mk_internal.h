@@ -60,6 +60,9 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(int64_t T, int d, int E, int k, int f);
+// The routing and dispatch part of the layout alone (the same offsets, up to
+// and including x_perm): the workspace of the Dispatch + GEMM entry point.
+WsLayout ws_layout_dispatch(int64_t T, int d, int E, int k);
 
 inline int64_t num_chunks(int64_t T) { return (T + kChunkTokens - 1) / kChunkTokens; }
 

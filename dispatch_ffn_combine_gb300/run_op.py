@@ -16,11 +16,11 @@ import json
 
 import torch
 
-from . import (MK_PATH_FUSED, MK_PATH_STEPS, alloc_workspace, mk_moe_combine, mk_moe_dispatch, mk_moe_expert_ffn,
-               mk_moe_layer, mk_moe_route)
+from . import (MK_PATH_FUSED, MK_PATH_STEPS, alloc_dispatch_gemm_workspace, alloc_workspace, mk_moe_combine,
+               mk_moe_dispatch, mk_moe_dispatch_gemm, mk_moe_expert_ffn, mk_moe_layer, mk_moe_route)
 from .workloads import CONFIGS, make_inputs
 
-OPS = ("route", "dispatch", "expert_ffn", "combine", "layer")
+OPS = ("route", "dispatch", "expert_ffn", "combine", "layer", "dispatch_gemm")
 
 
 def main(argv=None) -> dict:
@@ -35,7 +35,7 @@ def main(argv=None) -> dict:
 
     cfg = CONFIGS[args.config]
     dev = torch.device("cuda")
-    need_experts = args.op in ("expert_ffn", "combine", "layer")
+    need_experts = args.op in ("expert_ffn", "combine", "layer", "dispatch_gemm")
     inp = make_inputs(cfg, seed=0, device=dev, T=args.tokens, experts=need_experts)
     x, wg, bias = inp["x"], inp["wg"], inp["bias"]
     T, d = x.shape
@@ -43,6 +43,7 @@ def main(argv=None) -> dict:
     ws = alloc_workspace(T, d, E, k, f, dev)
     path = MK_PATH_STEPS if args.path == "steps" else MK_PATH_FUSED
 
+    dg_ws = alloc_dispatch_gemm_workspace(T, d, E, k, dev) if args.op == "dispatch_gemm" else None
     ids, w, _ = mk_moe_route(x, wg, bias, k, ws=ws)
     disp = mk_moe_dispatch(x, ids, w, E, ws=ws) if args.op in ("expert_ffn", "combine") else None
     h = P = None
@@ -61,6 +62,8 @@ def main(argv=None) -> dict:
                               inp["w2"], ws=ws)
         elif args.op == "combine":
             mk_moe_combine(P, disp["slot_row"], y=y)
+        elif args.op == "dispatch_gemm":  # the layer's gate projection W1 as the experts' weight
+            mk_moe_dispatch_gemm(x, wg, bias, inp["w1"], k, ws=dg_ws)
         else:
             mk_moe_layer(x, wg, bias, inp["w1"], inp["w3"], inp["w2"], k, y=y, ws=ws, path=path)
 

@@ -186,6 +186,22 @@ MK_API mk_status mk_moe_expert_ffn(const void* x_perm, const int32_t* expert_off
                             void* h, void* P,
                             void* ws, size_t ws_bytes, void* stream);
 
+/* Grouped GEMM on dispatched rows: the compute half of the README's "MoE
+ * Dispatch + GEMM" row ("runs the per-expert grouped GEMM"; paper section 4,
+ * Table 3), on the tensor cores:
+ *   out[r] = bf16( row_weight[r] * (x_perm[r] W_e^T) )   (fp32 accumulate)
+ * for every row r of expert e.
+ *   x_perm bf16 [S, d]; expert_offsets int32 [E+1] with off[0] = 0, off[E] = S
+ *   row_weight fp32 [S] or NULL (= 1)
+ *   w bf16 [E, n, d] (out x in), n a multiple of 64
+ *   out bf16 [S, n] (out)
+ *   ws: at least 256 + 4 (E + 1) bytes (control block and tile table).
+ * Offsets that are not monotone or do not end at S set MK_ERR_BOUNDS on the
+ * device and no row is computed. */
+MK_API mk_status mk_moe_grouped_gemm(const void* x_perm, const int32_t* expert_offsets, const float* row_weight,
+                              const void* w, int64_t S, int d, int E, int n, void* out,
+                              void* ws, size_t ws_bytes, void* stream);
+
 /* Combine (README row: "combines the weighted expert outputs back to each
  * token's source rank"; here: back to the token's row):
  *   y[t] = bf16( sum_{j=0..k-1} P[slot_row[t,j]] ), fp32 sum in ascending j.
@@ -202,6 +218,33 @@ MK_API mk_status mk_moe_layer(const void* x, const float* wg, const float* bias,
                        int64_t T, int d, int E, int k, int ffn,
                        void* y, void* ws, size_t ws_bytes,
                        const mk_moe_opts* opts, void* stream);
+
+/* Bytes of workspace mk_moe_dispatch_gemm needs for these sizes (the routing
+ * tables and the dispatched rows; the layer's workspace for the same T, d, E,
+ * k is larger and also serves).  Returns 0 if the sizes are invalid. */
+MK_API size_t mk_moe_dispatch_gemm_workspace_size(int64_t T, int d, int E, int k);
+
+/* MoE Dispatch + GEMM (README kernel table, row "MoE Dispatch + GEMM"; paper
+ * section 4, Table 3, and section 5.3): routes the tokens, sends each
+ * token's row to its k experts, and runs every expert's GEMM on the rows it
+ * received:
+ *   out[r] = bf16( x[row_token[r]] W_e^T )   for every row r of expert e,
+ * with the routing, slot order and row order of mk_moe_route and
+ * mk_moe_dispatch (on one GPU the exchange is the in-HBM permutation).  The
+ * routing weight is not applied here (a later combine applies it); it is
+ * returned per row.
+ *   x bf16 [T, d]; wg fp32 [E, d]; bias fp32 [E] or NULL; w bf16 [E, n, d]
+ *   out            bf16  [T*k, n] (out)  rows grouped by expert
+ *   expert_offsets int32 [E+1]  (out)    expert e owns rows [off[e], off[e+1])
+ *   row_token      int32 [T*k]  (out)    source token of each row
+ *   row_weight     fp32  [T*k]  (out, may be NULL)  routing weight of each row
+ *   ws: at least mk_moe_dispatch_gemm_workspace_size(T, d, E, k) bytes.
+ * Limits as for the layer, with n in the role of ffn.  T == 0 only zeroes
+ * expert_offsets (the other buffers are empty and may be NULL). */
+MK_API mk_status mk_moe_dispatch_gemm(const void* x, const float* wg, const float* bias, const void* w,
+                               int64_t T, int d, int E, int k, int n,
+                               void* out, int32_t* expert_offsets, int32_t* row_token, float* row_weight,
+                               void* ws, size_t ws_bytes, void* stream);
 
 /* The layer on HOST buffers: copies x_host (T*d bf16, pinned for an
  * asynchronous copy) into a staging region of `ws`, runs mk_moe_layer, and

@@ -18,6 +18,8 @@ Parity status of each function:
   dispatch           pinned (brute-force O(S^2) positions, invariants)
   expert_ffn / layer pinned (E=1,k=1 dense SwiGLU vs torch fp64, identical
                      experts, k=E full mixture, power-of-two scaling)
+  expert_linear      pinned (torch fp64 matmul, permutation and power-of-two
+                     expert matrices)
 """
 from __future__ import annotations
 
@@ -62,6 +64,7 @@ def _declare(lib):
     lib.oracle_dispatch.argtypes = [P, I64, I, I, P, P, P, P]
     lib.oracle_expert_ffn.argtypes = [P, P, P, P, I, I, P, P, I64, P]
     lib.oracle_layer.argtypes = [P, P, P, P, P, P, I64, I, I, I, I, P, I64, P, P, P]
+    lib.oracle_expert_linear.argtypes = [P, P, I, I, P, P, I64, P]
     return lib
 
 
@@ -183,6 +186,37 @@ def expert_ffn(x_bits, w1_bits, w3_bits, w2_bits, tokens, experts) -> np.ndarray
     _load().oracle_expert_ffn(_ptr(x_bits), _ptr(w1_bits), _ptr(w3_bits), _ptr(w2_bits), d, f,
                               _ptr(tokens), _ptr(experts), tokens.shape[0], _ptr(out))
     return out
+
+
+def expert_linear(x_bits, w_bits, tokens, experts) -> np.ndarray:
+    """fp64 W_e x_t for each (tokens[p], experts[p]) pair -> [npairs, n]; w is [E, n, d]."""
+    x_bits, w_bits = map(_u16, (x_bits, w_bits))
+    d = x_bits.shape[1]
+    n = w_bits.shape[1]
+    if w_bits.shape[2] != d:
+        raise ValueError("w must be [E, n, d]")
+    tokens = np.ascontiguousarray(tokens, dtype=np.int64)
+    experts = np.ascontiguousarray(experts, dtype=np.int32)
+    out = np.empty((tokens.shape[0], n), dtype=np.float64)
+    _load().oracle_expert_linear(_ptr(x_bits), _ptr(w_bits), d, n, _ptr(tokens), _ptr(experts), tokens.shape[0],
+                                 _ptr(out))
+    return out
+
+
+def dispatch_gemm(x_bits, wg, bias, w_bits, k: int):
+    """MoE Dispatch + GEMM on all tokens: route (R1-R4), dispatch (R5), then each
+    expert's linear map on its rows.  Returns (out [T*k, n] fp64 in dispatched row
+    order, offsets [E+1], row_token [T*k], row_weight [T*k] fp64)."""
+    x_bits = _u16(x_bits)
+    E = np.asarray(wg).shape[0]
+    ids, wts = topk(router_logits(x_bits, wg, bias), k)
+    _, offsets, row_token, slot_row = dispatch(ids, E)
+    row_expert = np.empty(row_token.shape[0], dtype=np.int32)
+    row_weight = np.empty(row_token.shape[0], dtype=np.float64)
+    row_expert[slot_row.ravel()] = ids.ravel()
+    row_weight[slot_row.ravel()] = wts.ravel()
+    out = expert_linear(x_bits, w_bits, row_token, row_expert)
+    return out, offsets, row_token, row_weight
 
 
 def layer(x_bits, wg, bias, w1_bits, w3_bits, w2_bits, k: int, tokens=None):

@@ -197,6 +197,26 @@ void oracle_expert_ffn(const uint16_t* x, const uint16_t* w1, const uint16_t* w3
     }
 }
 
+/* Per-expert linear map on given (token, expert) pairs, fp64: the grouped GEMM
+ * of the README's "MoE Dispatch + GEMM" row (each expert multiplies the token
+ * rows it receives by its weight):
+ *   out[p][c] = sum_i W_e[c][i] * x_t[i],  e = expert[p], t = token[p],
+ *   W: [E][n][d] (out x in, like a linear layer's weight).                   */
+void oracle_expert_linear(const uint16_t* x, const uint16_t* w, int d, int n,
+                          const int64_t* token, const int32_t* expert, int64_t npairs, double* out) {
+#pragma omp parallel for schedule(dynamic, 1)
+    for (int64_t p = 0; p < npairs; ++p) {
+        const uint16_t* xrow = x + token[p] * d;
+        const uint16_t* we = w + (int64_t)expert[p] * n * d;
+        for (int c = 0; c < n; ++c) {
+            const uint16_t* wrow = we + (int64_t)c * d;
+            double acc = 0.0;
+            for (int i = 0; i < d; ++i) acc += (double)bf16_bits_to_float(wrow[i]) * (double)bf16_bits_to_float(xrow[i]);
+            out[p * n + c] = acc;
+        }
+    }
+}
+
 /* The whole layer for a list of tokens (all of them, or a sample: tokens are
  * independent once the weights are fixed).  For each listed token t:
  *   route (R1-R4 + weights), run its k experts, y_t = sum_j w_j * out_j in j

@@ -116,3 +116,39 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.mk_moe_combine(None, A, T, d, k, A, None) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_moe_combine(A, A, 0, d, k, A, None) == mk.MK_OK
     assert lib.mk_moe_last_device_error(None, None, None) == mk.MK_ERR_WORKSPACE
+
+
+def test_dispatch_gemm_entry_points_reject_bad_arguments(lib):
+    A = _vp(0x10000)  # never dereferenced: every case fails validation first
+    T, d, E, k, n = 64, 256, 8, 2, 512
+    need = mk.dispatch_gemm_workspace_size(T, d, E, k)
+    # the routing and dispatch regions plus the dispatched rows, and less than the layer's
+    assert T * k * d * 2 < need < mk.workspace_size(T, d, E, k, n)
+    assert mk.dispatch_gemm_workspace_size(T, 100, E, k) == 0
+    assert mk.dispatch_gemm_workspace_size(T, d, E, 9) == 0
+    G = lib.mk_moe_dispatch_gemm
+    ok = [A, A, None, A, T, d, E, k, n, A, A, A, None, A, need, None]
+    names = ["x", "wg", "bias", "w", "T", "d", "E", "k", "n", "out", "off", "row_token", "row_weight", "ws", "wsb",
+             "s"]
+
+    def call(**over):
+        args = list(ok)
+        for key, v in over.items():
+            args[names.index(key)] = v
+        return G(*args)
+
+    assert call(n=96) == mk.MK_ERR_INVALID_ARG
+    assert call(d=100) == mk.MK_ERR_INVALID_ARG
+    assert call(k=0) == mk.MK_ERR_INVALID_ARG
+    assert call(w=None) == mk.MK_ERR_INVALID_ARG
+    assert call(out=None) == mk.MK_ERR_INVALID_ARG
+    assert call(row_token=None) == mk.MK_ERR_INVALID_ARG
+    assert call(w=_vp(0x10008)) == mk.MK_ERR_INVALID_ARG  # not 16-byte aligned
+    assert call(ws=None) == mk.MK_ERR_WORKSPACE
+    assert call(wsb=need - 1) == mk.MK_ERR_WORKSPACE
+    assert call(T=1 << 28, k=8) == mk.MK_ERR_UNSUPPORTED
+    Q = lib.mk_moe_grouped_gemm
+    assert Q(A, A, None, A, T, d, E, 96, A, A, 4096, None) == mk.MK_ERR_INVALID_ARG
+    assert Q(A, A, None, None, T, d, E, n, A, A, 4096, None) == mk.MK_ERR_INVALID_ARG
+    assert Q(A, A, None, A, T, d, E, n, A, A, 16, None) == mk.MK_ERR_WORKSPACE
+    assert Q(A, A, None, A, 0, d, E, n, A, A, 4096, None) == mk.MK_OK

@@ -25,6 +25,9 @@ PINS = [
     pins.test_layer_identical_experts_is_dense,
     pins.test_layer_k_equals_E_is_full_mixture,
     pins.test_layer_power_of_two_scaling_is_exact,
+    pins.test_expert_linear_matches_torch_matmul,
+    pins.test_expert_linear_permutation_and_scale_experts,
+    pins.test_dispatch_gemm_composes_route_dispatch_linear,
 ]
 
 MUTANTS = {
@@ -44,6 +47,14 @@ MUTANTS = {
     "rows_descending_in_expert": ("int32_t r = offsets[e] + fill[e];", "int32_t r = offsets[e + 1] - 1 - fill[e];"),
     "combine_uses_first_weight": ("yrow[c] += w[j] * out[c];", "yrow[c] += w[0] * out[c];"),
     "w3_uses_w1_row": ("const uint16_t* r3 = w3e + (int64_t)n * d;", "const uint16_t* r3 = w1e + (int64_t)n * d;"),
+    "linear_weight_transposed": ("const uint16_t* wrow = we + (int64_t)c * d;\n            double acc = 0.0;\n"
+                                 "            for (int i = 0; i < d; ++i) acc += (double)bf16_bits_to_float(wrow[i])",
+                                 "const uint16_t* wrow = we + c;\n            double acc = 0.0;\n"
+                                 "            for (int i = 0; i < d; ++i) acc += (double)bf16_bits_to_float(wrow[(int64_t)i * n])"),
+    "linear_expert_stride_d": ("const uint16_t* we = w + (int64_t)expert[p] * n * d;",
+                               "const uint16_t* we = w + (int64_t)expert[p] * d;"),
+    "linear_last_term_dropped": ("for (int i = 0; i < d; ++i) acc += (double)bf16_bits_to_float(wrow[i])",
+                                 "for (int i = 0; i < d - 1; ++i) acc += (double)bf16_bits_to_float(wrow[i])"),
 }
 
 

@@ -290,3 +290,61 @@ def test_layer_consistent_with_pieces_and_sample():
     sample = np.array([29, 3, 3, 0])
     ys, _, _ = oracle.layer(xb, wg, None, w1, w3, w2, k=k, tokens=sample)
     np.testing.assert_array_equal(ys, y[sample])
+
+
+# ---------------------------------------------------------------- expert linear (Dispatch + GEMM)
+
+def test_expert_linear_matches_torch_matmul():
+    """W_e x_t for listed pairs equals torch's fp64 matmul of the same bf16 values."""
+    rs = np.random.RandomState(21)
+    T, d, E, n = 9, 96, 4, 80
+    xb = _bf16(rs.randn(T, d))
+    wb = _bf16(rs.randn(E, n, d) * d ** -0.5)
+    toks = np.array([0, 8, 3, 3, 5, 1, 7])
+    exps = np.array([2, 0, 3, 1, 2, 0, 3])
+    out = oracle.expert_linear(xb, wb, toks, exps)
+    x = torch.from_numpy(bits_to_float(xb).astype(np.float64))
+    w = torch.from_numpy(bits_to_float(wb).astype(np.float64))
+    ref = torch.stack([w[e] @ x[t] for t, e in zip(toks, exps)]).numpy()
+    np.testing.assert_allclose(out, ref, rtol=1e-13, atol=1e-13 * np.abs(ref).max())
+
+
+def test_expert_linear_permutation_and_scale_experts():
+    """Expert e = 2^e times a permutation matrix: out row = 2^e * x permuted, exactly
+    (a transposed weight index would apply the inverse permutation)."""
+    rs = np.random.RandomState(22)
+    T, d, E = 5, 64, 3
+    xb = _bf16(rs.randn(T, d))
+    perms = [rs.permutation(d) for _ in range(E)]
+    w = np.zeros((E, d, d), dtype=np.float32)
+    for e, pi in enumerate(perms):
+        w[e, np.arange(d), pi] = 2.0 ** e          # row c picks input pi[c]
+    wb = _bf16(w)
+    toks = np.array([4, 0, 2, 2, 1])
+    exps = np.array([0, 1, 2, 0, 1])
+    out = oracle.expert_linear(xb, wb, toks, exps)
+    x = bits_to_float(xb).astype(np.float64)
+    for p, (t, e) in enumerate(zip(toks, exps)):
+        np.testing.assert_array_equal(out[p], (2.0 ** e) * x[t][perms[e]])
+
+
+def test_dispatch_gemm_composes_route_dispatch_linear():
+    """Dispatch + GEMM = the router's choice, the dispatch row order, and each row's
+    expert map: row r of expert e holds W_e x_{row_token[r]}; row weights are the
+    routing weights of (token, slot)."""
+    rs = np.random.RandomState(23)
+    T, d, E, k, n = 21, 64, 5, 2, 64
+    xb = _bf16(rs.randn(T, d))
+    wg = rs.randn(E, d).astype(np.float32)
+    wb = _bf16(rs.randn(E, n, d) * d ** -0.5)
+    out, off, row_token, row_weight = oracle.dispatch_gemm(xb, wg, None, wb, k)
+    ids, w = oracle.topk(oracle.router_logits(xb, wg, None), k)
+    x = bits_to_float(xb).astype(np.float64)
+    wf = bits_to_float(wb).astype(np.float64)
+    assert off[0] == 0 and off[-1] == T * k
+    for e in range(E):
+        for r in range(off[e], off[e + 1]):
+            t = row_token[r]
+            j = list(ids[t]).index(e)
+            assert row_weight[r] == w[t, j]
+            np.testing.assert_allclose(out[r], wf[e] @ x[t], rtol=1e-13, atol=1e-13)
