@@ -134,15 +134,16 @@ class ClockSampler:
 
 
 def launches_per_step(cfg, path) -> int:
-    """Kernels one mk_moe_layer call launches.  The fused path is one kernel.
-    The kernel-per-step path runs route (plain: logits + top-k; with the
-    tensor-core candidate filter, which the library picks when T >= 2048,
-    T*d*E >= 2^32 and the token row fits its staging: prep + approximate
-    logits + select), count, scan, scatter, gemm1, gemm2, combine."""
+    """Kernels one mk_moe_layer call launches.  The kernel-per-step path runs
+    route (plain: logits + top-k; with the tensor-core candidate filter, which
+    the library picks when T >= 2048, T*d*E >= 2^32 and the token row fits its
+    staging: prep + approximate logits + select), count, scan, scatter, gemm1,
+    gemm2, combine.  The fused path is one persistent kernel, preceded, where
+    the candidate filter applies, by the filter's three kernels, count and scan."""
     import dispatch_ffn_combine_gb300 as mk
-    if path == mk.MK_PATH_FUSED:
-        return 1
     filt = (cfg.T >= 2048 and cfg.T * cfg.d * cfg.E >= 2 ** 32 and 2 * cfg.d + 8 * cfg.E <= 160 * 1024)
+    if path == mk.MK_PATH_FUSED:
+        return 1 + (5 if filt else 0)
     return (3 if filt else 2) + 6
 
 

@@ -323,6 +323,13 @@ struct LayerHooks {
     bool skip_combine = false;            // the caller runs the combine itself (in chunks)
 };
 
+// The candidate filter pays off once the fixed-order work (T d E fused
+// multiply-adds) is large and there are enough 128-token tiles to fill the
+// GPU; below that the plain fixed-order router is faster.  Same bits.
+bool use_route_filter(int64_t T, int d, int E) {
+    return route_tc_supported(d, E) && T >= 2048 && static_cast<double>(T) * d * E >= 4294967296.0;
+}
+
 // Where the dispatch step writes (the layer's workspace, or the caller's buffers).
 struct DispatchOut {
     int32_t* offsets;    // [E+1]
@@ -347,12 +354,7 @@ mk_status route_dispatch_steps(const bf16* xb, const float* wg, const float* bia
     int32_t* rank = at<int32_t>(ws, L.rank);
     const uint64_t timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     MK_TRY(pm.mark(MK_PHASE_ROUTE_LOGITS));
-    // The candidate filter pays off once the fixed-order work (T d E fused
-    // multiply-adds) is large and there are enough 128-token tiles to fill the
-    // GPU; below that the plain fixed-order router is faster.  Same bits.
-    const bool filter = route_tc_supported(d, E) && T >= 2048 &&
-                        static_cast<double>(T) * d * E >= 4294967296.0;
-    if (filter || (opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND && route_tc_supported(d, E))) {
+    if (use_route_filter(T, d, E) || (opts && opts->inject == MK_INJECT_ROUTE_ZERO_BOUND && route_tc_supported(d, E))) {
         MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
                                    status, timeout_ns, s));
         MK_TRY(pm.mark(MK_PHASE_TOPK));
@@ -429,6 +431,21 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
         fa.trace_cap = (opts && opts->trace) ? opts->trace_cap : 0;
         fa.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
         MK_TRY(pm.mark(0));
+        if (use_route_filter(T, d, E)) {
+            // The persistent kernel's own router is the plain fixed-order one;
+            // where the candidate filter is faster, the routing (and the
+            // counts and scans that follow it) run first as their own kernels
+            // and the persistent kernel starts at the dispatch.  Same bits.
+            const bf16* xb = static_cast<const bf16*>(x);
+            MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
+                                       status, fa.timeout_ns, s));
+            MK_TRY(launch_route_select(xb, wg, bias, T, d, E, k, logits, at<float>(ws, L.wnorm), ids, w, nullptr,
+                                       status + 2, false, s));
+            MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s));
+            MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile,
+                               status + 3, s));
+            fa.routed = true;
+        }
         MK_TRY(launch_fused(fa, s));
         for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
         return MK_OK;

@@ -12,7 +12,10 @@
 // exchanges of the README's "MoE Dispatch + FFN + Combine" row become HBM
 // copies, so the mover role runs the router, the dispatch and the combine.
 //
-// Two task queues, each claimed in order with an atomic ticket:
+// Two task queues, each claimed in order with an atomic ticket (when the
+// routing comes in precomputed -- ids, weights, chunk counts and scans, from
+// the router and count/scan kernels launched just before -- the mover queue
+// starts at the dispatch chunks):
 //   mover queue:   route blocks (32 tokens x 32 experts of gate logits)
 //                  -> dispatch chunks (128 tokens: rows of their slots, and the
 //                     token rows copied into those rows, each read once)
@@ -121,6 +124,7 @@ struct FusedParams {
     uint32_t* h_done;      // [G_max]
     int n_tg, n_eg, ct, nchunks;
     int NR, NK;
+    int routed;  // 1: ids, weights, chunk counts, ranks and scans were computed before the launch
     int NT1, NT2, kb1, kb2;
     int mover_ctas;  // 0 adaptive; > 0 blocks [0, n) prefer mover tasks; < 0 no block prefers them
     uint64_t timeout_ns;
@@ -132,6 +136,12 @@ __device__ __forceinline__ uint32_t ld_acquire(const uint32_t* p) {
     uint32_t v;
     asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
     return v;
+}
+
+// The offsets, chunk bases and tile table exist (computed in this launch by
+// the last chunk counted, or before it when the routing came in precomputed).
+__device__ __forceinline__ bool scans_ready(const FusedParams& p) {
+    return p.routed != 0 || ld_acquire(&p.sync->scan_done) != 0u;
 }
 
 __device__ __forceinline__ uint32_t ld_relaxed(const uint32_t* p) {
@@ -195,7 +205,7 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
             kind = kActRoute;
             arg = static_cast<int>(h);
         } else {
-            if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0, 0};
+            if (!scans_ready(p)) return {kActIdle, 0, 0};
             const int G = p.mtile_start[p.E];
             const uint32_t b_index = p.NR, b_comb = b_index + p.nchunks, total = b_comb + p.NK;
             if (h >= total) return {kActExit, 0, 0};
@@ -227,7 +237,7 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
 // on nothing.
 __device__ Claim try_claim_compute(const FusedParams& p) {
     FusedSync* s = p.sync;
-    if (ld_acquire(&s->scan_done) == 0u) return {kActIdle, 0, 0};
+    if (!scans_ready(p)) return {kActIdle, 0, 0};
     if (ld_acquire(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0, 0};
     const int G = p.mtile_start[p.E];
     const uint32_t total = static_cast<uint32_t>(G) * (p.NT1 + p.NT2);
@@ -251,7 +261,7 @@ __device__ __forceinline__ int claim_next_tile(const FusedParams& p, uint32_t to
 __device__ int controller_target(const FusedParams& p) {
     FusedSync* s = p.sync;
     const int B = static_cast<int>(gridDim.x);
-    if (ld_acquire(&s->scan_done) == 0u) return B;
+    if (!scans_ready(p)) return B;
     const int G = p.mtile_start[p.E];
     const double mover_total = static_cast<double>(p.NR) + p.nchunks + p.NK;
     const double compute_total = static_cast<double>(G) * (p.NT1 + p.NT2);
@@ -923,7 +933,8 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     p.n_eg = (E + ce - 1) / ce;
     p.ct = ct;
     p.nchunks = static_cast<int>(nch);
-    p.NR = p.n_tg * p.n_eg;
+    p.routed = a.routed ? 1 : 0;
+    p.NR = a.routed ? 0 : p.n_tg * p.n_eg;  // no router tasks when the routing came in
     p.NK = static_cast<int>((T + kCombineTokens - 1) / kCombineTokens);
     p.NT1 = (f + MMA_N / 2 - 1) / (MMA_N / 2);
     p.NT2 = (d + MMA_N - 1) / MMA_N;

@@ -169,6 +169,7 @@ struct FusedArgs {
     uint64_t timeout_ns;
     uint32_t* trace;  // optional task trace (8 words per record)
     int trace_cap;
+    bool routed = false;  // ids, w, chunk_counts, rank and the scans are already computed
 };
 size_t fused_sync_bytes(int64_t T, int E, int k);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);

@@ -58,3 +58,14 @@ def test_fused_repeated_calls_same_workspace():
     ys = [mk.mk_moe_layer(*args, ws=ws, path=mk.MK_PATH_FUSED).clone() for _ in range(3)]
     assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
     assert all(torch.equal(ys[0].view(torch.int16), y.view(torch.int16)) for y in ys[1:])
+
+
+@pytest.mark.parametrize("movers", [8, -1])
+def test_fused_prerouted_any_split_bitwise(movers):
+    """Skewed is large enough for the candidate-filter router, so the fused path
+    takes its routing, counts and scans from kernels launched before the
+    persistent kernel; every split still gives the kernel-per-step bits."""
+    wl = Workload("skewed")
+    y_s = _layer(wl, path=mk.MK_PATH_STEPS)
+    y_f = _layer(wl, mover_ctas=movers)
+    assert torch.equal(y_f.view(torch.int16), y_s.view(torch.int16))
