@@ -68,6 +68,10 @@ CONFIGS = {
     "single": MoEConfig("single", 300, 256, 1, 1, 384),
     # ~500 rows per expert: several row blocks per expert, ragged in every tile dimension
     "ragged_pair": MoEConfig("ragged_pair", 1500, 384, 6, 2, 320),
+    # edge shapes: the smallest d and ffn with k = E (every expert takes every
+    # token), and 256 experts at k = 1 with most experts empty or single-row
+    "edge_min": MoEConfig("edge_min", 50, 64, 3, 3, 64),
+    "many_experts": MoEConfig("many_experts", 300, 128, 256, 1, 128),
     # profiling shape: the large layer's d and ffn with 16 experts (about 2.5 GB
     # on the device), small enough for multi-pass counter captures
     "prof": MoEConfig("prof", 4096, 7168, 16, 8, 2048),

@@ -102,7 +102,7 @@ def _check_tables(wl, res):
     return row_token_ref, row_expert
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "ragged_pair"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "ragged_pair", "edge_min", "many_experts"])
 def test_dispatch_gemm_small_all_rows(name):
     wl = Workload(name)
     res, _ = _run(wl)

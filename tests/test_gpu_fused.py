@@ -24,7 +24,7 @@ def _layer(wl, **kw):
     return y
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "ragged_pair", "mid", "skewed"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "ragged_pair", "edge_min", "many_experts", "mid", "skewed"])
 def test_fused_equals_steps_bitwise(name):
     wl = Workload(name)
     y_f = _layer(wl, path=mk.MK_PATH_FUSED, timeout_ns=500_000_000)

@@ -36,7 +36,7 @@ def _check_routing(wl, ws, ids_ref, w_ref):
     np.testing.assert_array_equal(slot.cpu().numpy(), slot_ref)
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "ragged_pair"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "ragged_pair", "edge_min", "many_experts"])
 def test_layer_small_all_tokens(name):
     wl = Workload(name)
     y, ws = _run_layer(wl)

@@ -15,7 +15,7 @@ from _support import Workload
 
 pytestmark = pytest.mark.gpu
 
-ROUTE_CONFIGS = ["tiny", "ragged", "ragged_skew", "single", "mid", "skewed", "decode", "large"]
+ROUTE_CONFIGS = ["tiny", "ragged", "ragged_skew", "single", "edge_min", "many_experts", "mid", "skewed", "decode", "large"]
 
 
 @pytest.mark.parametrize("name", ROUTE_CONFIGS)
@@ -112,7 +112,8 @@ def test_route_fixed_order_decides_weights():
     np.testing.assert_allclose(w.cpu().numpy()[0], [1 / (1 + e2), e2 / (1 + e2)], rtol=1e-6)
 
 
-@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "mid", "skewed", "decode"])
+@pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "edge_min", "many_experts", "mid", "skewed",
+                                  "decode"])
 def test_dispatch_bit_exact(name):
     """GPU dispatch of the oracle's routing equals the oracle's dispatch."""
     wl = Workload(name, experts=False)
