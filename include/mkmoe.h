@@ -82,7 +82,7 @@ enum {
     MK_PHASE_COUNT_ALL = 8
 };
 /* On the fused path (opts->path = MK_PATH_FUSED) the steps overlap inside one kernel: phase_events then
- * gets event 0 before the kernel and events 1..MK_PHASE_COUNT_ALL after it. */
+ * gets event 0 before the kernels and events 1..MK_PHASE_COUNT_ALL after them. */
 
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {
@@ -98,7 +98,11 @@ typedef struct {
                               path only.                                                     */
     int path;              /* MK_PATH_STEPS (0, default): one kernel per step, the faster
                               path on GB300 at every workload measured; MK_PATH_FUSED (1): one
-                              persistent kernel whose blocks take mover or compute roles.
+                              persistent kernel whose blocks take mover or compute roles
+                              (routing, counts and scans included; where the router's
+                              tensor-core candidate filter applies -- T >= 2048 and
+                              T d E >= 2^32 -- those run first as their own kernels and the
+                              persistent kernel starts at the dispatch).
                               Both give bit-identical results.                              */
     int mover_ctas;        /* fused path: 0 = adaptive split (on-GPU controller, paper
                               section 3.2 Eq. 2); n > 0 = fixed split, blocks [0, n) prefer
