@@ -697,11 +697,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = ctl->tmem_base;
-    volatile uint32_t* abort_local = &ctl->abort_local;
-    const volatile uint32_t* never = &ctl->zero;
 
     // Role of this block (thread 0 keeps it).  Adaptive mode starts with every
-    // block a mover: only route tasks exist before the scans.
+    // block a mover: with the routing computed in this kernel, only route
+    // tasks exist before the scans (otherwise the controller rebalances at
+    // the first decision).
     PipeState* ps = &ctl->ps;
     if (tid == 0) {
         *ps = PipeState{};
@@ -924,7 +924,6 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     p.sync = reinterpret_cast<FusedSync*>(sb);
     const int64_t n_tg_max = (T + 31) / 32;
     const int64_t nch = num_chunks(T);
-    const int64_t g_max = (S + kTileM - 1) / kTileM + E;
     uint32_t* arr = reinterpret_cast<uint32_t*>(sb + sizeof(FusedSync));
     p.route_done = arr;
     p.topk_done = arr + n_tg_max;
