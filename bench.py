@@ -20,6 +20,7 @@ layer) on a bounded token sample of the same workload, on the host cores.
 from __future__ import annotations
 
 import argparse
+import datetime
 import hashlib
 import json
 import os
@@ -77,9 +78,12 @@ def dist_env():
 
 
 class ClockSampler:
-    """nvidia-smi clocks / throttle reasons sampled during the timed region."""
+    """nvidia-smi clocks / throttle reasons sampled every 20 ms; the samples whose
+    timestamps fall inside the timed region (host clock, marked by begin/end)
+    are the ones reported (the nearest one if the region is shorter than the
+    interval)."""
 
-    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    FIELDS = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
               "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
               "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -87,6 +91,14 @@ class ClockSampler:
         self.gpu = gpu_index
         self.proc = None
         self.path = None
+        self.t_begin = None
+        self.t_end = None
+
+    def begin(self):
+        self.t_begin = time.time()
+
+    def end(self):
+        self.t_end = time.time()
 
     def start(self):
         try:
@@ -95,7 +107,7 @@ class ClockSampler:
             self.fh = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
-                 "-lms", "100"], stdout=self.fh, stderr=subprocess.DEVNULL)
+                 "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except (OSError, FileNotFoundError):
             self.proc = None
@@ -110,27 +122,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.fh.close()
-        sm, smax, power, reasons = [], [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        rows = []  # (time, sm, sm_max, power, reasons)
         with open(self.path) as fh:
             for ln in fh:
                 parts = [p.strip() for p in ln.split(",")]
-                if len(parts) < 9:
+                if len(parts) < 10:
                     continue
                 try:
-                    sm.append(float(parts[1]))
-                    smax.append(float(parts[2]))
-                    power.append(float(parts[3]))
+                    ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                    row = (ts, float(parts[2]), float(parts[3]), float(parts[4]),
+                           {nm for nm, v in zip(names, parts[6:10]) if v.lower() == "active"})
                 except ValueError:
                     continue
-                for nm, v in zip(names, parts[5:9]):
-                    if v.lower() == "active":
-                        reasons.add(nm)
-        if not sm:
+                rows.append(row)
+        if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        loaded = [s for s, p in zip(sm, power) if p > 0.5 * max(power)] or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "reasons": sorted(reasons),
-                "samples": len(sm), "power_w_max": max(power)}
+        inside = rows
+        if self.t_begin is not None and self.t_end is not None:
+            inside = [r for r in rows if self.t_begin <= r[0] <= self.t_end]
+            if not inside:
+                mid = 0.5 * (self.t_begin + self.t_end)
+                inside = [min(rows, key=lambda r: abs(r[0] - mid))]
+        reasons = set().union(*(r[4] for r in inside))
+        return {"sm_mhz": statistics.median(r[1] for r in inside), "sm_max_mhz": max(r[2] for r in rows),
+                "reasons": sorted(reasons), "samples": len(inside),
+                "power_w_max": max(r[3] for r in inside)}
 
 
 def launches_per_step(cfg, path) -> int:
@@ -289,6 +306,7 @@ def run_ours(args):
     if dist:
         tdist.barrier()
     torch.cuda.synchronize()
+    clocks.begin()
     if flush:
         total_ms = 0.0
         for i in range(args.steps):
@@ -305,6 +323,7 @@ def run_ours(args):
         t_end.record(stream)
         torch.cuda.synchronize()
         total_ms = t_start.elapsed_time(t_end)
+    clocks.end()
     if dist:
         tdist.barrier()
     clk = clocks.stop()
@@ -436,7 +455,7 @@ def run_ours(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--config", default="large", choices=sorted(CONFIGS))
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
