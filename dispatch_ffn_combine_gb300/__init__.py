@@ -36,6 +36,7 @@ ENTRY_POINTS = (
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
     "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count", "mk_moe_route_fallbacks",
     "mk_moe_grouped_gemm", "mk_moe_dispatch_gemm_workspace_size", "mk_moe_dispatch_gemm",
+    "mk_moe_route_approx_logits",
 )
 _SIZE_RESULT = ("mk_moe_workspace_size", "mk_moe_dispatch_gemm_workspace_size")
 
@@ -90,6 +91,7 @@ def load_library():
         lib.mk_moe_dispatch_gemm_workspace_size.restype = SZ
         lib.mk_moe_dispatch_gemm_workspace_size.argtypes = [I64, I, I, I]
         lib.mk_moe_dispatch_gemm.argtypes = [P, P, P, P, I64, I, I, I, I, P, P, P, P, P, SZ, P]
+        lib.mk_moe_route_approx_logits.argtypes = [P, I64, I, I, I, P, P]
         for name in ENTRY_POINTS:
             if name not in _SIZE_RESULT + ("mk_moe_status_string",):
                 getattr(lib, name).restype = I
@@ -375,6 +377,14 @@ def mk_moe_route_fallbacks(ws, stream=None):
     n = ctypes.c_uint32(0)
     _check(load_library().mk_moe_route_fallbacks(_p(ws), _stream(stream), ctypes.byref(n)), "mk_moe_route_fallbacks")
     return int(n.value)
+
+
+def mk_moe_route_approx_logits(ws, T, d, E, k, stream=None):
+    """The approximate logits [T, E] fp32 the last candidate-filter router run on ws left there."""
+    out = torch.empty((T, E), dtype=torch.float32, device=ws.device)
+    _check(load_library().mk_moe_route_approx_logits(_p(ws), T, d, E, k, _p(out), _stream(stream)),
+           "mk_moe_route_approx_logits")
+    return out
 
 
 def mk_moe_layer_trace_count(ws, T, d, E, k, ffn, stream=None):

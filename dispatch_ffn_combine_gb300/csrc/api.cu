@@ -741,6 +741,18 @@ mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int
     return MK_OK;
 }
 
+mk_status mk_moe_route_approx_logits(const void* ws, int64_t T, int d, int E, int k, float* out, void* stream) {
+    mk_status st = check_sizes(T, d, E, k, 64);
+    if (st != MK_OK) return st;
+    if (ws == nullptr) return MK_ERR_WORKSPACE;
+    if (out == nullptr) return MK_ERR_INVALID_ARG;
+    if (T == 0) return MK_OK;
+    const WsLayout L = ws_layout_dispatch(T, d, E, k);  // the logits sit at the same offset in every layout
+    MK_TRY(cudaMemcpyAsync(out, static_cast<const uint8_t*>(ws) + L.logits, static_cast<size_t>(T) * E * 4,
+                           cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
+    return MK_OK;
+}
+
 mk_status mk_moe_layer_routing(const void* ws, int64_t T, int d, int E, int k, int ffn, int32_t* topk_ids,
                                float* topk_w, int32_t* expert_offsets, int32_t* slot_row, void* stream) {
     mk_status st = check_sizes(T, d, E, k, ffn);

@@ -282,6 +282,14 @@ MK_API mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* deta
  * MK_ERR_WORKSPACE if ws is NULL. */
 MK_API mk_status mk_moe_route_fallbacks(void* ws, void* stream, uint32_t* count);
 
+/* Router diagnostics: copies the approximate logits (fp32 [T, E], bias added)
+ * that the last run of the tensor-core candidate filter on `ws` left there --
+ * mk_moe_route, mk_moe_dispatch_gemm, or mk_moe_layer when the filter applies
+ * (T >= 2048 and T d E >= 2^32) -- into `out` (device, T * E floats),
+ * asynchronously on `stream`.  Each lies within the filter's error bound of
+ * the fixed-order logit.  Returns MK_ERR_WORKSPACE if ws is NULL. */
+MK_API mk_status mk_moe_route_approx_logits(const void* ws, int64_t T, int d, int E, int k, float* out, void* stream);
+
 /* Records the last fused mk_moe_layer call on `ws` wrote into its trace buffer
  * (synchronises `stream`).  Returns MK_ERR_WORKSPACE if ws is NULL. */
 MK_API mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int ffn, void* stream,

@@ -116,6 +116,9 @@ def test_other_entry_points_reject_bad_arguments(lib):
     assert lib.mk_moe_combine(None, A, T, d, k, A, None) == mk.MK_ERR_INVALID_ARG
     assert lib.mk_moe_combine(A, A, 0, d, k, A, None) == mk.MK_OK
     assert lib.mk_moe_last_device_error(None, None, None) == mk.MK_ERR_WORKSPACE
+    assert lib.mk_moe_route_approx_logits(None, T, d, E, k, A, None) == mk.MK_ERR_WORKSPACE
+    assert lib.mk_moe_route_approx_logits(A, T, d, E, k, None, None) == mk.MK_ERR_INVALID_ARG
+    assert lib.mk_moe_route_approx_logits(A, T, 100, E, k, A, None) == mk.MK_ERR_INVALID_ARG
 
 
 def test_dispatch_gemm_entry_points_reject_bad_arguments(lib):
