@@ -162,24 +162,36 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
-// (expert, M-tile) of expert-M-tile index g: largest e with mtile_start[e] <= g.
-// `mts` / `offs` are the tile table and the expert offsets (global memory, or
-// the shared-memory copies a GEMM session makes).
-__device__ __forceinline__ void decode_g(const int32_t* mts, const int32_t* offs, int E, int g, int& e, int& row0,
-                                         int& rows) {
-    int lo = 0, hi = E - 1;
+// GEMM tile `local` of one GEMM (nt N blocks per M-tile) -> its M-tile g, its
+// N block and its expert (`mts` / `offs`: the tile table and the expert
+// offsets, the shared-memory copies a GEMM session makes): an expert's tiles occupy [mts[e] * nt, mts[e+1] * nt)
+// in groups of kNGroup N blocks, each group over all the expert's M-tiles, N
+// fastest, so tiles claimed close together share a weight block and a row
+// block in L2 (the stand-alone GEMMs' order).
+constexpr int kNGroup = 4;
+__device__ __forceinline__ void decode_tile(const int32_t* mts, const int32_t* offs, int E, int nt, int local, int& g,
+                                            int& n, int& e, int& row0, int& rows) {
+    const int gi = local / nt;
+    int lo = 0, hi = E - 1;  // largest e with mts[e] <= gi
     while (lo < hi) {
         const int mid = (lo + hi + 1) >> 1;
-        if (mts[mid] <= g)
+        if (mts[mid] <= gi)
             lo = mid;
         else
             hi = mid - 1;
     }
     e = lo;
-    const int mt = g - mts[lo];
+    const int p_e = mts[lo + 1] - mts[lo];
+    const int l = local - mts[lo] * nt;
+    const int q = l / (p_e * kNGroup);
+    const int nb = min(kNGroup, nt - q * kNGroup);
+    const int r = l - q * p_e * kNGroup;
+    const int j = r / nb;
+    n = q * kNGroup + (r - j * nb);
+    g = mts[lo] + j;
     const int off = offs[lo];
-    row0 = off + mt * BM;
-    rows = min(BM, offs[lo + 1] - off - mt * BM);
+    row0 = off + j * BM;
+    rows = min(BM, offs[lo + 1] - off - j * BM);
 }
 
 struct Claim {
@@ -228,7 +240,8 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
 
 // Compute tiles are claimed one at a time with a fetch-add on the queue head,
 // which never fails under contention and keeps the tiles in flight across the
-// grid consecutive (they share weights in L2, as a static stride would).
+// grid consecutive (in the grouped order of decode_tile they share weight and
+// row blocks in L2).
 // gemm1 tiles are claimable once every dispatch chunk is done, so they never
 // wait; a gemm2 tile's inputs (the four epilogue quarters of every gemm1 tile
 // of its M-tile) may still be in flight when it is claimed, and its producer
@@ -387,10 +400,9 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
             ts.mode = tile < n1 ? 0 : 1;
             const int local = ts.mode == 0 ? tile : tile - n1;
             const int nt_cnt = ts.mode == 0 ? p.NT1 : p.NT2;
-            ts.g = local / nt_cnt;
-            int e;
-            decode_g(ctl->s_mtile_start, ctl->s_offsets, p.E, ts.g, e, ts.row0, ts.rows);
-            ts.n0 = (local - ts.g * nt_cnt) * (ts.mode == 0 ? MMA_N / 2 : MMA_N);
+            int e, nblk;
+            decode_tile(ctl->s_mtile_start, ctl->s_offsets, p.E, nt_cnt, local, ts.g, nblk, e, ts.row0, ts.rows);
+            ts.n0 = nblk * (ts.mode == 0 ? MMA_N / 2 : MMA_N);
             ts.kblocks = ts.mode == 0 ? p.kb1 : p.kb2;
             ts.pad = e;
         }
