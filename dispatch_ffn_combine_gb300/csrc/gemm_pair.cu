@@ -308,64 +308,77 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0 && rank == 0) {
+        if (rank == 0) {
             // ------------------------------------------------ MMA issuer (CTA 0 only)
+            // The whole warp runs the loop and one elected lane issues the MMAs and
+            // commits: a converged issuing warp keeps more MMAs queued ahead of
+            // the tensor pipe than a lone diverged lane does.  Every wait result
+            // is made warp-uniform before it is acted on.
+            const bool leader = elect_one();
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0, slot_phase = 0;
             bool ok = true;
             for (;;) {
-                if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word,
-                                               p.timeout_ns)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase,
+                                                                      abort_word, p.timeout_ns))) {
                     ok = false;
                     break;
                 }
                 const int4 info = ctl->slot[slot];
-                mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
+                __syncwarp();
+                if (leader) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
                 if (++slot == kPairSlots) {
                     slot = 0;
                     slot_phase ^= 1u;
                 }
                 if (info.x < 0) break;
                 const uint32_t idesc = info.z <= BM ? PIDESC_HALF : PIDESC;
-                if (!mbar_wait_bounded_cluster(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, abort_word,
-                                               p.timeout_ns)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->tmem_empty[acc]),
+                                                                      acc_phase ^ 1u, abort_word, p.timeout_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * MMA_N;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->full[stage]), phase, abort_word, p.timeout_ns)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->full[stage]), phase,
+                                                                          abort_word, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
-                    const uint32_t sb = sa + PA_BYTES;
+                    if (leader) {
+                        const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
+                        const uint32_t sb = sa + PA_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = sw128_kmajor_desc(sa + kk * UMMA_K * 2);
-                        const uint64_t bd = sw128_kmajor_desc(sb + kk * UMMA_K * 2);
-                        mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint64_t ad = sw128_kmajor_desc(sa + kk * UMMA_K * 2);
+                            const uint64_t bd = sw128_kmajor_desc(sb + kk * UMMA_K * 2);
+                            mma_bf16_ss_pair(d_tmem, ad, bd, idesc, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), 0x3);
                     }
-                    mma_commit_pair_mc(smem_u32(&ctl->empty[stage]), 0x3);
+                    __syncwarp();
                     if (++stage == PSTAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit_pair_mc(smem_u32(&ctl->tmem_full[acc]), 0x3);
+                if (leader) mma_commit_pair_mc(smem_u32(&ctl->tmem_full[acc]), 0x3);
+                __syncwarp();
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            if (!ok) {
-                raise_abort(ctl, peer);
-                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+            if (leader) {
+                if (!ok) {
+                    raise_abort(ctl, peer);
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+                }
+                // All MMAs issued complete before either CTA frees TMEM or shared memory.
+                mma_commit_pair_mc(smem_u32(&ctl->drain), 0x1);
+                if (!mbar_wait_bounded_cluster(smem_u32(&ctl->drain), 0u, never, p.timeout_ns))
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmDrain);
             }
-            // All MMAs issued complete before either CTA frees TMEM or shared memory.
-            mma_commit_pair_mc(smem_u32(&ctl->drain), 0x1);
-            if (!mbar_wait_bounded_cluster(smem_u32(&ctl->drain), 0u, never, p.timeout_ns))
-                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmDrain);
         }
         __syncwarp();
     } else {
