@@ -530,69 +530,81 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
     __syncwarp();
 }
 
+// The whole warp runs the MMA role; one elected lane issues the MMAs, the
+// commits and the arrivals (a converged issuing warp keeps the tensor pipe's
+// queue fuller than a lone lane); wait results are made warp-uniform.
 __device__ __noinline__ void gemm_mma(const FusedParams& p, FusedCtl* ctl, uint8_t* smem, uint32_t tmem_base) {
     FusedSync* sync = p.sync;
     PipeState* ps = &ctl->ps;
     volatile uint32_t* abort_local = &ctl->abort_local;
+    const bool leader = elect_one();
     uint32_t mm_stage = ps->mm_stage, mm_phase = ps->mm_phase, mm_acc = ps->mm_acc,
              mm_acc_phase = ps->mm_acc_phase, mm_slot = ps->mm_slot, mm_slot_phase = ps->mm_slot_phase;
     bool ok = true;
     for (;;) {
-    if (!mbar_wait_bounded(smem_u32(&ctl->info_full[mm_slot]), mm_slot_phase, abort_local,
-                           p.timeout_ns)) {
-        ok = false;
-        break;
-    }
-    const TileSlot ts = ctl->info[mm_slot];
-    mbar_arrive(smem_u32(&ctl->info_empty[mm_slot]));
-    if (++mm_slot == kInfoSlots) {
-        mm_slot = 0;
-        mm_slot_phase ^= 1u;
-    }
-    if (ts.end) break;
-    if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[mm_acc]), mm_acc_phase ^ 1u, abort_local,
-                           p.timeout_ns)) {
-        ok = false;
-        break;
-    }
-    tc_fence_after();
-    const uint32_t d_tmem = tmem_base + mm_acc * MMA_N;
-    for (int kb = 0; kb < ts.kblocks; ++kb) {
-        if (!mbar_wait_bounded(smem_u32(&ctl->full[mm_stage]), mm_phase, abort_local,
-                               p.timeout_ns)) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->info_full[mm_slot]), mm_slot_phase,
+                                                      abort_local, p.timeout_ns))) {
+            ok = false;
+            break;
+        }
+        const TileSlot ts = ctl->info[mm_slot];
+        __syncwarp();
+        if (leader) mbar_arrive(smem_u32(&ctl->info_empty[mm_slot]));
+        if (++mm_slot == kInfoSlots) {
+            mm_slot = 0;
+            mm_slot_phase ^= 1u;
+        }
+        if (ts.end) break;
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->tmem_empty[mm_acc]), mm_acc_phase ^ 1u,
+                                                      abort_local, p.timeout_ns))) {
             ok = false;
             break;
         }
         tc_fence_after();
-        const uint32_t sa = smem_u32(smem + mm_stage * STAGE_BYTES);
-        const uint32_t sb = sa + A_BYTES;
+        const uint32_t d_tmem = tmem_base + mm_acc * MMA_N;
+        for (int kb = 0; kb < ts.kblocks; ++kb) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->full[mm_stage]), mm_phase, abort_local,
+                                                          p.timeout_ns))) {
+                ok = false;
+                break;
+            }
+            tc_fence_after();
+            if (leader) {
+                const uint32_t sa = smem_u32(smem + mm_stage * STAGE_BYTES);
+                const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-        for (int kk = 0; kk < BK / UMMA_K; ++kk)
-            mma_bf16_ss(d_tmem, sw128_kmajor_desc(sa + kk * UMMA_K * 2),
-                        sw128_kmajor_desc(sb + kk * UMMA_K * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
-        mma_commit(smem_u32(&ctl->empty[mm_stage]));
-        if (++mm_stage == STAGES) {
-            mm_stage = 0;
-            mm_phase ^= 1u;
+                for (int kk = 0; kk < BK / UMMA_K; ++kk)
+                    mma_bf16_ss(d_tmem, sw128_kmajor_desc(sa + kk * UMMA_K * 2),
+                                sw128_kmajor_desc(sb + kk * UMMA_K * 2), IDESC, (kb | kk) != 0 ? 1u : 0u);
+                mma_commit(smem_u32(&ctl->empty[mm_stage]));
+            }
+            __syncwarp();
+            if (++mm_stage == STAGES) {
+                mm_stage = 0;
+                mm_phase ^= 1u;
+            }
         }
+        if (!ok) break;
+        if (leader) mma_commit(smem_u32(&ctl->tmem_full[mm_acc]));
+        __syncwarp();
+        mm_acc ^= 1u;
+        if (mm_acc == 0) mm_acc_phase ^= 1u;
     }
-    if (!ok) break;
-    mma_commit(smem_u32(&ctl->tmem_full[mm_acc]));
-    mm_acc ^= 1u;
-    if (mm_acc == 0) mm_acc_phase ^= 1u;
+    if (leader) {
+        if (!ok) {
+            *abort_local = 1u;
+            atomicExch(&sync->abort_flag, 1u);
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+        }
+        ps->mm_stage = mm_stage;
+        ps->mm_phase = mm_phase;
+        ps->mm_acc = mm_acc;
+        ps->mm_acc_phase = mm_acc_phase;
+        ps->mm_slot = mm_slot;
+        ps->mm_slot_phase = mm_slot_phase;
     }
-    if (!ok) {
-    *abort_local = 1u;
-    atomicExch(&sync->abort_flag, 1u);
-    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
-    }
-    ps->mm_stage = mm_stage;
-    ps->mm_phase = mm_phase;
-    ps->mm_acc = mm_acc;
-    ps->mm_acc_phase = mm_acc_phase;
-    ps->mm_slot = mm_slot;
-    ps->mm_slot_phase = mm_slot_phase;
-    }
+    __syncwarp();
+}
 
 __device__ __noinline__ void gemm_epilogue(const FusedParams& p, FusedCtl* ctl, uint32_t tmem_base, int warp,
                                            int lane) {
@@ -818,8 +830,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (warp == 0) {
                 gemm_producer(p, maps, ctl, smem, arg, arg_n, lane);
             } else if (warp == 1) {
-                if (lane == 0) gemm_mma(p, ctl, smem, tmem_base);
-                __syncwarp();
+                gemm_mma(p, ctl, smem, tmem_base);
             } else if (warp >= 2 && warp <= 5) {
                 gemm_epilogue(p, ctl, tmem_base, warp, lane);
             }

@@ -232,61 +232,75 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ MMA issuer
+            // The whole warp runs the loop; one elected lane issues the MMAs and
+            // commits (a converged issuing warp keeps the tensor pipe's queue
+            // fuller than a lone lane); wait results are made warp-uniform.
+            const bool leader = elect_one();
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0, slot = 0, slot_phase = 0;
             bool ok = true;
             for (;;) {
-                if (!mbar_wait_bounded(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word, p.timeout_ns)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->slot_full[slot]), slot_phase,
+                                                              abort_word, p.timeout_ns))) {
                     ok = false;
                     break;
                 }
                 const int tile_e = ctl->slot[slot].x;
-                mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
+                __syncwarp();
+                if (leader) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
                 if (++slot == kSlots) {
                     slot = 0;
                     slot_phase ^= 1u;
                 }
                 if (tile_e < 0) break;
-                if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, abort_word, p.timeout_ns)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u,
+                                                              abort_word, p.timeout_ns))) {
                     ok = false;
                     break;
                 }
                 tc_fence_after();
                 const uint32_t d_tmem = tmem_base + acc * MMA_N;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_word, p.timeout_ns)) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_word, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
+                    if (leader) {
+                        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                        const uint32_t sb = sa + A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < BK / UMMA_K; ++kk) {
-                        const uint64_t ad = sw128_kmajor_desc(sa + kk * UMMA_K * 2);
-                        const uint64_t bd = sw128_kmajor_desc(sb + kk * UMMA_K * 2);
-                        mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        for (int kk = 0; kk < BK / UMMA_K; ++kk) {
+                            const uint64_t ad = sw128_kmajor_desc(sa + kk * UMMA_K * 2);
+                            const uint64_t bd = sw128_kmajor_desc(sb + kk * UMMA_K * 2);
+                            mma_bf16_ss(d_tmem, ad, bd, IDESC, (kb | kk) != 0 ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&ctl->empty[stage]));
                     }
-                    mma_commit(smem_u32(&ctl->empty[stage]));
+                    __syncwarp();
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&ctl->tmem_full[acc]));
+                if (leader) mma_commit(smem_u32(&ctl->tmem_full[acc]));
+                __syncwarp();
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            if (!ok) {
-                *abort_word = 1u;
-                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+            if (leader) {
+                if (!ok) {
+                    *abort_word = 1u;
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmMma);
+                }
+                // All MMAs issued by this thread complete before TMEM is freed.
+                mma_commit(smem_u32(&ctl->drain));
+                if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0u, never, p.timeout_ns))
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmDrain);
             }
-            // All MMAs issued by this thread complete before TMEM is freed.
-            mma_commit(smem_u32(&ctl->drain));
-            if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0u, never, p.timeout_ns))
-                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmDrain);
         }
         __syncwarp();
     } else {

@@ -190,12 +190,15 @@ __global__ void __launch_bounds__(kApproxThreads, 1)
         }
         __syncwarp();
     } else if (warp == 1) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ MMA issuer
+            // whole warp, one elected lane issues (see the grouped GEMMs)
+            const bool leader = elect_one();
             uint32_t stage = 0, phase = 0, acc = 0, acc_phase = 0;
             bool ok = true;
             for (int c = 0; ok && c < n_chunks; ++c) {
-                if (!mbar_wait_bounded(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u, abort_word, timeout_ns)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->tmem_empty[acc]), acc_phase ^ 1u,
+                                                              abort_word, timeout_ns))) {
                     ok = false;
                     break;
                 }
@@ -204,37 +207,44 @@ __global__ void __launch_bounds__(kApproxThreads, 1)
                 const int kb0 = c * kChunkKb;
                 const int kb1 = min(kb0 + kChunkKb, kb_total);
                 for (int kb = kb0; kb < kb1; ++kb) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_word, timeout_ns)) {
+                    if (!__all_sync(0xffffffffu,
+                                    mbar_wait_bounded(smem_u32(&ctl->full[stage]), phase, abort_word, timeout_ns))) {
                         ok = false;
                         break;
                     }
                     tc_fence_after();
-                    const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
-                    const uint32_t sb = sa + C::A_BYTES;
+                    if (leader) {
+                        const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+                        const uint32_t sb = sa + C::A_BYTES;
 #pragma unroll
-                    for (int kk = 0; kk < 4; ++kk) {
-                        const uint64_t ad = sw128_kmajor_desc(sa + kk * 32);
-                        const uint64_t bd = sw128_kmajor_desc(sb + kk * 32);
-                        mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        for (int kk = 0; kk < 4; ++kk) {
+                            const uint64_t ad = sw128_kmajor_desc(sa + kk * 32);
+                            const uint64_t bd = sw128_kmajor_desc(sb + kk * 32);
+                            mma_bf16_ss(d_tmem, ad, bd, C::IDESC, (kb != kb0 || kk != 0) ? 1u : 0u);
+                        }
+                        mma_commit(smem_u32(&ctl->empty[stage]));
                     }
-                    mma_commit(smem_u32(&ctl->empty[stage]));
+                    __syncwarp();
                     if (++stage == C::STAGES) {
                         stage = 0;
                         phase ^= 1u;
                     }
                 }
                 if (!ok) break;
-                mma_commit(smem_u32(&ctl->tmem_full[acc]));
+                if (leader) mma_commit(smem_u32(&ctl->tmem_full[acc]));
+                __syncwarp();
                 acc ^= 1u;
                 if (acc == 0) acc_phase ^= 1u;
             }
-            if (!ok) {
-                *abort_word = 1u;
-                report_error(status, MK_ERR_TIMEOUT, kSiteGemmMma);
+            if (leader) {
+                if (!ok) {
+                    *abort_word = 1u;
+                    report_error(status, MK_ERR_TIMEOUT, kSiteGemmMma);
+                }
+                mma_commit(smem_u32(&ctl->drain));
+                if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0u, never, timeout_ns))
+                    report_error(status, MK_ERR_TIMEOUT, kSiteGemmDrain);
             }
-            mma_commit(smem_u32(&ctl->drain));
-            if (!mbar_wait_bounded(smem_u32(&ctl->drain), 0u, never, timeout_ns))
-                report_error(status, MK_ERR_TIMEOUT, kSiteGemmDrain);
         }
         __syncwarp();
     } else {
