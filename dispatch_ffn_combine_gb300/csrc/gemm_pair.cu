@@ -217,15 +217,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);  // CTA 0's barriers
 
     if (warp == 0) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ claims (CTA 0) + TMA producer (both)
+            // whole warp, one elected lane claims, writes the slots, arrives and issues the copies
+            const bool leader = elect_one();
+            const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
             const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);
             const uint32_t peer_slot0 = mapa_shared(smem_u32(&ctl->slot[0]), peer);
             const uint32_t peer_slot_full0 = mapa_shared(smem_u32(&ctl->slot_full[0]), peer);
             const CUtensorMap* mb = (MODE == 0 && rank == 1) ? &tmB1 : &tmB0;
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
-            uint32_t tk = (rank == 0) ? atomicAdd(p.ticket, 1u) : 0u;
+            uint32_t tk = (rank == 0 && leader) ? atomicAdd(p.ticket, 1u) : 0u;
+            tk = __shfl_sync(0xffffffffu, tk, lead);
             for (;;) {
                 int4 info;
                 int cur_tile = -1;  // CTA 0 only: the claimed tile's index
@@ -237,24 +241,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const PairTile ti = decode_pair_tile(tile, ctl, p);
                         info = make_int4(ti.e, ti.row0, ti.rows, ti.n0);
                     }
-                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]), slot_phase ^ 1u, abort_word,
-                                                   p.timeout_ns)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]),
+                                                                          slot_phase ^ 1u, abort_word,
+                                                                          p.timeout_ns))) {
                         ok = false;
                         break;
                     }
-                    ctl->slot[slot] = info;
-                    st_shared_cluster_v4(peer_slot0 + slot * static_cast<uint32_t>(sizeof(int4)), info);
-                    mbar_arrive(smem_u32(&ctl->slot_full[slot]));
-                    mbar_arrive_cluster(peer_slot_full0 + slot * 8u);
-                    if (tile >= 0) tk = atomicAdd(p.ticket, 1u);  // used after this tile's loads
+                    if (leader) {
+                        ctl->slot[slot] = info;
+                        st_shared_cluster_v4(peer_slot0 + slot * static_cast<uint32_t>(sizeof(int4)), info);
+                        mbar_arrive(smem_u32(&ctl->slot_full[slot]));
+                        mbar_arrive_cluster(peer_slot_full0 + slot * 8u);
+                        if (tile >= 0) tk = atomicAdd(p.ticket, 1u);  // used after this tile's loads
+                    }
+                    tk = __shfl_sync(0xffffffffu, tk, lead);
                 } else {
-                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase, abort_word,
-                                                   p.timeout_ns)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]),
+                                                                          slot_phase, abort_word, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
                     info = ctl->slot[slot];
-                    mbar_arrive_cluster(slot_empty0 + slot * 8u);
+                    __syncwarp();
+                    if (leader) mbar_arrive_cluster(slot_empty0 + slot * 8u);
                 }
                 if (++slot == kPairSlots) {
                     slot = 0;
@@ -267,28 +276,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int b_row = info.x * p.b_rows_per_expert + info.w +
                                   static_cast<int>(rank) * ((MODE == 0 && half) ? BM / 2 : p.b_half_rows);
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait_bounded_cluster(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word,
-                                                   p.timeout_ns)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->empty[stage]),
+                                                                          phase ^ 1u, abort_word, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
-                    const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
-                    const uint32_t sb = sa + PA_BYTES;
+                    if (leader) {
+                        const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
+                        const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
+                        const uint32_t sb = sa + PA_BYTES;
+                        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), PTX_BYTES);
+                        const bool stall = p.stall_first_stage && rank == 0 && cur_tile == 0 && kb == 0;
+                        if (!stall) {  // injected stall: the stage is armed but this CTA's half never comes
+                            tma_load_2d_pair(sa, &tmA, kb * BK, a_row, fb);
+                            if (MODE == 0 && half) {
+                                tma_load_2d_pair(sb, &tmB0h, kb * BK, b_row, fb);
+                                tma_load_2d_pair(sb + PB_BYTES / 2, &tmB1h, kb * BK, b_row, fb);
+                            } else {
+                                tma_load_2d_pair(sb, mb, kb * BK, b_row, fb);
+                            }
+                        }
+                    }
+                    __syncwarp();
                     if (rank == 0) {
-                        mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), PTX_BYTES);
                         issued |= 1u << stage;
                         last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                    }
-                    const bool stall = p.stall_first_stage && rank == 0 && cur_tile == 0 && kb == 0;
-                    if (!stall) {  // injected stall: the stage is armed but this CTA's half never comes
-                        tma_load_2d_pair(sa, &tmA, kb * BK, a_row, fb);
-                        if (MODE == 0 && half) {
-                            tma_load_2d_pair(sb, &tmB0h, kb * BK, b_row, fb);
-                            tma_load_2d_pair(sb + PB_BYTES / 2, &tmB1h, kb * BK, b_row, fb);
-                        } else {
-                            tma_load_2d_pair(sb, mb, kb * BK, b_row, fb);
-                        }
                     }
                     if (++stage == PSTAGES) {
                         stage = 0;
@@ -297,14 +309,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
             }
-            if (!ok) {
-                raise_abort(ctl, peer);
-                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+            if (leader) {
+                if (!ok) {
+                    raise_abort(ctl, peer);
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+                }
+                // CTA 0: every stage it armed completes (or times out) before the CTA exits.
+                for (int s = 0; s < PSTAGES; ++s)
+                    if ((issued >> s) & 1u)
+                        mbar_wait_bounded_cluster(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never,
+                                                  p.timeout_ns);
             }
-            // CTA 0: every stage it armed completes (or times out) before the CTA exits.
-            for (int s = 0; s < PSTAGES; ++s)
-                if ((issued >> s) & 1u)
-                    mbar_wait_bounded_cluster(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == 1) {
