@@ -165,13 +165,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const volatile uint32_t* never = &ctl->zero;
 
     if (warp == 0) {
-        if (lane == 0) {
+        {
             // ------------------------------------------------ tile claims + TMA producer
+            // whole warp; one elected lane claims, writes the slots and issues the copies
+            const bool leader = elect_one();
+            const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
             // One ticket per tile.  The next ticket is taken before this tile's
             // loads and used after them, so the atomic's latency hides behind them.
-            uint32_t tk = atomicAdd(p.ticket, 1u);
+            uint32_t tk = leader ? atomicAdd(p.ticket, 1u) : 0u;
+            tk = __shfl_sync(0xffffffffu, tk, lead);
             for (;;) {
                 const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
                 int4 info = make_int4(-1, 0, 0, 0);
@@ -180,40 +184,48 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ti = decode_tile(tile, p);
                     info = make_int4(ti.e, ti.row0, ti.rows, ti.n0);
                 }
-                if (!mbar_wait_bounded(smem_u32(&ctl->slot_empty[slot]), slot_phase ^ 1u, abort_word, p.timeout_ns)) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->slot_empty[slot]), slot_phase ^ 1u,
+                                                              abort_word, p.timeout_ns))) {
                     ok = false;
                     break;
                 }
-                ctl->slot[slot] = info;
-                mbar_arrive(smem_u32(&ctl->slot_full[slot]));
+                if (leader) {
+                    ctl->slot[slot] = info;
+                    mbar_arrive(smem_u32(&ctl->slot_full[slot]));
+                }
                 if (++slot == kSlots) {
                     slot = 0;
                     slot_phase ^= 1u;
                 }
                 if (tile < 0) break;
-                tk = atomicAdd(p.ticket, 1u);
+                if (leader) tk = atomicAdd(p.ticket, 1u);
+                tk = __shfl_sync(0xffffffffu, tk, lead);
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
-                    if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, p.timeout_ns)) {
+                    if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u,
+                                                                  abort_word, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
-                    const uint32_t fb = smem_u32(&ctl->full[stage]);
-                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
-                    const uint32_t sb = sa + A_BYTES;
-                    mbar_arrive_expect_tx(fb, STAGE_BYTES);
-                    issued |= 1u << stage;
-                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
-                    const bool stall = p.stall_first_stage && tile == 0 && kb == 0;
-                    if (!stall) {  // injected stall: the stage is announced but never filled
-                        tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
-                        if (MODE == 0) {
-                            tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
-                            tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
-                        } else {
-                            tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                    if (leader) {
+                        const uint32_t fb = smem_u32(&ctl->full[stage]);
+                        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                        const uint32_t sb = sa + A_BYTES;
+                        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        const bool stall = p.stall_first_stage && tile == 0 && kb == 0;
+                        if (!stall) {  // injected stall: the stage is announced but never filled
+                            tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
+                            if (MODE == 0) {
+                                tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                                tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
+                            } else {
+                                tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
+                            }
                         }
                     }
+                    __syncwarp();
+                    issued |= 1u << stage;
+                    last_par = (last_par & ~(1u << stage)) | (phase << stage);
                     if (++stage == STAGES) {
                         stage = 0;
                         phase ^= 1u;
@@ -221,14 +233,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
             }
-            if (!ok) {
-                *abort_word = 1u;
-                report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+            if (leader) {
+                if (!ok) {
+                    *abort_word = 1u;
+                    report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+                }
+                // Every copy this thread started must land before the CTA exits.
+                for (int s = 0; s < STAGES; ++s)
+                    if ((issued >> s) & 1u)
+                        mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
             }
-            // Every copy this thread started must land before the CTA exits.
-            for (int s = 0; s < STAGES; ++s)
-                if ((issued >> s) & 1u)
-                    mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, p.timeout_ns);
         }
         __syncwarp();
     } else if (warp == 1) {
