@@ -172,12 +172,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
-            // One ticket per tile.  The next ticket is taken before this tile's
-            // loads and used after them, so the atomic's latency hides behind them.
+            // One ticket per tile.  The elected lane takes the next ticket before this tile's
+            // loads and the warp reads it (one shuffle) after them, so the atomic's
+            // latency hides behind them.
             uint32_t tk = leader ? atomicAdd(p.ticket, 1u) : 0u;
-            tk = __shfl_sync(0xffffffffu, tk, lead);
             for (;;) {
-                const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
+                const uint32_t tkw = __shfl_sync(0xffffffffu, tk, lead);
+                const int tile = tkw < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tkw) : -1;
                 int4 info = make_int4(-1, 0, 0, 0);
                 TileInfo ti{};
                 if (tile >= 0) {
@@ -199,7 +200,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (tile < 0) break;
                 if (leader) tk = atomicAdd(p.ticket, 1u);
-                tk = __shfl_sync(0xffffffffu, tk, lead);
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u,

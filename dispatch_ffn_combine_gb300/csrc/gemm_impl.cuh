@@ -34,8 +34,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return (g / (1.0f 
 //     h[n0 + c] = bf16(silu(g_c) * u_c), c < G
 //   weighted, C columns at tbase:  P[n0 + c] = bf16(wr * acc_c), c < C
 // A 128 x 256 single-CTA or 256 x 256 pair accumulator gives each lane
-// G = 128 (gate | up) or C = 256; the 128-row pair tile folds its upper output
-// columns into lanes 64..127, giving each lane G = 64 or C = 128.
+// G = 128 (gate | up) or C = 256.
 template <int G>
 __device__ __forceinline__ void epilogue_swiglu_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
 #pragma unroll 1

@@ -10,13 +10,20 @@
 //               rows of W3; gemm2: W2 rows n0 + 128 r ...) and receives its
 //               128 rows x 256 columns of the accumulator in its own TMEM.
 //               One thread of CTA 0 issues the MMAs (M = 256, N = 256, K = 16).
-//   half tile   an expert with an odd number of 128-row blocks ends in a pair
-//               block of at most 128 rows, run as an M = 128 pair MMA: each CTA
-//               holds 64 rows, and TMEM lanes 0-63 get output columns 0-127 of
-//               those rows, lanes 64-127 columns 128-255.  For gemm1 each CTA
-//               then loads 64 gate rows of W1 and the same 64 rows of W3, so
-//               every lane holds matching gate and up columns.  The pair thus
-//               computes no more rows than the single-CTA kernel.
+//   swap tile   an expert's last pair block with fewer than 256 rows runs with
+//               the operands exchanged: the 256 weight rows are the M side
+//               (128 per CTA) and the block's rows the N side, N = rows rounded
+//               up to 16 (CTA r holds rows [N/2 r, N/2 r + N/2), loaded with the
+//               smallest 16/32/64/128-row box that covers them), so the MMAs
+//               cost N/256 of a full tile's instead of a full tile's.  TMEM lane
+//               l of CTA r then holds weight row 128 r + l for every block row.
+//               gemm1 orders each CTA's 128 weight rows as four groups of 16
+//               gate rows (W1) followed by the same 16 up rows (W3), so lanes
+//               l and l + 16 of one warp hold the gate and up values of one
+//               output column.  Each output element is the same dot product,
+//               accumulated over K in the same order (the tests check that the
+//               bits agree).  gemm1 keeps its blocks of 129-255 rows as full
+//               tiles when K < 4096 (kSwapMaxRowsShortK).
 //   why         per SM and k-block, 32 KB of operands cross L2 and shared
 //               memory instead of 48 KB (B is split, not duplicated), so seven
 //               stages (3584 cycles of MMA work) fit instead of four.
@@ -54,10 +61,17 @@ constexpr uint32_t PB_BYTES = (MMA_N / 2) * BK * 2;     // this CTA's 128 of the
 constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;  // 32 KB
 constexpr uint32_t PTX_BYTES = 2 * PSTAGE_BYTES;        // both CTAs' copies of one stage
 constexpr uint32_t PIDESC = idesc_bf16_f32(PAIR_M, MMA_N);
-constexpr uint32_t PIDESC_HALF = idesc_bf16_f32(BM, MMA_N);  // 128-row pair tile, 64 rows per CTA
 constexpr int kPairNGroup = 4;
 constexpr int kPairSlots = 4;
 constexpr uint32_t kSlotConsumers = 10;  // CTA 0: MMA + 4 epilogue warps; CTA 1: producer + 4 epilogue warps
+// Which partial pair blocks run as swap tiles.  Measured (same GPU, every
+// expert 256 + t rows): a swap tile costs 0.24-0.34 of a full tile for t <= 64
+// and less than the full tile it replaces up to t ~ 240 with K = 7168; with
+// K = 2048 gemm1's swap tiles of more than 128 rows cost up to 7 % more than
+// full tiles (the SwiGLU epilogue and the eight 16-row weight copies per
+// k-block against a short main loop), gemm2's none.
+constexpr int kSwapMaxRows = PAIR_M - 1;
+constexpr int kSwapMaxRowsShortK = BM;  // gemm1 with K < 64 k-blocks
 
 struct PairCtl {
     uint64_t full[PSTAGES];   // CTA 0: both CTAs' copies of the stage landed
@@ -91,6 +105,7 @@ struct PairParams {
     int k_blocks;       // K / 64
     int b_rows_per_expert;
     int b_half_rows;    // row offset of CTA 1's half of B in a full tile (gemm1 0: own map; gemm2 128)
+    int swap_max_rows;  // pair blocks with at most this many rows run as swap tiles (0: none)
     uint32_t* status;
     uint64_t timeout_ns;
     int stall_first_stage;  // test hook: CTA 0 of the pair that claims tile 0 never loads its first stage
@@ -100,9 +115,77 @@ struct PairParams {
 struct PairTile {
     int e;
     int row0;  // first row of the pair block
-    int rows;  // valid rows of the pair block (1..256); <= 128 makes it a half tile
+    int rows;  // valid rows of the pair block (1..256)
     int n0;
 };
+
+// A pair block with at most swap_max_rows rows (>= 128) runs as a swap tile.
+__device__ __forceinline__ bool is_swap(int rows, const PairParams& p) { return rows <= p.swap_max_rows; }
+
+// Swap tile: the MMA's N (block rows rounded up to 16) and the row count of
+// the activation box each CTA loads (covers its N / 2 rows).
+__device__ __forceinline__ int swap_n(int rows) { return (rows + 15) & ~15; }
+__device__ __forceinline__ int swap_box(int half_n) {
+    return half_n <= 16 ? 16 : half_n <= 32 ? 32 : half_n <= 64 ? 64 : 128;
+}
+
+// Swap-tile epilogues: this thread's TMEM lane is one weight row (output
+// column), its columns the block's rows.  A warp stores one output row per
+// step (32 or 16 consecutive columns).
+//   gemm2:  out[j][n] = bf16(wr[j] * acc_j), j < rows; the block's row weights
+//           are loaded once, lane i holding rows i, i + 32, ...
+__device__ __forceinline__ void epilogue_weighted_swap(uint32_t tbase, int rows, bf16* ocol, int64_t ld, bool n_ok,
+                                                       const float* wr) {
+    const int lane = threadIdx.x & 31;
+    float wv[PAIR_M / 32];
+#pragma unroll
+    for (int c = 0; c < PAIR_M / 32; ++c) {
+        const int j = 32 * c + lane;
+        wv[c] = (wr != nullptr && j < rows) ? wr[j] : 1.0f;
+    }
+#pragma unroll 1
+    for (int c = 0; 32 * c < rows; ++c) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(tbase + 32 * c, a);
+        float w_lane = wv[0];
+#pragma unroll
+        for (int q = 1; q < PAIR_M / 32; ++q)
+            if (q == c) w_lane = wv[q];
+        tmem_ld_wait();
+        const int nj = rows - 32 * c;
+        bf16* o = ocol + static_cast<int64_t>(32 * c) * ld;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const float wj = __shfl_sync(0xffffffffu, w_lane, jj);
+            if (n_ok && jj < nj) *o = __float2bfloat16_rn(__uint_as_float(a[jj]) * wj);
+            o += ld;
+        }
+    }
+}
+
+//   gemm1:  lanes l and l + 16 hold the gate and up rows of one column; one
+//           exchange per pair of block rows gives lane l the up value of the
+//           even row and lane l + 16 the gate value of the odd one:
+//           h[j][col] = bf16(silu(g_j) * u_j), even j by lanes 0-15, odd j by 16-31
+__device__ __forceinline__ void epilogue_swiglu_swap(uint32_t tbase, int rows, bf16* ocol, int64_t ld, bool c_ok) {
+    const bool lo = (threadIdx.x & 16) == 0;
+#pragma unroll 1
+    for (int j0 = 0; j0 < rows; j0 += 32) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(tbase + j0, a);
+        tmem_ld_wait();
+        const int nj = rows - j0;
+        bf16* o = ocol + static_cast<int64_t>(j0 + (lo ? 0 : 1)) * ld;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float x = __shfl_xor_sync(0xffffffffu, __uint_as_float(lo ? a[2 * m + 1] : a[2 * m]), 16);
+            const float g = lo ? __uint_as_float(a[2 * m]) : x;
+            const float u = lo ? x : __uint_as_float(a[2 * m + 1]);
+            if (c_ok && 2 * m + (lo ? 0 : 1) < nj) *o = __float2bfloat16_rn(silu_mul(g, u));
+            o += 2 * ld;
+        }
+    }
+}
 
 // Tile t -> (expert, pair block, N block): an expert's tiles occupy
 // [pstart[e] * n_tiles, pstart[e + 1] * n_tiles), in groups of kPairNGroup N
@@ -142,8 +225,10 @@ __device__ __forceinline__ void raise_abort(PairCtl* ctl, uint32_t peer) {
 template <int MODE>  // 0: gemm1 + SwiGLU, 1: gemm2 + row weight
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmB0h,
-                             const __grid_constant__ CUtensorMap tmB1h, const PairParams p) {
+                             const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmA16,
+                             const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64,
+                             const __grid_constant__ CUtensorMap tmB0q, const __grid_constant__ CUtensorMap tmB1q,
+                             const PairParams p) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     PairCtl* ctl = reinterpret_cast<PairCtl*>(smem + PSTAGES * PSTAGE_BYTES);
@@ -198,9 +283,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         prefetch_tensormap(&tmB0);
         if (MODE == 0) {
             prefetch_tensormap(&tmB1);
-            prefetch_tensormap(&tmB0h);
-            prefetch_tensormap(&tmB1h);
+            prefetch_tensormap(&tmB0q);
+            prefetch_tensormap(&tmB1q);
         }
+        prefetch_tensormap(&tmA16);
+        prefetch_tensormap(&tmA32);
+        prefetch_tensormap(&tmA64);
     }
     if (warp == 1) {
         tmem_alloc_pair(smem_u32(&ctl->tmem_base), TMEM_COLS);
@@ -228,13 +316,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const CUtensorMap* mb = (MODE == 0 && rank == 1) ? &tmB1 : &tmB0;
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
+            // CTA 0 takes one ticket per tile.  The leader takes the next ticket
+            // before this tile's loads and the warp reads it after them, so the
+            // atomic's round trip hides behind the loads.
             uint32_t tk = (rank == 0 && leader) ? atomicAdd(p.ticket, 1u) : 0u;
-            tk = __shfl_sync(0xffffffffu, tk, lead);
             for (;;) {
                 int4 info;
                 int cur_tile = -1;  // CTA 0 only: the claimed tile's index
                 if (rank == 0) {
-                    const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
+                    const uint32_t tkw = __shfl_sync(0xffffffffu, tk, lead);
+                    const int tile = tkw < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tkw) : -1;
                     cur_tile = tile;
                     info = make_int4(-1, 0, 0, 0);
                     if (tile >= 0) {
@@ -252,9 +343,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         st_shared_cluster_v4(peer_slot0 + slot * static_cast<uint32_t>(sizeof(int4)), info);
                         mbar_arrive(smem_u32(&ctl->slot_full[slot]));
                         mbar_arrive_cluster(peer_slot_full0 + slot * 8u);
-                        if (tile >= 0) tk = atomicAdd(p.ticket, 1u);  // used after this tile's loads
+                        if (tile >= 0) tk = atomicAdd(p.ticket, 1u);  // read after this tile's loads
                     }
-                    tk = __shfl_sync(0xffffffffu, tk, lead);
                 } else {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]),
                                                                           slot_phase, abort_word, p.timeout_ns))) {
@@ -270,11 +360,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     slot_phase ^= 1u;
                 }
                 if (info.x < 0) break;
-                const bool half = info.z <= BM;
-                const int a_row = info.y + static_cast<int>(rank) * (half ? BM / 2 : BM);
-                // gemm1 half tile: W1 rows [n0 + 64 r, +64) then the same rows of W3
-                const int b_row = info.x * p.b_rows_per_expert + info.w +
-                                  static_cast<int>(rank) * ((MODE == 0 && half) ? BM / 2 : p.b_half_rows);
+                const bool swap = is_swap(info.z, p);
+                int a_row = info.y + static_cast<int>(rank) * BM;
+                int b_row = info.x * p.b_rows_per_expert + info.w + static_cast<int>(rank) * p.b_half_rows;
+                uint32_t stage_tx = PTX_BYTES;
+                const CUtensorMap* am = &tmA;
+                if (swap) {
+                    // weights into the A region (gemm1: 64 output columns per CTA,
+                    // gemm2: 128), this CTA's N / 2 block rows into the B region
+                    const int half_n = swap_n(info.z) >> 1;
+                    const int bx = swap_box(half_n);
+                    am = bx == 16 ? &tmA16 : bx == 32 ? &tmA32 : bx == 64 ? &tmA64 : &tmA;
+                    a_row = info.y + static_cast<int>(rank) * half_n;
+                    b_row = info.x * p.b_rows_per_expert + info.w +
+                            static_cast<int>(rank) * (MODE == 0 ? BM / 2 : p.b_half_rows);
+                    stage_tx = 2u * (PA_BYTES + static_cast<uint32_t>(bx) * BK * 2u);
+                }
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->empty[stage]),
                                                                           phase ^ 1u, abort_word, p.timeout_ns))) {
@@ -285,16 +386,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const uint32_t fb = full0 + static_cast<uint32_t>(stage) * 8u;
                         const uint32_t sa = smem_u32(smem + stage * PSTAGE_BYTES);
                         const uint32_t sb = sa + PA_BYTES;
-                        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), PTX_BYTES);
+                        if (rank == 0) mbar_arrive_expect_tx(smem_u32(&ctl->full[stage]), stage_tx);
                         const bool stall = p.stall_first_stage && rank == 0 && cur_tile == 0 && kb == 0;
-                        if (!stall) {  // injected stall: the stage is armed but this CTA's half never comes
-                            tma_load_2d_pair(sa, &tmA, kb * BK, a_row, fb);
-                            if (MODE == 0 && half) {
-                                tma_load_2d_pair(sb, &tmB0h, kb * BK, b_row, fb);
-                                tma_load_2d_pair(sb + PB_BYTES / 2, &tmB1h, kb * BK, b_row, fb);
+                        if (stall) {
+                            // injected stall: the stage is armed but this CTA's half never comes
+                        } else if (swap) {
+                            if (MODE == 0) {
+#pragma unroll
+                                for (int q = 0; q < 4; ++q) {
+                                    tma_load_2d_pair(sa + q * 32 * BK * 2, &tmB0q, kb * BK, b_row + 16 * q, fb);
+                                    tma_load_2d_pair(sa + (q * 32 + 16) * BK * 2, &tmB1q, kb * BK, b_row + 16 * q, fb);
+                                }
                             } else {
-                                tma_load_2d_pair(sb, mb, kb * BK, b_row, fb);
+                                tma_load_2d_pair(sa, &tmB0, kb * BK, b_row, fb);
                             }
+                            tma_load_2d_pair(sb, am, kb * BK, a_row, fb);
+                        } else {
+                            tma_load_2d_pair(sa, &tmA, kb * BK, a_row, fb);
+                            tma_load_2d_pair(sb, mb, kb * BK, b_row, fb);
                         }
                     }
                     __syncwarp();
@@ -346,7 +455,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     slot_phase ^= 1u;
                 }
                 if (info.x < 0) break;
-                const uint32_t idesc = info.z <= BM ? PIDESC_HALF : PIDESC;
+                const uint32_t idesc = is_swap(info.z, p) ? idesc_bf16_f32(PAIR_M, swap_n(info.z)) : PIDESC;
                 if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->tmem_empty[acc]),
                                                                       acc_phase ^ 1u, abort_word, p.timeout_ns))) {
                     ok = false;
@@ -422,27 +531,29 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * MMA_N;
-            const bool half = info.z <= BM;
-            // full tile: TMEM lane = row of this CTA's 128; half tile: lane & 63 =
-            // row of this CTA's 64, lane >> 6 = which half of the output columns
-            const int rows_per_cta = half ? BM / 2 : BM;
-            const int row_here = half ? (lane_in_tile & 63) : lane_in_tile;
-            const int col_half = half ? (lane_in_tile >> 6) : 0;
-            const bool row_ok = static_cast<int>(rank) * rows_per_cta + row_here < info.z;
-            const int64_t r = static_cast<int64_t>(info.y) + static_cast<int>(rank) * rows_per_cta + row_here;
-            bf16* orow = p.out + (row_ok ? r : 0) * p.out_ld;
-            if (MODE == 0) {
-                if (half)
-                    epilogue_swiglu_w<64>(tbase, row_ok, orow, info.w + 64 * col_half, p.n_valid);
-                else
-                    epilogue_swiglu(tbase, row_ok, orow, info.w, p.n_valid);
+            if (is_swap(info.z, p)) {
+                bf16* oblock = p.out + static_cast<int64_t>(info.y) * p.out_ld;
+                if (MODE == 0) {
+                    const int col = info.w + static_cast<int>(rank) * (BM / 2) + sub * 16 + (lane & 15);
+                    const bool c_ok = col < p.n_valid;
+                    epilogue_swiglu_swap(tbase, info.z, oblock + (c_ok ? col : 0), p.out_ld, c_ok);
+                } else {
+                    const int n = info.w + static_cast<int>(rank) * (MMA_N / 2) + lane_in_tile;
+                    const bool n_ok = n < p.n_valid;
+                    epilogue_weighted_swap(tbase, info.z, oblock + (n_ok ? n : 0), p.out_ld, n_ok,
+                                           p.row_weight != nullptr ? p.row_weight + info.y : nullptr);
+                }
             } else {
-                const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
-                if (half)
-                    epilogue_weighted_w<MMA_N / 2>(tbase, row_ok, orow, info.w + (MMA_N / 2) * col_half, p.n_valid,
-                                                   wr);
-                else
+                // full tile: TMEM lane = row of this CTA's 128
+                const bool row_ok = static_cast<int>(rank) * BM + lane_in_tile < info.z;
+                const int64_t r = static_cast<int64_t>(info.y) + static_cast<int>(rank) * BM + lane_in_tile;
+                bf16* orow = p.out + (row_ok ? r : 0) * p.out_ld;
+                if (MODE == 0) {
+                    epilogue_swiglu(tbase, row_ok, orow, info.w, p.n_valid);
+                } else {
+                    const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
                     epilogue_weighted(tbase, row_ok, orow, info.w, p.n_valid, wr);
+                }
             }
             tc_fence_before();
             __syncwarp();
@@ -473,10 +584,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
 // ------------------------------------------------------------------ host side
 
+// The tensor maps of one launch.  a*: the activation rows (x_perm or h) in
+// boxes of 128 / 16 / 32 / 64 rows; b0, b1: the weights in 128-row boxes
+// (gemm1 W1, W3; gemm2 W2 twice); b0q, b1q: 16-row boxes (gemm1 swap tiles).
+struct PairMaps {
+    CUtensorMap a, b0, b1, a16, a32, a64, b0q, b1q;
+};
+
 template <int MODE>
-cudaError_t launch_pair_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1,
-                             const CUtensorMap& b0h, const CUtensorMap& b1h, const PairParams& p, int64_t S,
-                             cudaStream_t s) {
+cudaError_t launch_pair_mode(const PairMaps& m, const PairParams& p, int64_t S, cudaStream_t s) {
     static int configured[64] = {0};
     static int max_clusters[64] = {0};
     int dev = 0;
@@ -510,19 +626,24 @@ cudaError_t launch_pair_mode(const CUtensorMap& a, const CUtensorMap& b0, const 
     const int64_t max_tiles = ((S + PAIR_M - 1) / PAIR_M + p.E) * static_cast<int64_t>(p.n_tiles);
     const int clusters = static_cast<int>(std::min<int64_t>(max_clusters[slot], std::max<int64_t>(max_tiles, 1)));
     cfg.gridDim = dim3(2 * clusters);
-    err = cudaLaunchKernelEx(&cfg, fn, a, b0, b1, b0h, b1h, p);
+    err = cudaLaunchKernelEx(&cfg, fn, m.a, m.b0, m.b1, m.a16, m.a32, m.a64, m.b0q, m.b1q, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
 }  // namespace
 
+bool make_act_maps(PairMaps* m, const void* act, uint64_t inner, uint64_t rows) {
+    return make_map(&m->a, act, inner, rows, BM) && make_map(&m->a16, act, inner, rows, 16) &&
+           make_map(&m->a32, act, inner, rows, 32) && make_map(&m->a64, act, inner, rows, 64);
+}
+
 cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s) {
-    CUtensorMap ma, mb0, mb1, mb0h, mb1h;
+    PairMaps m;
     const uint64_t wrows = static_cast<uint64_t>(a.E) * a.f;
-    if (!make_map(&ma, a.x_perm, a.d, a.S, BM) || !make_map(&mb0, a.w1, a.d, wrows, MMA_N / 2) ||
-        !make_map(&mb1, a.w3, a.d, wrows, MMA_N / 2) || !make_map(&mb0h, a.w1, a.d, wrows, MMA_N / 4) ||
-        !make_map(&mb1h, a.w3, a.d, wrows, MMA_N / 4))
+    if (!make_act_maps(&m, a.x_perm, a.d, a.S) || !make_map(&m.b0, a.w1, a.d, wrows, MMA_N / 2) ||
+        !make_map(&m.b1, a.w3, a.d, wrows, MMA_N / 2) || !make_map(&m.b0q, a.w1, a.d, wrows, 16) ||
+        !make_map(&m.b1q, a.w3, a.d, wrows, 16))
         return cudaErrorInvalidValue;
     PairParams p;
     p.offsets = a.offsets;
@@ -537,18 +658,19 @@ cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s) {
     p.k_blocks = a.d / BK;
     p.b_rows_per_expert = a.f;
     p.b_half_rows = 0;  // full tiles: CTA 1 reads the same rows of W3 through its own map
+    p.swap_max_rows = p.k_blocks >= 64 ? kSwapMaxRows : kSwapMaxRowsShortK;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
     p.ticket = a.tickets;
-    return launch_pair_mode<0>(ma, mb0, mb1, mb0h, mb1h, p, a.S, s);
+    return launch_pair_mode<0>(m, p, a.S, s);
 }
 
 cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s) {
-    CUtensorMap ma, mb0;
-    if (!make_map(&ma, a.h, a.f, a.S, BM) ||
-        !make_map(&mb0, a.w2, a.f, static_cast<uint64_t>(a.E) * a.d, MMA_N / 2))
+    PairMaps m;
+    if (!make_act_maps(&m, a.h, a.f, a.S) || !make_map(&m.b0, a.w2, a.f, static_cast<uint64_t>(a.E) * a.d, MMA_N / 2))
         return cudaErrorInvalidValue;
+    m.b1 = m.b0q = m.b1q = m.b0;  // unused by gemm2
     PairParams p;
     p.offsets = a.offsets;
     p.mtile_start = a.mtile_start;
@@ -562,11 +684,12 @@ cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s) {
     p.k_blocks = a.f / BK;
     p.b_rows_per_expert = a.d;
     p.b_half_rows = MMA_N / 2;
+    p.swap_max_rows = kSwapMaxRows;
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = 0;
     p.ticket = a.tickets + 1;
-    return launch_pair_mode<1>(ma, mb0, mb0, mb0, mb0, p, a.S, s);
+    return launch_pair_mode<1>(m, p, a.S, s);
 }
 
 // CTA pairs when experts hold 256 rows or more on average, single CTAs below:

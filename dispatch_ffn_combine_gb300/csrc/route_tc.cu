@@ -159,25 +159,20 @@ __global__ void __launch_bounds__(kApproxThreads, 1)
     const volatile uint32_t* never = &ctl->zero;
 
     if (warp == 0) {
-        {
-            // ------------------------------------------------ TMA producer (whole warp, elected lane issues)
-            const bool leader = elect_one();
+        if (lane == 0) {
+            // ------------------------------------------------ TMA producer
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0;
             bool ok = true;
             for (int kb = 0; kb < kb_total; ++kb) {
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word,
-                                                              timeout_ns))) {
+                if (!mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u, abort_word, timeout_ns)) {
                     ok = false;
                     break;
                 }
-                if (leader) {
-                    const uint32_t fb = smem_u32(&ctl->full[stage]);
-                    const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
-                    mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
-                    tma_load_2d(sa, &tmX, (kb >> 1) * 64, m0, fb);  // x block kb/2 serves its hi and mid blocks
-                    tma_load_2d(sa + C::A_BYTES, &tmW, kb * 64, 0, fb);
-                }
-                __syncwarp();
+                const uint32_t fb = smem_u32(&ctl->full[stage]);
+                const uint32_t sa = smem_u32(smem + stage * C::STAGE_BYTES);
+                mbar_arrive_expect_tx(fb, C::STAGE_BYTES);
+                tma_load_2d(sa, &tmX, (kb >> 1) * 64, m0, fb);  // x block kb/2 serves its hi and mid blocks
+                tma_load_2d(sa + C::A_BYTES, &tmW, kb * 64, 0, fb);
                 issued |= 1u << stage;
                 last_par = (last_par & ~(1u << stage)) | (phase << stage);
                 if (++stage == C::STAGES) {
@@ -185,15 +180,13 @@ __global__ void __launch_bounds__(kApproxThreads, 1)
                     phase ^= 1u;
                 }
             }
-            if (leader) {
-                if (!ok) {
-                    *abort_word = 1u;
-                    report_error(status, MK_ERR_TIMEOUT, kSiteGemmProducer);
-                }
-                for (int s = 0; s < C::STAGES; ++s)
-                    if ((issued >> s) & 1u)
-                        mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, timeout_ns);
+            if (!ok) {
+                *abort_word = 1u;
+                report_error(status, MK_ERR_TIMEOUT, kSiteGemmProducer);
             }
+            for (int s = 0; s < C::STAGES; ++s)
+                if ((issued >> s) & 1u)
+                    mbar_wait_bounded(smem_u32(&ctl->full[s]), (last_par >> s) & 1u, never, timeout_ns);
         }
         __syncwarp();
     } else if (warp == 1) {

@@ -75,6 +75,46 @@ def test_ffn_tile_edges_many_rows():
     _check_ffn([0, 1, 255, 256, 257, 600, 511, 513, 129], d=384, f=320, seed=60)
 
 
+@pytest.mark.parametrize("d,f", [(256, 384), (384, 320)])
+def test_ffn_swap_tile_sizes(d, f):
+    """Every expert has one full 256-row block and a partial one of 1..255
+    rows, which runs with the operands exchanged: the tails cross each
+    activation box (16 / 32 / 64 / 128 rows per CTA) and N step (16); with
+    d = 384 and ffn = 320 the last output tile of each GEMM is partly outside
+    the output."""
+    tails = [1, 8, 15, 16, 17, 31, 32, 33, 63, 64, 65, 127, 128, 129, 200, 240, 255]
+    _check_ffn([256 + t for t in tails], d=d, f=f, seed=70 + d)
+
+
+def test_ffn_swap_tile_sizes_long_k():
+    """K = 4096 (64 k-blocks): gemm1 also runs tails of 129..255 rows as swap
+    tiles (shorter K keeps them as full tiles); the tail rows are checked."""
+    tails = [1, 17, 100, 129, 200, 255]
+    counts = [256 + t for t in tails]
+    offs = np.cumsum([0] + counts)
+    sample = np.concatenate([np.arange(offs[i] + 250, offs[i + 1]) for i in range(len(counts))])
+    _check_ffn(counts, d=4096, f=256, seed=95, sample=sample)
+
+
+@pytest.mark.parametrize("d,tail", [(256, 100), (4096, 200)])
+def test_ffn_swap_tiles_bitwise_equal_full_tiles(d, tail):
+    """The same rows through a full tile and through a swap tile give the same
+    bits: expert 1 repeats expert 0's weights, and its rows after the first
+    256 repeat rows of expert 0 (the first 256 of them make a full tile)."""
+    f = 384
+    offsets, x_perm, w1, w3, w2, rw = _ffn_case([512, 256 + tail], d, f, seed=90)
+    for w in (w1, w3, w2):
+        w[1] = w[0]
+    x_perm[512 + 256:] = x_perm[:tail]
+    rw[512 + 256:] = rw[:tail]
+    h, P = mk.mk_moe_expert_ffn(x_perm.to(DEV), torch.from_numpy(offsets).to(DEV), rw.to(DEV), w1.to(DEV),
+                                w3.to(DEV), w2.to(DEV))
+    torch.cuda.synchronize()
+    h, P = h.cpu().view(torch.int16), P.cpu().view(torch.int16)
+    assert torch.equal(h[512 + 256:], h[:tail])
+    assert torch.equal(P[512 + 256:], P[:tail])
+
+
 def test_ffn_single_expert_many_tiles():
     _check_ffn([1000], d=512, f=640, seed=20)
 
