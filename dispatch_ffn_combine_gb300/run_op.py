@@ -8,6 +8,11 @@ then dispatch, then the expert FFN), outside the timed calls; then the call runs
 stream.  Prints one JSON line with the mean milliseconds per call.  This is the
 driver for profiling a single step of the layer (ncu ``-k`` on the step's
 kernel); ``bench.py`` is the one that times the whole layer.
+
+With ``--op layer --path fused --trace`` one more call records the persistent
+kernel's task trace, and a summary follows the JSON line: per task kind its
+count, span and mean duration, the GEMM tiles' mean time, and the number of
+blocks busy in each kind per time window.
 """
 from __future__ import annotations
 
@@ -16,11 +21,50 @@ import json
 
 import torch
 
-from . import (MK_PATH_FUSED, MK_PATH_STEPS, alloc_dispatch_gemm_workspace, alloc_workspace, mk_moe_combine,
-               mk_moe_dispatch, mk_moe_dispatch_gemm, mk_moe_expert_ffn, mk_moe_layer, mk_moe_route)
+from . import (MK_PATH_FUSED, MK_PATH_STEPS, TRACE_KINDS, alloc_dispatch_gemm_workspace, alloc_workspace,
+               mk_moe_combine, mk_moe_dispatch, mk_moe_dispatch_gemm, mk_moe_expert_ffn, mk_moe_layer,
+               mk_moe_layer_trace_count, mk_moe_route)
 from .workloads import CONFIGS, make_inputs
 
 OPS = ("route", "dispatch", "expert_ffn", "combine", "layer", "dispatch_gemm")
+
+
+def trace_summary(tr, n: int, windows: int = 20) -> list:
+    """Text lines describing one fused call's task records (see mk_moe_opts.trace)."""
+    import numpy as np
+
+    t = tr[: min(n, tr.shape[0])].cpu().numpy().astype(np.int64)
+    if len(t) == 0:
+        return ["no task records"]
+    start = (t[:, 4] & 0xFFFFFFFF) | (t[:, 5] << 32)
+    end = (t[:, 6] & 0xFFFFFFFF) | (t[:, 7] << 32)
+    t0 = start.min()
+    st, en = (start - t0) / 1e3, (end - t0) / 1e3  # microseconds from the first task
+    tiles = t[:, 3] & 0x7FFFFFFF
+    span = float(en.max())
+    lines = [f"records {len(t)}, span {span:.1f} us"]
+    for kind in sorted(set(t[:, 1].tolist())):
+        m = t[:, 1] == kind
+        name = TRACE_KINDS.get(int(kind), str(kind))
+        line = (f"  {name:8s} tasks {int(m.sum()):6d}  first start {st[m].min():9.1f} us  last end {en[m].max():9.1f} us"
+                f"  mean {float((en[m] - st[m]).mean()):9.1f} us")
+        if tiles[m].sum() > 0:
+            line += f"  tiles {int(tiles[m].sum())}, {float((en[m] - st[m]).sum() / tiles[m].sum()):.1f} us per tile"
+        lines.append(line)
+    kinds = sorted(set(t[:, 1].tolist()))
+    w = span / windows
+    occ = np.zeros((windows, len(kinds)))
+    for i in range(len(t)):
+        a, b = st[i], en[i]
+        for j in range(int(a // w), min(int(b // w), windows - 1) + 1):
+            lo, hi = max(a, j * w), min(b, (j + 1) * w)
+            if hi > lo:
+                occ[j, kinds.index(t[i, 1])] += (hi - lo) / w
+    lines.append("  window start (us)  " + "  ".join(f"{TRACE_KINDS.get(int(k), str(k)):>8s}" for k in kinds)
+                 + "   (blocks busy)")
+    for j in range(windows):
+        lines.append(f"  {j * w:17.0f}  " + "  ".join(f"{occ[j, c]:8.1f}" for c in range(len(kinds))))
+    return lines
 
 
 def main(argv=None) -> dict:
@@ -31,7 +75,10 @@ def main(argv=None) -> dict:
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--calls", type=int, default=1)
     ap.add_argument("--path", choices=("steps", "fused"), default="steps", help="layer path (op=layer)")
+    ap.add_argument("--trace", action="store_true", help="op=layer, path=fused: summarise one traced call")
     args = ap.parse_args(argv)
+    if args.trace and (args.op != "layer" or args.path != "fused"):
+        ap.error("--trace needs --op layer --path fused")
 
     cfg = CONFIGS[args.config]
     dev = torch.device("cuda")
@@ -81,6 +128,11 @@ def main(argv=None) -> dict:
     if args.op == "layer":
         out["path"] = args.path
     print(json.dumps(out))
+    if args.trace:
+        tr = torch.zeros((1 << 18, 8), dtype=torch.int32, device=dev)
+        mk_moe_layer(x, wg, bias, inp["w1"], inp["w3"], inp["w2"], k, y=y, ws=ws, path=path, trace=tr)
+        n = mk_moe_layer_trace_count(ws, T, d, E, k, f)
+        print("\n".join(trace_summary(tr, n)))
     return out
 
 
