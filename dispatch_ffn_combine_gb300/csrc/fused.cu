@@ -201,41 +201,38 @@ struct Claim {
 };
 
 // ------------------------------------------------------------------ claiming
-// Run by thread 0 only.  A task is claimed only when its inputs are ready:
-// the head ticket's readiness is read with relaxed loads, the ticket taken
-// with a compare-and-swap (retried while the head stays ready), and an
-// acquire fence after a won claim orders the task's reads after the flags.
-
-constexpr int kClaimTries = 64;
+// Run by thread 0 only.  The mover queue is three ranges, route -> dispatch
+// -> combine, each with its own head.  All tasks of a range become ready at
+// once (route tasks from the start, dispatch tasks with the scans, combine
+// tasks when every gemm2 quarter is published), so a block claims from a range
+// only after seeing it ready, with a fetch-add that never fails under
+// contention, and never holds a ticket whose inputs may still be missing.  An
+// acquire fence after a claim orders the task's reads after the flags.
 
 __device__ Claim try_claim_mover(const FusedParams& p) {
     FusedSync* s = p.sync;
-    for (int attempt = 0; attempt < kClaimTries; ++attempt) {
-        const uint32_t h = ld_relaxed(&s->mover_head);
-        int kind, arg;
+    if (ld_relaxed(&s->route_head) < static_cast<uint32_t>(p.NR)) {
+        const uint32_t h = atomicAdd(&s->route_head, 1u);
         if (h < static_cast<uint32_t>(p.NR)) {
-            kind = kActRoute;
-            arg = static_cast<int>(h);
-        } else {
-            if (!scans_ready(p)) return {kActIdle, 0, 0};
-            const int G = p.mtile_start[p.E];
-            const uint32_t b_index = p.NR, b_comb = b_index + p.nchunks, total = b_comb + p.NK;
-            if (h >= total) return {kActExit, 0, 0};
-            if (h < b_comb) {
-                kind = kActIndex;
-                arg = static_cast<int>(h - b_index);
-            } else {
-                if (ld_relaxed(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0, 0};
-                kind = kActCombine;
-                arg = static_cast<int>(h - b_comb);
-            }
-        }
-        if (atomicCAS(&s->mover_head, h, h + 1) == h) {
             __threadfence();
-            return {kind, arg, 1};
+            return {kActRoute, static_cast<int>(h), 1};
         }
     }
-    return {kActIdle, 0, 0};
+    if (!scans_ready(p)) return {kActIdle, 0, 0};
+    if (ld_relaxed(&s->index_head) < static_cast<uint32_t>(p.nchunks)) {
+        const uint32_t h = atomicAdd(&s->index_head, 1u);
+        if (h < static_cast<uint32_t>(p.nchunks)) {
+            __threadfence();
+            return {kActIndex, static_cast<int>(h), 1};
+        }
+    }
+    if (ld_relaxed(&s->comb_head) >= static_cast<uint32_t>(p.NK)) return {kActExit, 0, 0};
+    const int G = p.mtile_start[p.E];
+    if (ld_relaxed(&s->p_done) != static_cast<uint32_t>(4 * G * p.NT2)) return {kActIdle, 0, 0};
+    const uint32_t h = atomicAdd(&s->comb_head, 1u);
+    if (h >= static_cast<uint32_t>(p.NK)) return {kActExit, 0, 0};
+    __threadfence();
+    return {kActCombine, static_cast<int>(h), 1};
 }
 
 // Compute tiles are claimed one at a time with a fetch-add on the queue head,
@@ -278,7 +275,10 @@ __device__ int controller_target(const FusedParams& p) {
     const int G = p.mtile_start[p.E];
     const double mover_total = static_cast<double>(p.NR) + p.nchunks + p.NK;
     const double compute_total = static_cast<double>(G) * (p.NT1 + p.NT2);
-    const double Rs = fmax(0.0, mover_total - static_cast<double>(ld_relaxed(&s->mover_head)));
+    const uint32_t claimed = min(ld_relaxed(&s->route_head), static_cast<uint32_t>(p.NR)) +
+                             min(ld_relaxed(&s->index_head), static_cast<uint32_t>(p.nchunks)) +
+                             min(ld_relaxed(&s->comb_head), static_cast<uint32_t>(p.NK));
+    const double Rs = fmax(0.0, mover_total - static_cast<double>(claimed));
     const double Rp = fmax(0.0, compute_total - static_cast<double>(ld_relaxed(&s->compute_head)));
     const unsigned long long cs = ld_relaxed64(&s->cyc[0]), cp = ld_relaxed64(&s->cyc[1]);
     const uint32_t ns = ld_relaxed(&s->ntask[0]), np = ld_relaxed(&s->ntask[1]);

@@ -124,7 +124,9 @@ cudaError_t launch_gemm2_auto(const FfnArgs& a, cudaStream_t s);
 // Fused persistent kernel: tickets, role accounting and cost sums (followed in
 // the workspace by the per-token-group, per-chunk and per-M-tile counters).
 struct FusedSync {
-    uint32_t mover_head;      // next mover-queue ticket
+    uint32_t route_head;      // next route task (mover queue, ready from the start)
+    uint32_t index_head;      // next dispatch task (ready once the scans are done)
+    uint32_t comb_head;       // next combine task (ready once every gemm2 quarter is published)
     uint32_t compute_head;    // next compute-queue ticket
     uint32_t movers_active;   // blocks in the mover role (adaptive mode)
     uint32_t target_movers;   // controller target (Eq. 2)
