@@ -15,10 +15,11 @@
 // Two task queues, each claimed in order with an atomic ticket (when the
 // routing comes in precomputed -- ids, weights, chunk counts and scans, from
 // the router and count/scan kernels launched just before -- the mover queue
-// starts at the dispatch chunks):
+// starts at the dispatch tasks):
 //   mover queue:   route blocks (32 tokens x 32 experts of gate logits)
-//                  -> dispatch chunks (128 tokens: rows of their slots, and the
-//                     token rows copied into those rows, each read once)
+//                  -> dispatch tasks (128 tokens, or 32 in small layers: rows
+//                     of their slots, and the token rows copied into those
+//                     rows, each read once)
 //                  -> combine tasks (32 tokens)
 //   compute queue: gemm1 tiles (expert M-tile x 128 h columns)
 //                  -> gemm2 tiles (expert M-tile x 256 output columns)
@@ -27,7 +28,7 @@
 //   last top-k of a 128-token chunk   -> expert histogram + ranks of the chunk
 //   last chunk counted                -> scans (offsets, chunk bases, tiles)
 // Readiness: dispatch tasks need the scans; gemm1 tiles need every dispatch
-// chunk (an expert's 128-row tile draws its rows from tokens all over the
+// task (an expert's 128-row tile draws its rows from tokens all over the
 // batch); gemm2 tile (g, n) needs all gemm1 tiles of g; combine tasks need
 // every gemm2 tile.  Each of the four epilogue warps
 // of a GEMM tile publishes its own 32 rows, so a tile counts 4 when done.  A block claims only tasks whose
@@ -45,6 +46,11 @@ using namespace gemm_detail;
 constexpr int kThreads = 256;
 constexpr int kInfoSlots = 4;
 constexpr int kCombineTokens = 32;
+// A dispatch task is a counting chunk, or a quarter of one when the layer has
+// fewer chunks than blocks (mid: 32 chunks for 152 blocks ran 0.430 ms, its
+// quarters 0.395; large: 256 chunks 20.19 ms, 1024 quarters 20.38).
+constexpr int kDispatchTokensSmall = 32;
+static_assert(kChunkTokens % kDispatchTokensSmall == 0, "a dispatch task stays inside one counting chunk");
 
 enum : int { kRoleMover = 0, kRoleCompute = 1 };
 enum : int { kActExit = 0, kActIdle = 1, kActRoute = 2, kActIndex = 3, kActCombine = 5, kActGemm = 6 };
@@ -123,7 +129,8 @@ struct FusedParams {
     uint32_t* topk_done;   // [nchunks]
     uint32_t* h_done;      // [G_max]
     int n_tg, n_eg, ct, nchunks;
-    int NR, NK;
+    int NR, ND, NK;  // route, dispatch and combine tasks
+    int dtok;        // tokens per dispatch task (kChunkTokens or kDispatchTokensSmall)
     int routed;  // 1: ids, weights, chunk counts, ranks and scans were computed before the launch
     int NT1, NT2, kb1, kb2;
     int mover_ctas;  // 0 adaptive; > 0 blocks [0, n) prefer mover tasks; < 0 no block prefers them
@@ -219,9 +226,9 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
         }
     }
     if (!scans_ready(p)) return {kActIdle, 0, 0};
-    if (ld_relaxed(&s->index_head) < static_cast<uint32_t>(p.nchunks)) {
+    if (ld_relaxed(&s->index_head) < static_cast<uint32_t>(p.ND)) {
         const uint32_t h = atomicAdd(&s->index_head, 1u);
-        if (h < static_cast<uint32_t>(p.nchunks)) {
+        if (h < static_cast<uint32_t>(p.ND)) {
             __threadfence();
             return {kActIndex, static_cast<int>(h), 1};
         }
@@ -239,7 +246,7 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
 // which never fails under contention and keeps the tiles in flight across the
 // grid consecutive (in the grouped order of decode_tile they share weight and
 // row blocks in L2).
-// gemm1 tiles are claimable once every dispatch chunk is done, so they never
+// gemm1 tiles are claimable once every dispatch task is done, so they never
 // wait; a gemm2 tile's inputs (the four epilogue quarters of every gemm1 tile
 // of its M-tile) may still be in flight when it is claimed, and its producer
 // waits for them.  That wait cannot deadlock: every gemm1 tile was claimed
@@ -248,7 +255,7 @@ __device__ Claim try_claim_mover(const FusedParams& p) {
 __device__ Claim try_claim_compute(const FusedParams& p) {
     FusedSync* s = p.sync;
     if (!scans_ready(p)) return {kActIdle, 0, 0};
-    if (ld_acquire(&s->index_done) != static_cast<uint32_t>(p.nchunks)) return {kActIdle, 0, 0};
+    if (ld_acquire(&s->index_done) != static_cast<uint32_t>(p.ND)) return {kActIdle, 0, 0};
     const int G = p.mtile_start[p.E];
     const uint32_t total = static_cast<uint32_t>(G) * (p.NT1 + p.NT2);
     if (ld_relaxed(&s->compute_head) >= total) return {kActExit, 0, 0};
@@ -273,10 +280,10 @@ __device__ int controller_target(const FusedParams& p) {
     const int B = static_cast<int>(gridDim.x);
     if (!scans_ready(p)) return B;
     const int G = p.mtile_start[p.E];
-    const double mover_total = static_cast<double>(p.NR) + p.nchunks + p.NK;
+    const double mover_total = static_cast<double>(p.NR) + p.ND + p.NK;
     const double compute_total = static_cast<double>(G) * (p.NT1 + p.NT2);
     const uint32_t claimed = min(ld_relaxed(&s->route_head), static_cast<uint32_t>(p.NR)) +
-                             min(ld_relaxed(&s->index_head), static_cast<uint32_t>(p.nchunks)) +
+                             min(ld_relaxed(&s->index_head), static_cast<uint32_t>(p.ND)) +
                              min(ld_relaxed(&s->comb_head), static_cast<uint32_t>(p.NK));
     const double Rs = fmax(0.0, mover_total - static_cast<double>(claimed));
     const double Rp = fmax(0.0, compute_total - static_cast<double>(ld_relaxed(&s->compute_head)));
@@ -348,9 +355,11 @@ __device__ __noinline__ void fused_route_block(uint8_t* smem, const FusedParams&
 
 // The dispatch and combine bodies keep many loads in flight; separate
 // functions keep their registers out of the persistent kernel's allocation.
-__device__ __noinline__ void fused_dispatch(const FusedParams& p, int64_t c) {
-    tasks::dispatch_chunk(p.ids, p.w, p.T, p.d, p.E, p.k, c, p.offsets, p.chunk_base, p.rank, p.x, p.x_perm,
-                          p.row_token, p.row_weight, p.slot_row);
+__device__ __noinline__ void fused_dispatch(const FusedParams& p, int64_t task) {
+    const int64_t t_begin = task * p.dtok;
+    const int nt = static_cast<int>(p.T - t_begin < p.dtok ? p.T - t_begin : p.dtok);
+    tasks::dispatch_tokens(p.ids, p.w, p.d, p.E, p.k, t_begin / kChunkTokens, t_begin, nt, p.offsets, p.chunk_base,
+                           p.rank, p.x, p.x_perm, p.row_token, p.row_weight, p.slot_row);
 }
 
 __device__ __noinline__ void fused_combine(const FusedParams& p, int64_t t0, int nt) {
@@ -957,6 +966,8 @@ cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s) {
     p.nchunks = static_cast<int>(nch);
     p.routed = a.routed ? 1 : 0;
     p.NR = a.routed ? 0 : p.n_tg * p.n_eg;  // no router tasks when the routing came in
+    p.dtok = nch < device_sm_count() ? kDispatchTokensSmall : kChunkTokens;
+    p.ND = static_cast<int>((T + p.dtok - 1) / p.dtok);
     p.NK = static_cast<int>((T + kCombineTokens - 1) / kCombineTokens);
     p.NT1 = (f + MMA_N / 2 - 1) / (MMA_N / 2);
     p.NT2 = (d + MMA_N - 1) / MMA_N;

@@ -168,21 +168,20 @@ __device__ __forceinline__ void scan_all(int32_t* s_counts, const int32_t* __res
     }
 }
 
-// Dispatch of one 128-token chunk: the row of every (token, slot), the row ->
-// token / weight maps, and the token rows copied into their k expert rows.
-// A warp per token reads the row once (8 independent 16-byte loads in flight
-// per lane) and writes it k times.
-__device__ __forceinline__ void dispatch_chunk(const int32_t* __restrict__ ids, const float* __restrict__ w, int64_t T,
-                                               int d, int E, int k, int64_t c, const int32_t* __restrict__ offsets,
-                                               const int32_t* __restrict__ chunk_base,
-                                               const int32_t* __restrict__ rank, const bf16* __restrict__ x,
-                                               bf16* __restrict__ x_perm, int32_t* __restrict__ row_token,
-                                               float* __restrict__ row_weight, int32_t* __restrict__ slot_row) {
+// Dispatch of tokens [t_begin, t_begin + nt), all inside counting chunk c:
+// the row of every (token, slot), the row -> token / weight maps, and the
+// token rows copied into their k expert rows.  A warp per token reads the row
+// once (8 independent 16-byte loads in flight per lane) and writes it k times.
+__device__ __forceinline__ void dispatch_tokens(const int32_t* __restrict__ ids, const float* __restrict__ w, int d,
+                                                int E, int k, int64_t c, int64_t t_begin, int nt,
+                                                const int32_t* __restrict__ offsets,
+                                                const int32_t* __restrict__ chunk_base,
+                                                const int32_t* __restrict__ rank, const bf16* __restrict__ x,
+                                                bf16* __restrict__ x_perm, int32_t* __restrict__ row_token,
+                                                float* __restrict__ row_weight, int32_t* __restrict__ slot_row) {
     constexpr int U = 8;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t t_begin = c * kChunkTokens;
-    const int nt = static_cast<int>((T - t_begin < kChunkTokens) ? (T - t_begin) : kChunkTokens);
     const int n16 = d / 8;
     for (int tt = warp; tt < nt; tt += kThreads / 32) {
         const int64_t t = t_begin + tt;
