@@ -381,8 +381,9 @@ struct GemmMaps {
 
 __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps& m, FusedCtl* ctl, uint8_t* smem,
                                            int arg, int arg_n, int lane) {
-    // Whole warp, lane 0 does the work: the barriers, the claims, the
-    // tile-info ring and the TMA loads; the other lanes follow its decisions.
+    // Whole warp, lane 0 does the work: the claims, the tile-info ring and the
+    // TMA loads; the other lanes follow its decisions.  The stage waits of the
+    // k-loop are made by every lane, so lane 0 issues the copies converged.
     FusedSync* sync = p.sync;
     PipeState* ps = &ctl->ps;
     volatile uint32_t* abort_local = &ctl->abort_local;
@@ -484,13 +485,9 @@ __device__ __noinline__ void gemm_producer(const FusedParams& p, const GemmMaps&
         const int e = ts.pad;
         const int b_row = ts.mode == 0 ? e * p.f + ts.n0 : e * p.d + ts.n0;
         for (int kb = 0; kb < ts.kblocks; ++kb) {
-            uint32_t free_ok = 1u;
-            if (lane == 0)
-                free_ok = mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u, abort_local,
-                                            p.timeout_ns)
-                              ? 1u
-                              : 0u;
-            if (!__shfl_sync(0xffffffffu, free_ok, 0)) {
+            // the whole warp waits for the stage (lane 0 then issues from a converged warp)
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->empty[pr_stage]), pr_phase ^ 1u,
+                                                          abort_local, p.timeout_ns))) {
                 ok = false;
                 break;
             }
