@@ -27,6 +27,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -102,9 +103,8 @@ class ClockSampler:
 
     def start(self):
         try:
-            os.makedirs(os.path.join(ROOT, "gpurun_out"), exist_ok=True)
-            self.path = os.path.join(ROOT, "gpurun_out", f"clocks_rank{self.gpu}.csv")
-            self.fh = open(self.path, "w")
+            fd, self.path = tempfile.mkstemp(prefix=f"mkmoe_clocks_gpu{self.gpu}_", suffix=".csv")
+            self.fh = os.fdopen(fd, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
                  "-lms", "20"], stdout=self.fh, stderr=subprocess.DEVNULL)
@@ -136,6 +136,10 @@ class ClockSampler:
                 except ValueError:
                     continue
                 rows.append(row)
+        try:
+            os.remove(self.path)
+        except OSError:
+            pass
         if not rows:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
         inside = rows
