@@ -32,6 +32,16 @@ def test_fused_equals_steps_bitwise(name):
     assert torch.equal(y_f.view(torch.int16), y_s.view(torch.int16))
 
 
+def test_fused_chunk_dispatch_tasks_bitwise():
+    """20000 tokens make 157 counting chunks, at least one per SM, so the
+    persistent kernel dispatches whole 128-token chunks (smaller layers take
+    quarter chunks); the result must equal the kernel-per-step path's."""
+    wl = Workload("ragged", T=20000)
+    y_f = _layer(wl, path=mk.MK_PATH_FUSED)
+    y_s = _layer(wl, path=mk.MK_PATH_STEPS)
+    assert torch.equal(y_f.view(torch.int16), y_s.view(torch.int16))
+
+
 @pytest.mark.parametrize("movers", [1, 16, 75, 151, -1])
 def test_fused_any_split_bitwise(movers):
     wl = Workload("ragged_skew")
