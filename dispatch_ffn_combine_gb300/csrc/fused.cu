@@ -12,7 +12,8 @@
 // exchanges of the README's "MoE Dispatch + FFN + Combine" row become HBM
 // copies, so the mover role runs the router, the dispatch and the combine.
 //
-// Two task queues, each claimed in order with an atomic ticket (when the
+// Two task queues claimed in order with atomic tickets: the mover queue in
+// three ranges with a head each, the compute queue with one head (when the
 // routing comes in precomputed -- ids, weights, chunk counts and scans, from
 // the router and count/scan kernels launched just before -- the mover queue
 // starts at the dispatch tasks):
