@@ -187,6 +187,26 @@ def flops_bytes(cfg, offsets):
     }
 
 
+def roofline(work: dict, ms: float, peaks: dict) -> dict:
+    """A kernel's algorithmic work per launch (flops, bytes) over its time:
+    against the tensor roof (the sustained bf16 rate) when its arithmetic
+    intensity is at or above the ridge point, else against the HBM copy rate;
+    `other` is the same kernel against the other roof."""
+    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
+    tfs = work["flops"] / (ms / 1e3) / 1e12
+    gbs = work["bytes"] / (ms / 1e3) / 1e9
+    t = {"bound": "tensor", "achieved": tfs, "peak": tensor_peak, "unit": "TFLOP/s", "frac": tfs / tensor_peak}
+    h = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}
+    src = peaks.get("source", "")
+    if work["flops"] and work["flops"] / max(work["bytes"], 1) >= ridge:
+        return dict(t, peak_source=src + " (bf16 sustained)", other=h)
+    roof = dict(h, peak_source=src + " (HBM copy)")
+    if work["flops"]:
+        roof["other"] = t
+    return roof
+
+
 def traffic_record(kernel: str, cfg_name: str):
     """DRAM bytes per launch from a committed ncu summary, only while the kernel
     source is unchanged since the counters were taken (else None)."""
@@ -402,29 +422,8 @@ def run_ours(args):
         dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
         work = fb[dom]
     dom_ms = phase_ms[dom]
-    ai = work["flops"] / max(work["bytes"], 1)
-    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
-    ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
-    if work["flops"] and ai >= ridge:
-        achieved = work["flops"] / (dom_ms / 1e3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": tensor_peak, "unit": "TFLOP/s",
-                "frac": achieved / tensor_peak}
-    else:
-        achieved = work["bytes"] / (dom_ms / 1e3) / 1e9
-        roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                "frac": achieved / peaks["hbm_gbs"]}
-    roof.update({"kernel": dom, "kernel_ms": dom_ms, "peak_source": peaks["source"] +
-                 (" (bf16 sustained)" if roof["bound"] == "tensor" else " (HBM copy)"),
-                 "traffic": traffic_record(dom, args.config)})
-    # the same kernel against the other roof (a balanced layer, such as mid, is near both)
-    if roof["bound"] == "tensor":
-        gbs = work["bytes"] / (dom_ms / 1e3) / 1e9
-        roof["other"] = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s",
-                         "frac": gbs / peaks["hbm_gbs"]}
-    elif work["flops"]:
-        tfs = work["flops"] / (dom_ms / 1e3) / 1e12
-        roof["other"] = {"bound": "tensor", "achieved": tfs, "peak": tensor_peak, "unit": "TFLOP/s",
-                         "frac": tfs / tensor_peak}
+    roof = roofline(work, dom_ms, peaks)
+    roof.update({"kernel": dom, "kernel_ms": dom_ms, "traffic": traffic_record(dom, args.config)})
 
     # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
     cpu = None

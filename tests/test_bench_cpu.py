@@ -1,0 +1,63 @@
+"""bench.py's algorithmic work per phase and its roofline arithmetic, on the
+CPU with hand-computed values (no GPU)."""
+import os
+import sys
+
+import numpy as np
+import pytest
+
+sys.path.insert(0, os.path.dirname(os.path.dirname(os.path.abspath(__file__))))
+import bench  # noqa: E402
+from dispatch_ffn_combine_gb300.workloads import CONFIGS  # noqa: E402
+
+PEAKS = {"hbm_gbs": 6793.1, "bf16_tflops": 1939.5, "bf16_tflops_sustained": 1721.2, "source": "measured"}
+
+
+def test_flops_bytes_large_hand_computed():
+    cfg = CONFIGS["large"]  # T 32768, d 7168, E 256, k 8, f 2048
+    offsets = np.arange(0, 257, dtype=np.int64) * 1024  # every expert touched, 1024 rows each
+    fb = bench.flops_bytes(cfg, offsets)
+    S = 32768 * 8
+    assert fb["gemm1"]["flops"] == 4 * S * 7168 * 2048 == 15_393_162_788_864
+    # W1 and W3 of 256 experts + x_perm read + h written
+    assert fb["gemm1"]["bytes"] == 2 * 256 * 2048 * 7168 * 2 + S * 7168 * 2 + S * 2048 * 2
+    assert fb["gemm2"]["flops"] == 2 * S * 7168 * 2048
+    assert fb["layer"]["flops"] == 6 * S * 7168 * 2048
+    assert fb["combine"] == {"flops": 0, "bytes": S * 7168 * 2 + 32768 * 7168 * 2}
+    assert fb["touched_experts"] == 256
+
+
+def test_flops_bytes_counts_only_touched_experts():
+    cfg = CONFIGS["decode"]  # T 128, d 7168, E 256, k 8, f 2048
+    counts = np.zeros(256, dtype=np.int64)
+    counts[:128] = 8  # 128 experts hold all 1024 rows
+    offsets = np.concatenate([[0], np.cumsum(counts)])
+    fb = bench.flops_bytes(cfg, offsets)
+    assert fb["touched_experts"] == 128
+    assert fb["gemm1"]["bytes"] == 2 * 128 * 2048 * 7168 * 2 + 1024 * 7168 * 2 + 1024 * 2048 * 2
+
+
+def test_roofline_tensor_bound_with_hbm_beside():
+    work = {"flops": 15.4e12, "bytes": 20.0e9}  # 770 FLOP/B, above the ridge (253 FLOP/B)
+    r = bench.roofline(work, 9.0, PEAKS)
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1721.2
+    assert r["achieved"] == pytest.approx(15.4e12 / 9.0e-3 / 1e12)
+    assert r["frac"] == pytest.approx(r["achieved"] / 1721.2)
+    assert r["other"]["bound"] == "hbm"
+    assert r["other"]["achieved"] == pytest.approx(20.0e9 / 9.0e-3 / 1e9)
+    assert r["other"]["frac"] == pytest.approx(r["other"]["achieved"] / 6793.1)
+    assert r["peak_source"].endswith("(bf16 sustained)")
+
+
+def test_roofline_hbm_bound_and_copy_kernels():
+    r = bench.roofline({"flops": 60e9, "bytes": 14.9e9}, 2.14, PEAKS)  # decode's gemm1: 4 FLOP/B
+    assert r["bound"] == "hbm" and r["frac"] == pytest.approx(14.9e9 / 2.14e-3 / 1e9 / 6793.1)
+    assert r["other"]["bound"] == "tensor"
+    c = bench.roofline({"flops": 0, "bytes": 4.2e9}, 0.65, PEAKS)  # the combine: no arithmetic
+    assert c["bound"] == "hbm" and "other" not in c
+
+
+def test_roofline_falls_back_to_burst_peak():
+    peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
+    r = bench.roofline({"flops": 1e12, "bytes": 1e9}, 1.0, peaks)
+    assert r["bound"] == "tensor" and r["peak"] == 1900.0
