@@ -92,10 +92,9 @@ typedef struct {
                               the last one after the final phase (for per-phase timing)      */
     int inject;            /* test hook, 0 = off.  MK_INJECT_STALL_GEMM1: in the first grouped
                               GEMM, the block that takes tile 0 announces one shared-memory
-                              stage but never loads
-                              it, so its consumers' bounded waits run out; the call then
-                              reports MK_ERR_TIMEOUT (no fault, no hang).  Kernel-per-step
-                              path only.                                                     */
+                              stage but never loads it, so its consumers' bounded waits run
+                              out; the call then reports MK_ERR_TIMEOUT (no fault, no hang).
+                              Kernel-per-step path only.                                     */
     int path;              /* MK_PATH_STEPS (0, default): one kernel per step, the faster
                               path on GB300 at every workload measured; MK_PATH_FUSED (1): one
                               persistent kernel whose blocks take mover or compute roles
