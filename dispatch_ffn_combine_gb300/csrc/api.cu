@@ -1,5 +1,6 @@
 // api.cu -- the C ABI (include/mkmoe.h): argument checks, workspace layout,
 // and the launch sequence of the layer's steps on the caller's stream.
+#include <atomic>
 #include <algorithm>
 #include <mutex>
 
@@ -60,7 +61,7 @@ WsLayout ws_layout(int64_t T, int d, int E, int k, int f) { return make_layout(T
 WsLayout ws_layout_dispatch(int64_t T, int d, int E, int k) { return make_layout(T, d, E, k, 64, false); }
 
 int device_sm_count() {
-    static int cache[64] = {0};
+    static std::atomic<int> cache[64];  // per device, 0 until first read (a racing first read repeats the query)
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return 1;
     if (dev >= 64) {
@@ -68,12 +69,13 @@ int device_sm_count() {
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
         return n;
     }
-    if (cache[dev] == 0) {
-        int n = 1;
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n == 0) {
+        n = 1;
         cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-        cache[dev] = n;
+        cache[dev].store(n, std::memory_order_relaxed);
     }
-    return cache[dev];
+    return n;
 }
 
 bool device_is_sm103() {

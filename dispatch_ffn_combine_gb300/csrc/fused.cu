@@ -35,6 +35,7 @@
 // of a GEMM tile publishes its own 32 rows, so a tile counts 4 when done.  A block claims only tasks whose
 // inputs are ready, so claiming in order never deadlocks; every wait is
 // bounded by %globaltimer and an abort word.
+#include <atomic>
 #include "gemm_impl.cuh"
 #include "layer_tasks.cuh"
 #include "route_impl.cuh"
@@ -879,15 +880,15 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int WT, int WE>
 cudaError_t launch_fused_shape(const FusedArgs& a, const FusedParams& p, const CUtensorMap* maps, cudaStream_t s) {
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     auto fn = fused_layer_kernel<WT, WE>;
-    if (dev < 64 && !configured[dev]) {
+    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFusedSmem));
         if (err != cudaSuccess) return err;
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_release);
     }
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, kFusedSmem);

@@ -32,6 +32,7 @@
 //             result.
 // Every wait is bounded (see mk_device.cuh): on a timeout the CTA records
 // MK_ERR_TIMEOUT, drains its own copies and MMAs, frees TMEM, returns.
+#include <atomic>
 #include "gemm_impl.cuh"
 
 namespace mk {
@@ -375,15 +376,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 template <int MODE>
 cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUtensorMap& b1, const GemmParams& p,
                         int64_t S, cudaStream_t s) {
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev < 64 && !configured[dev]) {
+    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(SMEM_BYTES));
         if (err != cudaSuccess) return err;
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_release);
     }
     // Upper bound on the tile count: every expert adds at most one partial block.
     const int64_t max_tiles = ((S + BM - 1) / BM + p.E) * static_cast<int64_t>(p.n_tiles);

@@ -46,6 +46,7 @@
 // raises the abort word of both CTAs; both leave through one cluster barrier,
 // so neither exits while the other may still touch its shared memory.
 #include <algorithm>
+#include <atomic>
 
 #include "gemm_impl.cuh"
 
@@ -593,8 +594,8 @@ struct PairMaps {
 
 template <int MODE>
 cudaError_t launch_pair_mode(const PairMaps& m, const PairParams& p, int64_t S, cudaStream_t s) {
-    static int configured[64] = {0};
-    static int max_clusters[64] = {0};
+    static std::atomic<int> configured[64];    // per device: attributes set, max_clusters valid
+    static std::atomic<int> max_clusters[64];  // written before `configured` (release / acquire)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
@@ -611,7 +612,7 @@ cudaError_t launch_pair_mode(const PairMaps& m, const PairParams& p, int64_t S, 
     cfg.stream = s;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    if (dev >= 64 || !configured[dev]) {
+    if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(PSMEM_BYTES));
         if (err != cudaSuccess) return err;
         cfg.gridDim = dim3(2 * std::max(1, device_sm_count() / 2));
@@ -619,12 +620,13 @@ cudaError_t launch_pair_mode(const PairMaps& m, const PairParams& p, int64_t S, 
         err = cudaOccupancyMaxActiveClusters(&n, fn, &cfg);
         if (err != cudaSuccess) return err;
         if (n < 1) return cudaErrorInvalidConfiguration;
-        max_clusters[slot] = n;
-        if (dev < 64) configured[dev] = 1;
+        max_clusters[slot].store(n, std::memory_order_relaxed);
+        if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     // Upper bound on the pair tiles: every expert adds at most one partial block.
     const int64_t max_tiles = ((S + PAIR_M - 1) / PAIR_M + p.E) * static_cast<int64_t>(p.n_tiles);
-    const int clusters = static_cast<int>(std::min<int64_t>(max_clusters[slot], std::max<int64_t>(max_tiles, 1)));
+    const int64_t resident = max_clusters[slot].load(std::memory_order_relaxed);
+    const int clusters = static_cast<int>(std::min<int64_t>(resident, std::max<int64_t>(max_tiles, 1)));
     cfg.gridDim = dim3(2 * clusters);
     err = cudaLaunchKernelEx(&cfg, fn, m.a, m.b0, m.b1, m.a16, m.a32, m.a64, m.b0q, m.b1q, p);
     if (err != cudaSuccess) return err;

@@ -1,6 +1,7 @@
 // route.cu -- router kernels: fp32 gate logits in a fixed summation order
 // (the block computation lives in route_impl.cuh, shared with the fused
 // layer kernel), then top-k with the renormalised softmax weights.
+#include <atomic>
 #include <math.h>
 
 #include "route_impl.cuh"
@@ -29,15 +30,15 @@ template <int WT, int WE, int HT, int MINB>
 cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* logits, cudaStream_t s) {
     using RT = RouteTile<WT, WE, HT, MINB>;
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev < 64 && !configured[dev]) {
+    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(route_logits_kernel<WT, WE, HT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    RT::SMEM);
         if (err != cudaSuccess) return err;
-        configured[dev] = 1;
+        configured[dev].store(1, std::memory_order_release);
     }
     const unsigned grid = static_cast<unsigned>(((E + RT::CE - 1) / RT::CE) * ((T + RT::CT - 1) / RT::CT));
     route_logits_kernel<WT, WE, HT, MINB><<<grid, 256, RT::SMEM, s>>>(xb, wg, bias, static_cast<int>(T), d, E, logits);

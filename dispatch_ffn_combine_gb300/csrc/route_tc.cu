@@ -41,6 +41,7 @@
 //   chunk sums in fp32: n_c u S; the bf16 split: 2^-16 S; the fixed-order
 //     logit itself: (d/32 + 6) u S; bias adds and rounding of the bound
 //     arithmetic: 8 u |A|;  u = 2^-24.
+#include <atomic>
 #include <math.h>
 
 #include <algorithm>
@@ -542,16 +543,16 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
 template <int N>
 cudaError_t launch_approx_n(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int64_t T, int E,
                             int kb_total, float* approx, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     auto fn = route_approx_kernel<N>;
-    if (dev >= 64 || !configured[dev]) {
+    if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(approx_smem<N>()));
         if (err != cudaSuccess) return err;
-        if (dev < 64) configured[dev] = 1;
+        if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     const unsigned grid = static_cast<unsigned>((T + 127) / 128);
     fn<<<grid, kApproxThreads, approx_smem<N>(), s>>>(mx, mw, bias, static_cast<int>(T), E, kb_total, approx, status,
@@ -599,15 +600,15 @@ cudaError_t launch_route_select(const bf16* x, const float* wg, const float* bia
     const float c_rel_f = zero_bound ? 0.0f : std::nextafter(static_cast<float>(c_rel), INFINITY);
     const float c_abs_f = zero_bound ? 0.0f : std::nextafter(static_cast<float>(c_abs), INFINITY);
     const size_t smem = route_select_smem(d, E);
-    static int configured[64] = {0};
+    static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (smem > 48 * 1024 && (dev >= 64 || !configured[dev])) {
+    if (smem > 48 * 1024 && (dev >= 64 || !configured[dev].load(std::memory_order_acquire))) {
         err = cudaFuncSetAttribute(route_select_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(160 * 1024));
         if (err != cudaSuccess) return err;
-        if (dev < 64) configured[dev] = 1;
+        if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     route_select_kernel<<<static_cast<unsigned>(T), kSelThreads, smem, s>>>(x, wg, bias, approx, wnorm, d, E, k,
                                                                           c_rel_f, c_abs_f, ids, w, counts,
