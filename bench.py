@@ -189,18 +189,24 @@ def flops_bytes(cfg, offsets):
 
 def roofline(work: dict, ms: float, peaks: dict) -> dict:
     """A kernel's algorithmic work per launch (flops, bytes) over its time:
-    against the tensor roof (the sustained bf16 rate) when its arithmetic
-    intensity is at or above the ridge point, else against the HBM copy rate;
-    `other` is the same kernel against the other roof."""
-    tensor_peak = peaks.get("bf16_tflops_sustained", peaks["bf16_tflops"])
+    against the tensor roof when its arithmetic intensity is at or above the
+    ridge point, else against the HBM copy rate; `other` is the same kernel
+    against the other roof.  The tensor roof is the burst bf16 rate (the
+    timed region is under a second, as the burst figure's matmul loop); the
+    fraction of the sustained rate (a seconds-long loop under the power cap)
+    is given beside it."""
+    tensor_peak = peaks["bf16_tflops"]
+    sustained = peaks.get("bf16_tflops_sustained")
     ridge = tensor_peak * 1e12 / (peaks["hbm_gbs"] * 1e9)
     tfs = work["flops"] / (ms / 1e3) / 1e12
     gbs = work["bytes"] / (ms / 1e3) / 1e9
     t = {"bound": "tensor", "achieved": tfs, "peak": tensor_peak, "unit": "TFLOP/s", "frac": tfs / tensor_peak}
+    if sustained:
+        t["sustained"] = {"peak": sustained, "frac": tfs / sustained}
     h = {"bound": "hbm", "achieved": gbs, "peak": peaks["hbm_gbs"], "unit": "GB/s", "frac": gbs / peaks["hbm_gbs"]}
     src = peaks.get("source", "")
     if work["flops"] and work["flops"] / max(work["bytes"], 1) >= ridge:
-        return dict(t, peak_source=src + " (bf16 sustained)", other=h)
+        return dict(t, peak_source=src + " (bf16 burst)", other=h)
     roof = dict(h, peak_source=src + " (HBM copy)")
     if work["flops"]:
         roof["other"] = t
@@ -278,6 +284,122 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def time_layer(mk, cfg, inp, ws, y, stream, path, mover_ctas, steps, warmup, scrub=None, clocks=None,
+               dist=False, dev=None):
+    """Warm-up, then `steps` timed layer calls on `stream` (CUDA events).
+    With `scrub` (a buffer larger than L2) L2 is flushed before every step and
+    only the steps themselves are summed; without it the steps run back to
+    back between two events.  Returns (total ms over the steps, per-phase ms
+    per step)."""
+    x, wg, bias, w1, w3, w2 = (inp[k] for k in ("x", "wg", "bias", "w1", "w3", "w2"))
+    nph = len(mk.PHASES)
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(steps)]
+    for row in ev:  # materialise the event handles before passing them to the library
+        for e in row:
+            e.record(stream)
+    torch.cuda.synchronize()
+
+    def step(i=None):
+        mk.mk_moe_layer(x, wg, bias, w1, w3, w2, cfg.k, y=y, ws=ws, phase_events=None if i is None else ev[i],
+                        stream=stream, path=path, mover_ctas=mover_ctas)
+
+    for _ in range(warmup):
+        if scrub is not None:
+            scrub.random_()
+        step()
+    st, site = mk.mk_moe_last_device_error(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"device error during warm-up: {mk.status_string(st)} site {site:#x}")
+    if clocks is not None:
+        clocks.start()
+    if dist:
+        import torch.distributed as tdist
+        tdist.barrier()
+    torch.cuda.synchronize()
+    if clocks is not None:
+        clocks.begin()
+    if scrub is not None:
+        for i in range(steps):
+            scrub.random_()
+            step(i)
+        torch.cuda.synchronize()
+        total_ms = sum(ev[i][0].elapsed_time(ev[i][nph]) for i in range(steps))
+    else:
+        t_start = torch.cuda.Event(enable_timing=True)
+        t_end = torch.cuda.Event(enable_timing=True)
+        t_start.record(stream)
+        for i in range(steps):
+            step(i)
+        t_end.record(stream)
+        torch.cuda.synchronize()
+        total_ms = t_start.elapsed_time(t_end)
+    if clocks is not None:
+        clocks.end()
+    if dist:
+        tdist.barrier()
+    st, site = mk.mk_moe_last_device_error(ws)
+    if st != mk.MK_OK:
+        raise RuntimeError(f"device error in the timed region: {mk.status_string(st)} site {site:#x}")
+    phase_ms = {}
+    if path == mk.MK_PATH_FUSED:  # event 0 before the kernels, the others after them
+        phase_ms["fused_layer"] = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)) / steps
+    else:
+        for p, name in enumerate(mk.PHASES):
+            phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(steps)) / steps
+    return total_ms, phase_ms
+
+
+def dominant_roofline(fb, phase_ms, path, peaks, fused_key="fused_layer"):
+    """The roofline object of the step that takes the most time (the whole
+    persistent kernel on the fused path)."""
+    import dispatch_ffn_combine_gb300 as mk
+    if path == mk.MK_PATH_FUSED:
+        dom, work = fused_key, fb["layer"]
+    else:
+        dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
+        work = fb[dom]
+    roof = roofline(work, phase_ms[dom], peaks)
+    roof.update({"kernel": dom, "kernel_ms": phase_ms[dom]})
+    return roof
+
+
+def needs_flush(inp) -> bool:
+    """Inputs that fit twice in L2 are flushed out of it between steps."""
+    nbytes = sum(t.numel() * t.element_size() for k, t in inp.items() if t is not None and k != "bias")
+    return nbytes < 2 * L2_BYTES
+
+
+def other_configs(mk, names, dev, stream, steps, warmup, peaks):
+    """Each other layer workload timed as the headline (both paths), one at a
+    time, its tensors freed before the next: ms/step, tokens/s, TFLOP/s, the
+    dominant kernel's roofline and the whole layer against the HBM roof."""
+    out = {}
+    for name in names:
+        cfg = CONFIGS[name]
+        inp = make_inputs(cfg, seed=0, device=dev)
+        ws = mk.alloc_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, dev)
+        y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
+        scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if needs_flush(inp) else None
+        res = {"workload": cfg.describe(), "l2": "flushed between steps" if scrub is not None else
+               "inputs larger than L2 (no flush)", "steps": steps}
+        for path, key in ((mk.MK_PATH_STEPS, "steps_path"), (mk.MK_PATH_FUSED, "fused_path")):
+            total, phase = time_layer(mk, cfg, inp, ws, y, stream, path, 0, steps, warmup, scrub=scrub)
+            ms = total / steps
+            _, _, offsets, _ = mk.mk_moe_layer_routing(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
+            fb = flops_bytes(cfg, offsets.cpu().numpy())
+            r = {"ms_per_step": ms, "tokens_per_s": cfg.T / (ms / 1e3),
+                 "tflops": fb["layer"]["flops"] / (ms / 1e3) / 1e12,
+                 "layer_hbm_frac": fb["layer"]["bytes"] / (ms / 1e3) / 1e9 / peaks["hbm_gbs"],
+                 "roofline": dominant_roofline(fb, phase, path, peaks)}
+            if path == mk.MK_PATH_STEPS:
+                r["phase_ms"] = phase
+            res[key] = r
+        out[name] = res
+        del inp, ws, y, scrub
+        torch.cuda.empty_cache()
+    return out
+
+
 def run_ours(args):
     import dispatch_ffn_combine_gb300 as mk
 
@@ -300,68 +422,13 @@ def run_ours(args):
     ws = mk.alloc_workspace(cfg.T, cfg.d, cfg.E, cfg.k, cfg.f, dev)
     y = torch.empty((cfg.T, cfg.d), dtype=torch.bfloat16, device=dev)
     stream = torch.cuda.current_stream()
-
-    input_bytes = sum(t.numel() * t.element_size() for t in (x, wg, w1, w3, w2))
-    flush = input_bytes < 2 * L2_BYTES
+    flush = needs_flush(inp)
     scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if flush else None
 
-    nph = len(mk.PHASES)
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(nph + 1)] for _ in range(args.steps)]
-    for row in ev:  # materialise the event handles before passing them to the library
-        for e in row:
-            e.record(stream)
-    torch.cuda.synchronize()
-
-    def step(i=None):
-        mk.mk_moe_layer(x, wg, bias, w1, w3, w2, cfg.k, y=y, ws=ws,
-                        phase_events=None if i is None else ev[i], stream=stream, path=args.path,
-                        mover_ctas=args.mover_ctas)
-
-    for _ in range(args.warmup):
-        step()
-        if flush:
-            scrub.random_()
-    st, site = mk.mk_moe_last_device_error(ws)
-    if st != mk.MK_OK:
-        raise RuntimeError(f"device error during warm-up: {mk.status_string(st)} site {site:#x}")
-
     clocks = ClockSampler(local)
-    clocks.start()
-    if dist:
-        tdist.barrier()
-    torch.cuda.synchronize()
-    clocks.begin()
-    if flush:
-        total_ms = 0.0
-        for i in range(args.steps):
-            scrub.random_()
-            step(i)
-        torch.cuda.synchronize()
-        total_ms = sum(ev[i][0].elapsed_time(ev[i][nph]) for i in range(args.steps))
-    else:
-        t_start = torch.cuda.Event(enable_timing=True)
-        t_end = torch.cuda.Event(enable_timing=True)
-        t_start.record(stream)
-        for i in range(args.steps):
-            step(i)
-        t_end.record(stream)
-        torch.cuda.synchronize()
-        total_ms = t_start.elapsed_time(t_end)
-    clocks.end()
-    if dist:
-        tdist.barrier()
+    total_ms, phase_ms = time_layer(mk, cfg, inp, ws, y, stream, args.path, args.mover_ctas, args.steps,
+                                    args.warmup, scrub=scrub, clocks=clocks, dist=dist, dev=dev)
     clk = clocks.stop()
-    st, site = mk.mk_moe_last_device_error(ws)
-    if st != mk.MK_OK:
-        raise RuntimeError(f"device error in the timed region: {mk.status_string(st)} site {site:#x}")
-
-    phase_ms = {}
-    if args.path == mk.MK_PATH_FUSED:  # one kernel: event 0 before it, the others after it
-        phase_ms["fused_layer"] = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(args.steps)) / args.steps
-    else:
-        for p, name in enumerate(mk.PHASES):
-            phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(args.steps)) / args.steps
-
     total_ms = max_over_ranks(total_ms, dev, dist)
     ms_per_step = total_ms / args.steps
     value = world * cfg.T / (ms_per_step / 1e3)
@@ -388,24 +455,11 @@ def run_ours(args):
         tdist.barrier()
     e2e_value = world * cfg.T / (te / args.steps / 1e3)
 
-    # ---- the other layer path on the same inputs (device buffers), for comparison:
-    # the persistent kernel with the on-GPU SM-role controller and task queue, or
-    # the kernel-per-step path when that one is timed above
+    # ---- the other layer path on the same inputs (device buffers), for comparison
     other = mk.MK_PATH_FUSED if args.path == mk.MK_PATH_STEPS else mk.MK_PATH_STEPS
-    for _ in range(args.warmup):
-        mk.mk_moe_layer(x, wg, bias, w1, w3, w2, cfg.k, y=y, ws=ws, stream=stream, path=other)
-    torch.cuda.synchronize()
-    o_ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
-    for i in range(args.steps):
-        if flush:
-            scrub.random_()
-        o_ev[i][0].record(stream)
-        mk.mk_moe_layer(x, wg, bias, w1, w3, w2, cfg.k, y=y, ws=ws, stream=stream, path=other)
-        o_ev[i][1].record(stream)
-    torch.cuda.synchronize()
-    if mk.mk_moe_last_device_error(ws)[0] != mk.MK_OK:
-        raise RuntimeError("device error on the comparison path")
-    other_ms = max_over_ranks(sum(a.elapsed_time(b) for a, b in o_ev), dev, dist) / args.steps
+    other_total, other_phase = time_layer(mk, cfg, inp, ws, y, stream, other, 0, args.steps, args.warmup,
+                                          scrub=scrub)
+    other_ms = max_over_ranks(other_total, dev, dist) / args.steps
 
     if rank != 0:
         if dist:
@@ -415,15 +469,9 @@ def run_ours(args):
     # ---- roofline of the dominant kernel
     _, _, offsets, _ = mk.mk_moe_layer_routing(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
     fb = flops_bytes(cfg, offsets.cpu().numpy())
-    if args.path == mk.MK_PATH_FUSED:
-        dom = "fused_layer"
-        work = fb["layer"]
-    else:
-        dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
-        work = fb[dom]
-    dom_ms = phase_ms[dom]
-    roof = roofline(work, dom_ms, peaks)
-    roof.update({"kernel": dom, "kernel_ms": dom_ms, "traffic": traffic_record(dom, args.config)})
+    roof = dominant_roofline(fb, phase_ms, args.path, peaks)
+    roof["traffic"] = traffic_record(roof["kernel"], args.config)
+    other_roof = dominant_roofline(fb, other_phase, other, peaks)
 
     # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
     cpu = None
@@ -433,8 +481,18 @@ def run_ours(args):
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
                "sample": f"{n} random tokens of the workload (route + k expert FFNs + combine in fp64), "
                          f"{dt:.1f} s"}
+        del host
+
+    # ---- the other workloads, one at a time (rank 0 at N=1 only)
+    configs = None
+    if world == 1 and not args.no_configs:
+        del inp, x, wg, bias, w1, w3, w2, ws, y, x_host, y_host, scrub
+        torch.cuda.empty_cache()
+        names = [n for n in ("tiny", "mid", "skewed", "decode", "large") if n != args.config]
+        configs = other_configs(mk, names, dev, stream, args.config_steps, args.warmup, peaks)
 
     layer_tflops = fb["layer"]["flops"] / (ms_per_step / 1e3) / 1e12 * world
+    path_name = lambda p: "fused persistent kernel" if p == mk.MK_PATH_FUSED else "one kernel per step"
     line = {
         "metric": "MoE layer tokens/s (TFLOP/s beside it)", "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -451,11 +509,12 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": launches_per_step(cfg, args.path) * args.steps,
-        "path": "fused persistent kernel" if args.path == mk.MK_PATH_FUSED else "one kernel per step",
+        "path": path_name(args.path),
         "mover_ctas": args.mover_ctas,
-        "other_path": {"path": "fused persistent kernel" if other == mk.MK_PATH_FUSED else "one kernel per step",
-                       "ms_per_step": other_ms, "value": world * cfg.T / (other_ms / 1e3), "unit": "tokens/s",
+        "other_path": {"path": path_name(other), "ms_per_step": other_ms, "value": world * cfg.T / (other_ms / 1e3),
+                       "unit": "tokens/s", "roofline": other_roof,
                        "note": "same inputs and timing rules, measured after the main run; not the headline"},
+        "configs": configs,
         "clocks": clk,
         "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},
     }
@@ -473,6 +532,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--cpu-budget", type=float, default=15.0, help="seconds of oracle work for cpu_baseline")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' entries")
+    ap.add_argument("--config-steps", type=int, default=20, help="timed steps per path for each other workload")
     ap.add_argument("--path", type=int, default=0, help="0: one kernel per step (default), 1: one persistent kernel")
     ap.add_argument("--mover-ctas", type=int, default=0,
                     help="fused path: 0 adaptive SM split, n > 0 fixed split with n mover blocks, -1 none")

@@ -36,7 +36,7 @@ ENTRY_POINTS = (
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
     "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count", "mk_moe_route_fallbacks",
     "mk_moe_grouped_gemm", "mk_moe_dispatch_gemm_workspace_size", "mk_moe_dispatch_gemm",
-    "mk_moe_route_approx_logits",
+    "mk_moe_route_approx_logits", "mk_moe_workspace_region",
 )
 _SIZE_RESULT = ("mk_moe_workspace_size", "mk_moe_dispatch_gemm_workspace_size")
 
@@ -92,6 +92,7 @@ def load_library():
         lib.mk_moe_dispatch_gemm_workspace_size.argtypes = [I64, I, I, I]
         lib.mk_moe_dispatch_gemm.argtypes = [P, P, P, P, I64, I, I, I, I, P, P, P, P, P, SZ, P]
         lib.mk_moe_route_approx_logits.argtypes = [P, I64, I, I, I, P, P]
+        lib.mk_moe_workspace_region.argtypes = [I64, I, I, I, I, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
         for name in ENTRY_POINTS:
             if name not in _SIZE_RESULT + ("mk_moe_status_string",):
                 getattr(lib, name).restype = I
@@ -409,3 +410,33 @@ def mk_moe_layer_routing(ws, T, d, E, k, ffn, stream=None):
                                              _stream(stream))
     _check(st, "mk_moe_layer_routing")
     return ids, w, off, slot
+
+
+# Workspace regions (mk_ws_region): name -> (id, dtype, shape(T, d, E, k, ffn))
+WS_REGIONS = {
+    "ids": (0, torch.int32, lambda T, d, E, k, f: (T, k)),
+    "w": (1, torch.float32, lambda T, d, E, k, f: (T, k)),
+    "offsets": (2, torch.int32, lambda T, d, E, k, f: (E + 1,)),
+    "row_token": (3, torch.int32, lambda T, d, E, k, f: (T * k,)),
+    "row_weight": (4, torch.float32, lambda T, d, E, k, f: (T * k,)),
+    "slot_row": (5, torch.int32, lambda T, d, E, k, f: (T, k)),
+    "x_perm": (6, torch.bfloat16, lambda T, d, E, k, f: (T * k, d)),
+    "h": (7, torch.bfloat16, lambda T, d, E, k, f: (T * k, f)),
+    "P": (8, torch.bfloat16, lambda T, d, E, k, f: (T * k, d)),
+}
+
+
+def mk_moe_workspace_region(T, d, E, k, ffn, region):
+    """(offset, bytes) of a workspace region (host arithmetic, no GPU call)."""
+    rid = WS_REGIONS[region][0] if isinstance(region, str) else int(region)
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(load_library().mk_moe_workspace_region(T, d, E, k, ffn, rid, ctypes.byref(off), ctypes.byref(nb)),
+           "mk_moe_workspace_region")
+    return int(off.value), int(nb.value)
+
+
+def workspace_view(ws, T, d, E, k, ffn, region):
+    """A typed view (no copy) of a region the last mk_moe_layer call on ws filled."""
+    _, dtype, shape = WS_REGIONS[region]
+    off, nb = mk_moe_workspace_region(T, d, E, k, ffn, region)
+    return ws[off:off + nb].view(dtype).view(shape(T, d, E, k, ffn))

@@ -90,7 +90,7 @@ bool device_is_sm103() {
 
 using namespace mk;
 
-namespace {
+namespace mk {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
@@ -104,6 +104,10 @@ mk_status check_sizes(int64_t T, int d, int E, int k, int f_or_64) {
     if (static_cast<int64_t>(E) * std::max(d, f_or_64) >= (int64_t(1) << 31)) return MK_ERR_UNSUPPORTED;
     return MK_OK;
 }
+
+}  // namespace mk
+
+namespace {
 
 mk_status check_ws(const void* ws, size_t ws_bytes, const WsLayout& L) {
     if (ws == nullptr || (reinterpret_cast<uintptr_t>(ws) & 255u) != 0 || ws_bytes < L.total) return MK_ERR_WORKSPACE;
@@ -752,6 +756,26 @@ mk_status mk_moe_route_approx_logits(const void* ws, int64_t T, int d, int E, in
     const WsLayout L = ws_layout_dispatch(T, d, E, k);  // the logits sit at the same offset in every layout
     MK_TRY(cudaMemcpyAsync(out, static_cast<const uint8_t*>(ws) + L.logits, static_cast<size_t>(T) * E * 4,
                            cudaMemcpyDeviceToDevice, static_cast<cudaStream_t>(stream)));
+    return MK_OK;
+}
+
+mk_status mk_moe_workspace_region(int64_t T, int d, int E, int k, int ffn, int region, size_t* offset,
+                                  size_t* bytes) {
+    if (check_sizes(T, d, E, k, ffn) != MK_OK || offset == nullptr || bytes == nullptr) return MK_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(T, d, E, k, ffn);
+    const size_t S = static_cast<size_t>(T) * k;
+    switch (region) {
+        case MK_WS_IDS: *offset = L.ids; *bytes = S * 4; break;
+        case MK_WS_W: *offset = L.w; *bytes = S * 4; break;
+        case MK_WS_OFFSETS: *offset = L.offsets; *bytes = (static_cast<size_t>(E) + 1) * 4; break;
+        case MK_WS_ROW_TOKEN: *offset = L.row_token; *bytes = S * 4; break;
+        case MK_WS_ROW_WEIGHT: *offset = L.row_weight; *bytes = S * 4; break;
+        case MK_WS_SLOT_ROW: *offset = L.slot_row; *bytes = S * 4; break;
+        case MK_WS_X_PERM: *offset = L.x_perm; *bytes = S * d * 2; break;
+        case MK_WS_H: *offset = L.h; *bytes = S * ffn * 2; break;
+        case MK_WS_P: *offset = L.P; *bytes = S * d * 2; break;
+        default: return MK_ERR_INVALID_ARG;
+    }
     return MK_OK;
 }
 

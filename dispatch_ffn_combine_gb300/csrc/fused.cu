@@ -885,10 +885,10 @@ cudaError_t launch_fused_shape(const FusedArgs& a, const FusedParams& p, const C
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
     auto fn = fused_layer_kernel<WT, WE>;
-    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+    if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(fn, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(kFusedSmem));
         if (err != cudaSuccess) return err;
-        configured[dev].store(1, std::memory_order_release);
+        if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     int per_sm = 0;
     err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fn, kThreads, kFusedSmem);

@@ -380,11 +380,11 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUten
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+    if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(grouped_gemm_kernel<MODE>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    static_cast<int>(SMEM_BYTES));
         if (err != cudaSuccess) return err;
-        configured[dev].store(1, std::memory_order_release);
+        if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     // Upper bound on the tile count: every expert adds at most one partial block.
     const int64_t max_tiles = ((S + BM - 1) / BM + p.E) * static_cast<int64_t>(p.n_tiles);

@@ -177,6 +177,11 @@ size_t fused_sync_bytes(int64_t T, int E, int k);
 cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s);
 
+// Argument checks every entry point shares: sizes within the limits the
+// header states (MK_ERR_INVALID_ARG / MK_ERR_UNSUPPORTED), and 16-byte alignment.
+mk_status check_sizes(int64_t T, int d, int E, int k, int f_or_64);
+bool aligned16(const void* p);
+
 int device_sm_count();      // SMs of the current device (cached per device)
 bool device_is_sm103();     // current device is compute capability 10.3
 

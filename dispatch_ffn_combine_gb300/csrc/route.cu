@@ -34,11 +34,11 @@ cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
     if (err != cudaSuccess) return err;
-    if (dev < 64 && !configured[dev].load(std::memory_order_acquire)) {
+    if (dev >= 64 || !configured[dev].load(std::memory_order_acquire)) {
         err = cudaFuncSetAttribute(route_logits_kernel<WT, WE, HT, MINB>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                    RT::SMEM);
         if (err != cudaSuccess) return err;
-        configured[dev].store(1, std::memory_order_release);
+        if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     const unsigned grid = static_cast<unsigned>(((E + RT::CE - 1) / RT::CE) * ((T + RT::CT - 1) / RT::CT));
     route_logits_kernel<WT, WE, HT, MINB><<<grid, 256, RT::SMEM, s>>>(xb, wg, bias, static_cast<int>(T), d, E, logits);

@@ -56,11 +56,12 @@ using namespace mk;
 extern "C" mk_status mk_moe_route_noalloc(const void* x, const float* wg, const float* bias, int64_t T, int d,
                                           int E, int k, int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
                                           void* stream) {
-    if (T < 0 || d <= 0 || E <= 0 || k <= 0 || E > kMaxExperts || k > kMaxTopK || k > E || d % 64 != 0)
-        return MK_ERR_INVALID_ARG;
-    if (T * k >= (int64_t(1) << 31) || T * static_cast<int64_t>(d) >= (int64_t(1) << 31) ||
-        static_cast<int64_t>(E) * d >= (int64_t(1) << 31))
-        return MK_ERR_UNSUPPORTED;
+    // The checks of mk_moe_route (sizes, then pointers, then alignment), plus
+    // the size of the static scratch array.
+    mk_status st = check_sizes(T, d, E, k, 64);
+    if (st != MK_OK) return st;
+    if (!x || !wg || !topk_ids || !topk_w) return MK_ERR_INVALID_ARG;
+    if (!aligned16(x) || !aligned16(wg)) return MK_ERR_INVALID_ARG;
     if (T * E > kNoAllocLogits) return MK_ERR_UNSUPPORTED;  // more logits than the static scratch holds
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T == 0) {
@@ -68,9 +69,6 @@ extern "C" mk_status mk_moe_route_noalloc(const void* x, const float* wg, const 
             return MK_ERR_CUDA;
         return MK_OK;
     }
-    if (!x || !wg || !topk_ids || !topk_w) return MK_ERR_INVALID_ARG;
-    if ((reinterpret_cast<uintptr_t>(x) & 15u) || (reinterpret_cast<uintptr_t>(wg) & 15u))
-        return MK_ERR_INVALID_ARG;
     if (!device_is_sm103()) return MK_ERR_UNSUPPORTED;
     float* logits = nullptr;
     if (scratch_for_current_device(&logits) != cudaSuccess) return MK_ERR_CUDA;

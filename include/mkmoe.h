@@ -152,7 +152,9 @@ MK_API mk_status mk_moe_route(const void* x, const float* wg, const float* bias,
  * the process exits; T * E above 2,097,152 returns MK_ERR_UNSUPPORTED.  The
  * first call on a device looks up that array's device address, so make the
  * first call on each device before any stream capture.  All calls share the
- * array: calls that overlap on the GPU race.  Allocates nothing. */
+ * array: calls that overlap on the GPU race.  Allocates nothing.  Its results
+ * equal mk_moe_route's bit for bit (the same fixed-order logits, top-k and
+ * softmax; it always computes every logit in the fixed order). */
 MK_API mk_status mk_moe_route_noalloc(const void* x, const float* wg, const float* bias,
                                       int64_t T, int d, int E, int k,
                                       int32_t* topk_ids, float* topk_w, int32_t* expert_counts,
@@ -293,6 +295,36 @@ MK_API mk_status mk_moe_route_approx_logits(const void* ws, int64_t T, int d, in
  * (synchronises `stream`).  Returns MK_ERR_WORKSPACE if ws is NULL. */
 MK_API mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int ffn, void* stream,
                                           uint32_t* count);
+
+/* Regions of a layer workspace (mk_moe_workspace_size(T, d, E, k, ffn) bytes)
+ * that mk_moe_layer leaves filled when its call has finished, for checks and
+ * diagnostics; both paths fill the same regions with the same bits.
+ *   MK_WS_IDS        int32 [T, k]    chosen experts, slot order
+ *   MK_WS_W          fp32  [T, k]    routing weights
+ *   MK_WS_OFFSETS    int32 [E + 1]   expert e owns rows [off[e], off[e+1])
+ *   MK_WS_ROW_TOKEN  int32 [T * k]   source token of each dispatched row
+ *   MK_WS_ROW_WEIGHT fp32  [T * k]   routing weight of each dispatched row
+ *   MK_WS_SLOT_ROW   int32 [T, k]    row that holds (token t, slot j)
+ *   MK_WS_X_PERM     bf16  [T * k, d]   dispatched token rows
+ *   MK_WS_H          bf16  [T * k, ffn] SwiGLU activations
+ *   MK_WS_P          bf16  [T * k, d]   weighted expert outputs (combined into y) */
+typedef enum {
+    MK_WS_IDS = 0,
+    MK_WS_W = 1,
+    MK_WS_OFFSETS = 2,
+    MK_WS_ROW_TOKEN = 3,
+    MK_WS_ROW_WEIGHT = 4,
+    MK_WS_SLOT_ROW = 5,
+    MK_WS_X_PERM = 6,
+    MK_WS_H = 7,
+    MK_WS_P = 8
+} mk_ws_region;
+
+/* Byte offset from the start of the workspace, and size in bytes, of `region`
+ * for these sizes.  Host-only arithmetic (no GPU call).  Returns
+ * MK_ERR_INVALID_ARG for invalid sizes, an unknown region or NULL outputs. */
+MK_API mk_status mk_moe_workspace_region(int64_t T, int d, int E, int k, int ffn, int region, size_t* offset,
+                                         size_t* bytes);
 
 /* Static, human-readable name of a status code. */
 MK_API const char* mk_moe_status_string(mk_status s);

@@ -155,3 +155,47 @@ def test_dispatch_gemm_entry_points_reject_bad_arguments(lib):
     assert Q(A, A, None, None, T, d, E, n, A, A, 4096, None) == mk.MK_ERR_INVALID_ARG
     assert Q(A, A, None, A, T, d, E, n, A, A, 16, None) == mk.MK_ERR_WORKSPACE
     assert Q(A, A, None, A, 0, d, E, n, A, A, 4096, None) == mk.MK_OK
+
+
+def test_workspace_regions(lib):
+    """Every region the layer leaves filled lies inside the workspace, starts
+    256-byte aligned, has the bytes of its documented shape, and no two
+    overlap."""
+    for T, d, E, k, f in [(32768, 7168, 256, 8, 2048), (300, 128, 256, 1, 64), (1, 64, 3, 3, 64)]:
+        total = mk.workspace_size(T, d, E, k, f)
+        spans = []
+        for name, (_, dtype, shape) in mk.WS_REGIONS.items():
+            off, nb = mk.mk_moe_workspace_region(T, d, E, k, f, name)
+            n = 1
+            for s in shape(T, d, E, k, f):
+                n *= s
+            esz = 2 if dtype.is_floating_point and dtype.itemsize == 2 else 4
+            assert nb == n * esz, name
+            assert off % 256 == 0 and off + nb <= total, name
+            spans.append((off, off + nb, name))
+        spans.sort()
+        for (a0, a1, na), (b0, b1, nb_) in zip(spans, spans[1:]):
+            assert a1 <= b0, (na, nb_)
+    off, nb = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    R = lib.mk_moe_workspace_region
+    assert R(64, 256, 8, 2, 512, 9, ctypes.byref(off), ctypes.byref(nb)) == mk.MK_ERR_INVALID_ARG
+    assert R(64, 100, 8, 2, 512, 0, ctypes.byref(off), ctypes.byref(nb)) == mk.MK_ERR_INVALID_ARG
+    assert R(64, 256, 8, 2, 512, 0, None, ctypes.byref(nb)) == mk.MK_ERR_INVALID_ARG
+
+
+def test_noalloc_router_rejects_bad_arguments(lib):
+    """The no-alloc router runs mk_moe_route's checks in the same order (sizes,
+    pointers, alignment) before its own limit on T * E, so both entry points
+    answer the same for the same arguments."""
+    A = _vp(0x10000)  # never dereferenced: every case fails validation first
+    N = lib.mk_moe_route_noalloc
+    T, d, E, k = 64, 256, 8, 2
+    assert N(A, A, None, T, 96, E, k, A, A, None, None) == mk.MK_ERR_INVALID_ARG
+    assert N(A, A, None, T, d, E, 9, A, A, None, None) == mk.MK_ERR_INVALID_ARG
+    assert N(A, A, None, -1, d, E, k, A, A, None, None) == mk.MK_ERR_INVALID_ARG
+    assert N(None, A, None, 0, d, E, k, A, A, None, None) == mk.MK_ERR_INVALID_ARG  # pointers before T == 0
+    assert N(A, A, None, T, d, E, k, None, A, None, None) == mk.MK_ERR_INVALID_ARG
+    assert N(_vp(0x10008), A, None, T, d, E, k, A, A, None, None) == mk.MK_ERR_INVALID_ARG
+    assert N(A, A, None, 8193, 64, 256, 2, A, A, None, None) == mk.MK_ERR_UNSUPPORTED  # T * E > 2^21
+    assert N(A, A, None, 1 << 28, 64, 8, 8, A, A, None, None) == mk.MK_ERR_UNSUPPORTED  # T * k >= 2^31
+    assert lib.mk_moe_route(None, A, None, 0, d, E, k, A, A, None, A, 1 << 20, None) == mk.MK_ERR_INVALID_ARG

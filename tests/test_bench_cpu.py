@@ -40,13 +40,14 @@ def test_flops_bytes_counts_only_touched_experts():
 def test_roofline_tensor_bound_with_hbm_beside():
     work = {"flops": 15.4e12, "bytes": 20.0e9}  # 770 FLOP/B, above the ridge (253 FLOP/B)
     r = bench.roofline(work, 9.0, PEAKS)
-    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1721.2
+    assert r["bound"] == "tensor" and r["unit"] == "TFLOP/s" and r["peak"] == 1939.5
     assert r["achieved"] == pytest.approx(15.4e12 / 9.0e-3 / 1e12)
-    assert r["frac"] == pytest.approx(r["achieved"] / 1721.2)
+    assert r["frac"] == pytest.approx(r["achieved"] / 1939.5)
+    assert r["sustained"]["frac"] == pytest.approx(r["achieved"] / 1721.2)
     assert r["other"]["bound"] == "hbm"
     assert r["other"]["achieved"] == pytest.approx(20.0e9 / 9.0e-3 / 1e9)
     assert r["other"]["frac"] == pytest.approx(r["other"]["achieved"] / 6793.1)
-    assert r["peak_source"].endswith("(bf16 sustained)")
+    assert r["peak_source"].endswith("(bf16 burst)")
 
 
 def test_roofline_hbm_bound_and_copy_kernels():
@@ -57,7 +58,7 @@ def test_roofline_hbm_bound_and_copy_kernels():
     assert c["bound"] == "hbm" and "other" not in c
 
 
-def test_roofline_falls_back_to_burst_peak():
+def test_roofline_without_a_sustained_figure():
     peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
     r = bench.roofline({"flops": 1e12, "bytes": 1e9}, 1.0, peaks)
-    assert r["bound"] == "tensor" and r["peak"] == 1900.0
+    assert r["bound"] == "tensor" and r["peak"] == 1900.0 and "sustained" not in r

@@ -151,14 +151,69 @@ def test_layer_bounded_wait_times_out_cleanly(name):
     check_output(y.cpu(), y_ref, "after timeout")
 
 
-@pytest.mark.parametrize("name,n_sample", [("skewed", 96), ("decode", 128), ("large", 64)])
+def _check_experts_every_row(wl, ws, name):
+    """Every row of a few experts of the layer just run, through the oracle's
+    per-expert FFN: P[r] = row_weight[r] * FFN_e(x[row_token[r]]).  The experts
+    are the one with the most rows, the one with the fewest, and the ones whose
+    last 256-row block is the shortest and the longest short of a full block,
+    so the CTA-pair GEMMs' swap tiles (an expert's partial last block) and the
+    tile tables at full size are covered.  Returns the experts checked."""
+    c = wl.cfg
+    view = lambda r: mk.workspace_view(ws, wl.T, c.d, c.E, c.k, c.f, r)
+    offsets = view("offsets").cpu().numpy().astype(np.int64)
+    row_token = view("row_token").cpu().numpy().astype(np.int64)
+    row_weight = view("row_weight").cpu().numpy().astype(np.float64)
+    counts = np.diff(offsets)
+    live = np.nonzero(counts)[0]
+    tail = counts % 256
+    has_tail = live[tail[live] > 0]
+    picks = [int(live[np.argmax(counts[live])]), int(live[np.argmin(counts[live])])]
+    if has_tail.size:
+        picks += [int(has_tail[np.argmin(tail[has_tail])]), int(has_tail[np.argmax(tail[has_tail])])]
+    picks = sorted(set(picks))
+    P = view("P")
+    for e in picks:
+        r0, r1 = int(offsets[e]), int(offsets[e + 1])
+        toks = row_token[r0:r1]
+        ref = oracle.expert_ffn(wl.bits("x"), wl.bits("w1"), wl.bits("w3"), wl.bits("w2"), toks,
+                                np.full(toks.size, e, dtype=np.int64))
+        ref = ref * row_weight[r0:r1, None]
+        check_output(P[r0:r1].cpu(), ref, f"{name} expert {e} ({r1 - r0} rows, tail {tail[e]})")
+    return picks, counts
+
+
+def chunk_spread_tokens(T, n, seed=0):
+    """The first, middle and last 128-token chunks whole, plus a seeded random
+    spread of the other tokens: n tokens in all (n >= 384)."""
+    chunks = [np.arange(0, 128), np.arange(T // 2 - 64, T // 2 + 64), np.arange(T - 128, T)]
+    fixed = np.unique(np.concatenate(chunks))
+    rest = np.setdiff1d(np.arange(T), fixed)
+    rs = np.random.RandomState(seed)
+    extra = rs.choice(rest, size=max(0, n - fixed.size), replace=False)
+    return np.sort(np.concatenate([fixed, extra])).astype(np.int64)
+
+
+@pytest.mark.parametrize("name,n_sample", [("skewed", 512), ("decode", 128), ("large", 1024)])
 def test_layer_full_size(name, n_sample):
-    """Full-size workload in the benchmark's launch configuration."""
+    """Full-size workload in the benchmark's launch configuration: routing and
+    dispatch tables of every token bit-exact, the dispatched rows bitwise
+    copies of their tokens, every row of a few experts through the oracle's
+    expert FFN, and the output on a token sample that covers the first,
+    middle and last chunks."""
     wl = Workload(name)
+    c = wl.cfg
     y, ws = _run_layer(wl)
     _, ids_ref, w_ref = wl.oracle_routing()
     _check_routing(wl, ws, ids_ref, w_ref)
-    toks = sample_tokens(wl.T, n_sample)
+    _, _, row_token_ref, _ = oracle.dispatch(ids_ref, c.E)
+    row_token = mk.workspace_view(ws, wl.T, c.d, c.E, c.k, c.f, "row_token")
+    np.testing.assert_array_equal(row_token.cpu().numpy(), row_token_ref)
+    xp = mk.workspace_view(ws, wl.T, c.d, c.E, c.k, c.f, "x_perm").view(torch.int16)
+    rt = torch.from_numpy(row_token_ref.astype(np.int64)).to(wl.dev)
+    for r0 in range(0, rt.numel(), 1 << 16):
+        assert torch.equal(xp[r0:r0 + (1 << 16)], wl.g["x"].view(torch.int16).index_select(0, rt[r0:r0 + (1 << 16)]))
+    _check_experts_every_row(wl, ws, name)
+    toks = chunk_spread_tokens(wl.T, n_sample) if wl.T > 384 else np.arange(wl.T, dtype=np.int64)
     y_ref, _, _ = wl.oracle_layer(tokens=toks)
     check_output(y.cpu()[torch.from_numpy(toks)], y_ref, name)
     # the persistent-kernel path on the same workspace: the same bits
@@ -166,6 +221,6 @@ def test_layer_full_size(name, n_sample):
                           path=mk.MK_PATH_FUSED)
     assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
     assert torch.equal(y_f.view(torch.int16), y.view(torch.int16))
-    del wl, y, y_f, ws
+    del wl, y, y_f, ws, xp, rt
     gc.collect()
     torch.cuda.empty_cache()

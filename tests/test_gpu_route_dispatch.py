@@ -114,7 +114,7 @@ def test_route_fixed_order_decides_weights():
 
 
 @pytest.mark.parametrize("name", ["tiny", "ragged", "ragged_skew", "single", "edge_min", "many_experts", "mid", "skewed",
-                                  "decode"])
+                                  "decode", "large"])
 def test_dispatch_bit_exact(name):
     """GPU dispatch of the oracle's routing equals the oracle's dispatch."""
     wl = Workload(name, experts=False)
@@ -206,3 +206,59 @@ def test_approx_logit_error_within_model(name):
     ratio = np.abs(A[toks] - exact) / (nx[:, None] * nw[None, :])
     assert ratio.max() <= 2.0 ** -19, f"{name}: approximate logit error 2^{np.log2(ratio.max()):.2f} ||x|| ||w||"
     assert mk.mk_moe_route_fallbacks(ws) == 0
+
+
+def test_tensor_core_step_error_within_eta():
+    """The router's candidate filter assumes that one tcgen05 MMA step (16 bf16
+    products added to the fp32 accumulator) errs by at most
+    eta * (|acc| + sum |products|), eta = 2^-18.  This test measures that on
+    inputs built to make the step error as large as the accumulator allows:
+    d = 64, so the approximate logit is one accumulation of four steps over the
+    gate rows' high parts (then four steps of exactly zero products, the gate
+    rows being bf16 values), with no bias and one chunk, so the logit the
+    library returns is the accumulator itself.  Column 0 holds a large product
+    2^(a_t + b_e) (a_t in [0, 20], b_e in [-8, 23]); the other 63 columns hold
+    products of mixed sign with exponents spread over [-8, 10), so across the
+    (token, expert) pairs the small products fall above, across and below the
+    accumulator's last bit.  Every product is exact in fp64 and the exact sum
+    comes from math.fsum, so |A - exact| is the hardware's accumulation error;
+    it must stay under eta times sum over the four steps of (|exact partial sum
+    before the step| + sum |products of the step|)."""
+    import math
+
+    T, d, E, k = 2048, 64, 64, 2
+    rs = np.random.RandomState(21)
+    mx = rs.randint(0, 128, size=(T, d))
+    ex = rs.randint(-4, 5, size=(T, d))
+    sx = rs.choice([-1.0, 1.0], size=(T, d))
+    x = sx * (1.0 + mx / 128.0) * np.exp2(ex)
+    x[:, 0] = np.exp2(rs.randint(0, 21, size=T))
+    mw = rs.randint(0, 128, size=(E, d))
+    ew = rs.randint(-4, 5, size=(E, d))
+    sw = rs.choice([-1.0, 1.0], size=(E, d))
+    w = sw * (1.0 + mw / 128.0) * np.exp2(ew)
+    w[:, 0] = np.exp2((np.arange(E) % 32) - 8)
+    xb = torch.from_numpy(x.astype(np.float32)).to(torch.bfloat16)
+    assert torch.equal(xb.float(), torch.from_numpy(x.astype(np.float32)))  # every value exact in bf16
+    wg = torch.from_numpy(w.astype(np.float32))
+    assert torch.equal(wg.to(torch.bfloat16).float(), wg)  # the gate rows' low parts are zero
+    dev = torch.device("cuda:0")
+    ws = mk.alloc_workspace(T, d, E, k, 64, dev)
+    mk.mk_moe_route(xb.to(dev), wg.to(dev), None, k, ws=ws)
+    A = mk.mk_moe_route_approx_logits(ws, T, d, E, k).cpu().numpy().astype(np.float64)
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+
+    prods = x[:, None, :] * w[None, :, :]  # [T, E, d], exact in fp64 (8-bit x 8-bit significands)
+    exact = np.array([[math.fsum(prods[t, e]) for e in range(E)] for t in range(T)])
+    steps = prods.reshape(T, E, 4, 16)
+    step_abs = np.abs(steps).sum(axis=3)
+    before = np.zeros((T, E, 4))
+    for s in range(1, 4):
+        before[:, :, s] = np.array([[math.fsum(steps[t, e, :s].ravel()) for e in range(E)] for t in range(T)])
+    M = (np.abs(before) + step_abs).sum(axis=2)
+    ratio = np.abs(A - exact) / M
+    eta = 2.0 ** -18
+    worst = float(ratio.max())
+    assert worst <= eta, f"tensor-core accumulation error 2^{math.log2(worst):.2f} of its magnitudes > 2^-18"
+    # the construction does reach the accumulator's last bit: some pairs lose low-order product bits
+    assert np.count_nonzero(ratio) > T * E // 100
