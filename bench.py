@@ -165,7 +165,7 @@ def launches_per_step(cfg, path) -> int:
     filt = (cfg.T >= 2048 and cfg.T * cfg.d * cfg.E >= 2 ** 32 and 2 * cfg.d + 8 * cfg.E <= 160 * 1024)
     if path == mk.MK_PATH_FUSED:
         return 1 + (5 if filt else 0)
-    return (3 if filt else 2) + 6
+    return (3 if filt else 2) + 6  # the tile-synchronised path launches the same kernels
 
 
 def flops_bytes(cfg, offsets):
@@ -341,20 +341,24 @@ def time_layer(mk, cfg, inp, ws, y, stream, path, mover_ctas, steps, warmup, scr
     if st != mk.MK_OK:
         raise RuntimeError(f"device error in the timed region: {mk.status_string(st)} site {site:#x}")
     phase_ms = {}
-    if path == mk.MK_PATH_FUSED:  # event 0 before the kernels, the others after them
-        phase_ms["fused_layer"] = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)) / steps
+    if path in (mk.MK_PATH_FUSED, mk.MK_PATH_TILES):  # event 0 before the kernels, the others after them
+        phase_ms[PATH_KEYS[path]] = sum(ev[i][0].elapsed_time(ev[i][1]) for i in range(steps)) / steps
     else:
         for p, name in enumerate(mk.PHASES):
             phase_ms[name] = sum(ev[i][p].elapsed_time(ev[i][p + 1]) for i in range(steps)) / steps
     return total_ms, phase_ms
 
 
-def dominant_roofline(fb, phase_ms, path, peaks, fused_key="fused_layer"):
+PATH_KEYS = {1: "fused_layer", 2: "tiles_layer"}
+PATH_NAMES = {0: "one kernel per step", 1: "fused persistent kernel",
+              2: "kernel per step, tile semaphores and programmatic dependent launch"}
+
+
+def dominant_roofline(fb, phase_ms, path, peaks):
     """The roofline object of the step that takes the most time (the whole
-    persistent kernel on the fused path)."""
-    import dispatch_ffn_combine_gb300 as mk
-    if path == mk.MK_PATH_FUSED:
-        dom, work = fused_key, fb["layer"]
+    layer on the paths whose steps overlap)."""
+    if path in PATH_KEYS:
+        dom, work = PATH_KEYS[path], fb["layer"]
     else:
         dom = max(("gemm1", "gemm2", "combine", "scatter", "route_logits"), key=lambda n: phase_ms[n])
         work = fb[dom]
@@ -382,7 +386,8 @@ def other_configs(mk, names, dev, stream, steps, warmup, peaks):
         scrub = torch.empty(256 * 1024 * 1024, dtype=torch.uint8, device=dev) if needs_flush(inp) else None
         res = {"workload": cfg.describe(), "l2": "flushed between steps" if scrub is not None else
                "inputs larger than L2 (no flush)", "steps": steps}
-        for path, key in ((mk.MK_PATH_STEPS, "steps_path"), (mk.MK_PATH_FUSED, "fused_path")):
+        for path, key in ((mk.MK_PATH_STEPS, "steps_path"), (mk.MK_PATH_FUSED, "fused_path"),
+                          (mk.MK_PATH_TILES, "tiles_path")):
             total, phase = time_layer(mk, cfg, inp, ws, y, stream, path, 0, steps, warmup, scrub=scrub)
             ms = total / steps
             _, _, offsets, _ = mk.mk_moe_layer_routing(ws, cfg.T, cfg.d, cfg.E, cfg.k, cfg.f)
@@ -455,11 +460,14 @@ def run_ours(args):
         tdist.barrier()
     e2e_value = world * cfg.T / (te / args.steps / 1e3)
 
-    # ---- the other layer path on the same inputs (device buffers), for comparison
-    other = mk.MK_PATH_FUSED if args.path == mk.MK_PATH_STEPS else mk.MK_PATH_STEPS
-    other_total, other_phase = time_layer(mk, cfg, inp, ws, y, stream, other, 0, args.steps, args.warmup,
-                                          scrub=scrub)
-    other_ms = max_over_ranks(other_total, dev, dist) / args.steps
+    # ---- the other layer paths on the same inputs (device buffers), for comparison
+    others = {}
+    for other in (mk.MK_PATH_STEPS, mk.MK_PATH_FUSED, mk.MK_PATH_TILES):
+        if other == args.path:
+            continue
+        other_total, other_phase = time_layer(mk, cfg, inp, ws, y, stream, other, 0, args.steps, args.warmup,
+                                              scrub=scrub)
+        others[other] = (max_over_ranks(other_total, dev, dist) / args.steps, other_phase)
 
     if rank != 0:
         if dist:
@@ -471,7 +479,6 @@ def run_ours(args):
     fb = flops_bytes(cfg, offsets.cpu().numpy())
     roof = dominant_roofline(fb, phase_ms, args.path, peaks)
     roof["traffic"] = traffic_record(roof["kernel"], args.config)
-    other_roof = dominant_roofline(fb, other_phase, other, peaks)
 
     # ---- CPU baseline (oracle) on a bounded sample, rank 0 at N=1 only
     cpu = None
@@ -492,7 +499,6 @@ def run_ours(args):
         configs = other_configs(mk, names, dev, stream, args.config_steps, args.warmup, peaks)
 
     layer_tflops = fb["layer"]["flops"] / (ms_per_step / 1e3) / 1e12 * world
-    path_name = lambda p: "fused persistent kernel" if p == mk.MK_PATH_FUSED else "one kernel per step"
     line = {
         "metric": "MoE layer tokens/s (TFLOP/s beside it)", "value": value, "unit": "tokens/s",
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup, "ms_per_step": ms_per_step,
@@ -509,11 +515,12 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2},
         "gpu_launches": launches_per_step(cfg, args.path) * args.steps,
-        "path": path_name(args.path),
+        "path": PATH_NAMES[args.path],
         "mover_ctas": args.mover_ctas,
-        "other_path": {"path": path_name(other), "ms_per_step": other_ms, "value": world * cfg.T / (other_ms / 1e3),
-                       "unit": "tokens/s", "roofline": other_roof,
-                       "note": "same inputs and timing rules, measured after the main run; not the headline"},
+        "other_paths": [{"path": PATH_NAMES[o], "ms_per_step": ms, "value": world * cfg.T / (ms / 1e3),
+                         "unit": "tokens/s", "roofline": dominant_roofline(fb, ph, o, peaks)}
+                        for o, (ms, ph) in others.items()],
+        "other_paths_note": "same inputs and timing rules, measured after the main run; not the headline",
         "configs": configs,
         "clocks": clk,
         "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},
@@ -534,7 +541,9 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-configs", action="store_true", help="skip the other workloads' entries")
     ap.add_argument("--config-steps", type=int, default=20, help="timed steps per path for each other workload")
-    ap.add_argument("--path", type=int, default=0, help="0: one kernel per step (default), 1: one persistent kernel")
+    ap.add_argument("--path", type=int, default=0, choices=[0, 1, 2],
+                    help="0: one kernel per step (default), 1: one persistent kernel, "
+                         "2: kernel per step with tile semaphores and programmatic dependent launch")
     ap.add_argument("--mover-ctas", type=int, default=0,
                     help="fused path: 0 adaptive SM split, n > 0 fixed split with n mover blocks, -1 none")
     args = ap.parse_args()

@@ -58,8 +58,10 @@ class MkMoeOpts(ctypes.Structure):
 
 MK_INJECT_STALL_GEMM1 = 1
 MK_INJECT_ROUTE_ZERO_BOUND = 2
+MK_INJECT_DROP_TILE_SIGNAL = 3
 MK_PATH_STEPS = 0
 MK_PATH_FUSED = 1
+MK_PATH_TILES = 2
 
 
 def load_library():
@@ -341,8 +343,10 @@ def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None,
                  inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None):
     """The whole layer on device tensors; returns y [T, d] bf16.
 
-    path: MK_PATH_STEPS (one kernel per step, default) or MK_PATH_FUSED
-    (one persistent kernel).  mover_ctas: fused-path SM split, 0 = adaptive."""
+    path: MK_PATH_STEPS (one kernel per step, default), MK_PATH_FUSED (one
+    persistent kernel) or MK_PATH_TILES (one kernel per step, launched as
+    programmatic dependents and synchronised per tile by data-tile
+    semaphores).  mover_ctas: fused-path SM split, 0 = adaptive."""
     T, d, E, f = _layer_shapes(x, wg, bias, w1, w3, w2)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device) if y is None else y
     ws = alloc_workspace(T, d, E, k, f, x.device) if ws is None else ws

@@ -49,6 +49,7 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int f, bool full) {
     L.h = take(S * f * 2);
     L.P = take(S * d * 2);
     L.sync = take(fused_sync_bytes(T, E, k));
+    L.tile_sems = take(tile_sems_bytes(static_cast<int64_t>(S), E));
     L.x_stage = take(static_cast<size_t>(T) * d * 2);
     L.y_stage = take(static_cast<size_t>(T) * d * 2);
     L.total = o;
@@ -57,6 +58,18 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int f, bool full) {
 }  // namespace
 
 WsLayout ws_layout(int64_t T, int d, int E, int k, int f) { return make_layout(T, d, E, k, f, true); }
+
+TileSems tile_sems_at(void* base, int64_t S, int E, bool pdl) {
+    const int64_t n = tile_sem_units(S, E);
+    uint32_t* w = static_cast<uint32_t*>(base);
+    TileSems t;
+    t.mt_rows = w;
+    t.h_ready = w + n;
+    t.p_ready = w + 2 * n;
+    t.tok_done = w + 3 * n;
+    t.pdl = pdl;
+    return t;
+}
 
 WsLayout ws_layout_dispatch(int64_t T, int d, int E, int k) { return make_layout(T, d, E, k, 64, false); }
 
@@ -456,6 +469,67 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
         for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
         return MK_OK;
     }
+    if (opts && opts->path == MK_PATH_TILES) {
+        // Kernel per step, each launched as a programmatic dependent of the one
+        // before (it may start before that one has finished).  The routing
+        // kernels wait for their predecessor to finish before reading; the
+        // scatter, both GEMMs and the combine synchronise per 128-row M-tile
+        // through the data-tile semaphores instead (rows landed -> gemm1;
+        // every gemm1 N block of the tile stored -> gemm2; every gemm2 N block
+        // -> the combine of the tile's tokens), so a step starts on the tiles
+        // whose inputs are ready while the step before finishes the others.
+        const int64_t S = T * k;
+        const TileSems sem = tile_sems_at(at<uint8_t>(ws, L.tile_sems), S, E, true);
+        MK_TRY(cudaMemsetAsync(at<uint8_t>(ws, L.tile_sems), 0, tile_sems_bytes(S, E), s));
+        const bf16* xb = static_cast<const bf16*>(x);
+        const uint64_t timeout_ns = (opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
+        MK_TRY(pm.mark(0));
+        if (use_route_filter(T, d, E)) {
+            MK_TRY(launch_route_approx(xb, wg, bias, T, d, E, logits, at<bf16>(ws, L.wsplit), at<float>(ws, L.wnorm),
+                                       status, timeout_ns, s, true));
+            MK_TRY(launch_route_select(xb, wg, bias, T, d, E, k, logits, at<float>(ws, L.wnorm), ids, w, nullptr,
+                                       status + 2, false, s, true));
+        } else {
+            MK_TRY(launch_route_logits(xb, wg, bias, T, d, E, logits, s, false));
+            MK_TRY(launch_topk(logits, T, E, k, ids, w, nullptr, s, true));
+        }
+        MK_TRY(launch_count(ids, T, E, k, chunk_counts, rank, status, s, true));
+        MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), offsets, mtile,
+                           status + 3, s, true));
+        TileSems scatter_sem = sem;
+        scatter_sem.drop_token0 = opts->inject == MK_INJECT_DROP_TILE_SIGNAL;
+        MK_TRY(launch_scatter(xb, ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm, at<int32_t>(ws, L.row_token),
+                              row_weight, slot_row, s, &scatter_sem, mtile));
+        if (hk.after_scatter != nullptr) MK_TRY(cudaEventRecord(hk.after_scatter, s));
+        FfnArgs a;
+        a.x_perm = x_perm;
+        a.offsets = offsets;
+        a.mtile_start = mtile;
+        a.row_weight = row_weight;
+        a.w1 = static_cast<const bf16*>(w1);
+        a.w3 = static_cast<const bf16*>(w3);
+        a.w2 = static_cast<const bf16*>(w2);
+        a.S = S;
+        a.d = d;
+        a.E = E;
+        a.f = ffn;
+        a.h = at<bf16>(ws, L.h);
+        a.P = at<bf16>(ws, L.P);
+        a.status = status;
+        a.timeout_ns = timeout_ns;
+        a.inject = 0;
+        a.tickets = status + 4;
+        a.sem = sem;
+        MK_TRY(launch_gemm1_auto(a, s));
+        MK_TRY(launch_gemm2_auto(a, s));
+        if (!hk.skip_combine) {
+            const bool pairs = use_pairs(a);
+            MK_TRY(launch_combine_sem(a.P, slot_row, offsets, mtile, T, d, E, k, static_cast<bf16*>(y), sem, pairs,
+                                      (d + 255) / 256, pair_swap_max_rows(2, ffn / 64), status, timeout_ns, s));
+        }
+        for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
+        return MK_OK;
+    }
     const DispatchOut dout{offsets, at<int32_t>(ws, L.row_token), row_weight, slot_row, x_perm};
     mk_status st = route_dispatch_steps(static_cast<const bf16*>(x), wg, bias, T, d, E, k, ws, L, dout, opts, pm, s);
     if (st != MK_OK) return st;
@@ -499,9 +573,15 @@ mk_status validate_layer(const void* x, const float* wg, const void* w1, const v
     if (device_xy && (!aligned16(x) || !aligned16(y))) return MK_ERR_INVALID_ARG;
     if (opts != nullptr) {
         if (opts->trace_cap < 0 || (opts->trace_cap > 0 && opts->trace == nullptr)) return MK_ERR_INVALID_ARG;
-        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1 && opts->inject != MK_INJECT_ROUTE_ZERO_BOUND)
+        if (opts->inject != 0 && opts->inject != MK_INJECT_STALL_GEMM1 && opts->inject != MK_INJECT_ROUTE_ZERO_BOUND &&
+            opts->inject != MK_INJECT_DROP_TILE_SIGNAL)
             return MK_ERR_INVALID_ARG;
-        if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS) return MK_ERR_INVALID_ARG;
+        if (opts->path != MK_PATH_FUSED && opts->path != MK_PATH_STEPS && opts->path != MK_PATH_TILES)
+            return MK_ERR_INVALID_ARG;
+        // the tile-synchronised path takes only its own hook, and that hook only that path
+        if (opts->inject == MK_INJECT_DROP_TILE_SIGNAL && opts->path != MK_PATH_TILES) return MK_ERR_INVALID_ARG;
+        if (opts->path == MK_PATH_TILES && opts->inject != 0 && opts->inject != MK_INJECT_DROP_TILE_SIGNAL)
+            return MK_ERR_INVALID_ARG;
         if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
     }
     if ((st = check_ws(ws, ws_bytes, ws_layout(T, d, E, k, ffn))) != MK_OK) return st;

@@ -24,6 +24,8 @@ __global__ void __launch_bounds__(256) count_kernel(const int32_t* __restrict__ 
                                                     int32_t* __restrict__ chunk_counts, int32_t* __restrict__ rank,
                                                     uint32_t* status) {
     __shared__ uint32_t mask[kMaxExperts][kChunkTokens / 32];
+    pdl_wait();  // as a programmatic dependent: the routing is complete
+    pdl_launch_dependents();
     const int64_t c = blockIdx.x;
     const int64_t t_begin = c * kChunkTokens;
     const int nt = static_cast<int>((T - t_begin < kChunkTokens) ? (T - t_begin) : kChunkTokens);
@@ -114,6 +116,8 @@ __global__ void __launch_bounds__(1024) scan_kernel(const int32_t* __restrict__ 
     __shared__ int32_t s_part[32][33];
     __shared__ int32_t s_counts[kMaxExperts];
     __shared__ int s_last;
+    pdl_wait();  // as a programmatic dependent: the chunk counts are complete
+    pdl_launch_dependents();
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int e = blockIdx.x * 32 + lane;
@@ -196,25 +200,37 @@ __global__ void __launch_bounds__(32) mtile_table_kernel(const int32_t* __restri
 }
 
 // One block per token: read the row once, write it to its k destination rows.
+// With mt_rows (the tile-synchronised path) each written row is published on
+// its M-tile's counter and the token on tok_done, with release semantics after
+// a proxy fence by every writing thread (the rows are read next by TMA).
 __global__ void __launch_bounds__(128) scatter_kernel(const bf16* __restrict__ x, const int32_t* __restrict__ ids,
                                                       const float* __restrict__ w, int64_t T, int d, int E, int k,
                                                       const int32_t* __restrict__ offsets,
                                                       const int32_t* __restrict__ chunk_base,
                                                       const int32_t* __restrict__ rank, bf16* __restrict__ x_perm,
                                                       int32_t* __restrict__ row_token, float* __restrict__ row_weight,
-                                                      int32_t* __restrict__ slot_row) {
+                                                      int32_t* __restrict__ slot_row, uint32_t* mt_rows,
+                                                      uint32_t* tok_done, const int32_t* __restrict__ mtile_start,
+                                                      int drop_token0) {
     __shared__ int64_t rows[kMaxTopK];
+    __shared__ int32_t tiles[kMaxTopK];
+    pdl_wait();  // as a programmatic dependent: offsets, chunk bases and ranks are complete
+    pdl_launch_dependents();
     const int64_t t = blockIdx.x;
     const int64_t S = T * k;
     if (threadIdx.x < k) {
         const int j = threadIdx.x;
         const int e = ids[t * k + j];
         int64_t r = -1;
+        int32_t g = -1;
         if (e >= 0 && e < E) {
-            r = static_cast<int64_t>(offsets[e]) + chunk_base[(t / kChunkTokens) * E + e] + rank[t * k + j];
+            const int64_t in_e = static_cast<int64_t>(chunk_base[(t / kChunkTokens) * E + e]) + rank[t * k + j];
+            r = static_cast<int64_t>(offsets[e]) + in_e;
             if (r < 0 || r >= S) r = -1;
+            if (r >= 0 && mt_rows != nullptr) g = mtile_start[e] + static_cast<int32_t>(in_e / kTileM);
         }
         rows[j] = r;
+        tiles[j] = g;
         slot_row[t * k + j] = static_cast<int32_t>(r);
         if (r >= 0) {
             row_token[r] = static_cast<int32_t>(t);
@@ -231,20 +247,34 @@ __global__ void __launch_bounds__(128) scatter_kernel(const bf16* __restrict__ x
             if (r >= 0) reinterpret_cast<uint4*>(x_perm + r * d)[c] = v;
         }
     }
+    if (mt_rows != nullptr) {
+        // every writer's proxy fence (the rows are read next through TMA); the
+        // block barrier orders all threads' stores before the release increments,
+        // which are cumulative over them
+        fence_proxy_async_global();
+        __syncthreads();
+        const bool drop = drop_token0 != 0 && t == 0;  // test hook: these rows never count as landed
+        if (threadIdx.x < k && tiles[threadIdx.x] >= 0 && !drop) red_release_gpu_add(mt_rows + tiles[threadIdx.x], 1u);
+        if (threadIdx.x == 0) red_release_gpu_add(tok_done, 1u);
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_count(const int32_t* ids, int64_t T, int E, int k, int32_t* chunk_counts, int32_t* rank,
-                         uint32_t* status, cudaStream_t s) {
-    count_kernel<<<static_cast<unsigned>(num_chunks(T)), 256, 0, s>>>(ids, T, E, k, chunk_counts, rank, status);
+                         uint32_t* status, cudaStream_t s, bool pdl) {
+    LaunchCfg lc(dim3(static_cast<unsigned>(num_chunks(T))), dim3(256), 0, s, pdl);
+    const cudaError_t err = cudaLaunchKernelEx(&lc.cfg, count_kernel, ids, T, E, k, chunk_counts, rank, status);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
 cudaError_t launch_scan(const int32_t* chunk_counts, int64_t nchunks, int E, int32_t* chunk_base, int32_t* counts,
-                        int32_t* offsets, int32_t* mtile_start, uint32_t* done, cudaStream_t s) {
-    scan_kernel<<<(E + 31) / 32, 1024, 0, s>>>(chunk_counts, nchunks, E, chunk_base, counts, offsets, mtile_start,
-                                                 done);
+                        int32_t* offsets, int32_t* mtile_start, uint32_t* done, cudaStream_t s, bool pdl) {
+    LaunchCfg lc(dim3((E + 31) / 32), dim3(1024), 0, s, pdl);
+    const cudaError_t err = cudaLaunchKernelEx(&lc.cfg, scan_kernel, chunk_counts, nchunks, E, chunk_base, counts,
+                                               offsets, mtile_start, done);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
@@ -256,9 +286,15 @@ cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t
 
 cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, int64_t T, int d, int E, int k,
                            const int32_t* offsets, const int32_t* chunk_base, const int32_t* rank, bf16* x_perm,
-                           int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s) {
-    scatter_kernel<<<static_cast<unsigned>(T), 128, 0, s>>>(x, ids, w, T, d, E, k, offsets, chunk_base, rank, x_perm,
-                                                             row_token, row_weight, slot_row);
+                           int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s,
+                           const TileSems* sem, const int32_t* mtile_start) {
+    uint32_t* mt_rows = sem != nullptr ? sem->mt_rows : nullptr;
+    uint32_t* tok_done = sem != nullptr ? sem->tok_done : nullptr;
+    LaunchCfg lc(dim3(static_cast<unsigned>(T)), dim3(128), 0, s, sem != nullptr && sem->pdl);
+    const cudaError_t err = cudaLaunchKernelEx(&lc.cfg, scatter_kernel, x, ids, w, T, d, E, k, offsets, chunk_base,
+                                               rank, x_perm, row_token, row_weight, slot_row, mt_rows, tok_done,
+                                               mtile_start, (sem != nullptr && sem->drop_token0) ? 1 : 0);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

@@ -165,10 +165,6 @@ __device__ __forceinline__ unsigned long long ld_relaxed64(const unsigned long l
     return v;
 }
 
-__device__ __forceinline__ void fence_proxy_async_global() {
-    asm volatile("fence.proxy.async.global;" ::: "memory");
-}
-
 __device__ __forceinline__ void nanosleep_ns(uint32_t ns) { asm volatile("nanosleep.u32 %0;" ::"r"(ns)); }
 
 // GEMM tile `local` of one GEMM (nt N blocks per M-tile) -> its M-tile g, its

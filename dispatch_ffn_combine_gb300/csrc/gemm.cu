@@ -75,6 +75,13 @@ struct GemmParams {
     uint64_t timeout_ns;
     int stall_first_stage;  // test hook: the CTA that claims tile 0 never loads its first stage
     uint32_t* ticket;       // a zeroed word: tiles claimed so far
+    // Tile-synchronised path (all null / 0 otherwise): per-M-tile semaphores.
+    const uint32_t* wait_rows;    // gemm1: rows the dispatch has landed per M-tile
+    const uint32_t* wait_h;       // gemm2: gemm1 epilogue completions per M-tile (4 per N block)
+    int wait_ntiles;              // gemm2: gemm1's N blocks
+    const uint32_t* weight_rows;  // gemm2: the dispatch's row counters, acquired before row weights
+    uint32_t* post;               // this GEMM's epilogue completions per M-tile
+    int pdl;                      // 1: let the next kernel launch after the prologue; 2: once the tiles run out
 };
 
 struct TileInfo {
@@ -161,6 +168,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
+    if (p.pdl == 1) pdl_launch_dependents();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile uint32_t* abort_word = &ctl->abort_flag;
     const volatile uint32_t* never = &ctl->zero;
@@ -201,6 +209,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (tile < 0) break;
                 if (leader) tk = atomicAdd(p.ticket, 1u);
+                if (p.wait_rows != nullptr || p.wait_h != nullptr) {
+                    // tile-synchronised path: the M-tile's rows have landed (gemm1) or every gemm1
+                    // tile of the M-tile has stored its h rows (gemm2)
+                    uint32_t ready = 1u;
+                    if (leader) {
+                        const int g = sem_tile0(p.offsets, p.mtile_start, ti.e, ti.row0);
+                        ready = p.wait_rows != nullptr
+                                    ? wait_count_bounded(p.wait_rows + g, static_cast<uint32_t>(ti.rows), abort_word,
+                                                         p.timeout_ns)
+                                    : wait_count_bounded(p.wait_h + g, static_cast<uint32_t>(4 * p.wait_ntiles),
+                                                         abort_word, p.timeout_ns);
+                        fence_proxy_async_global();  // the rows are read next through TMA
+                    }
+                    if (!__shfl_sync(0xffffffffu, ready ? 1u : 0u, lead)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u,
@@ -234,6 +260,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
             }
+            if (p.pdl == 2) pdl_launch_dependents();  // no tile left to claim: the next kernel may launch
             if (leader) {
                 if (!ok) {
                     *abort_word = 1u;
@@ -343,6 +370,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * MMA_N;
+            if (p.weight_rows != nullptr) {
+                // the row weights were written by the dispatch with the rows: acquire the M-tile's counter
+                if (lane == 0 && !wait_count_bounded(p.weight_rows + sem_tile0(p.offsets, p.mtile_start, info.x, info.y),
+                                                     static_cast<uint32_t>(info.z), abort_word, p.timeout_ns))
+                    ok = false;
+                __syncwarp();
+                if (!__shfl_sync(0xffffffffu, ok ? 1u : 0u, 0)) break;
+            }
             const bool row_ok = row_in_tile < info.z;
             const int64_t r = static_cast<int64_t>(info.y) + row_in_tile;
             bf16* orow = p.out + (row_ok ? r : 0) * p.out_ld;
@@ -355,6 +390,14 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->tmem_empty[acc]));
+            if (p.post != nullptr) {
+                // publish this warp's rows of the M-tile: every lane's proxy fence (gemm2 reads h
+                // through TMA), the warp barrier, one release increment (cumulative over the
+                // lanes' stores)
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) red_release_gpu_add(p.post + sem_tile0(p.offsets, p.mtile_start, info.x, info.y), 1u);
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -389,7 +432,9 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUten
     // Upper bound on the tile count: every expert adds at most one partial block.
     const int64_t max_tiles = ((S + BM - 1) / BM + p.E) * static_cast<int64_t>(p.n_tiles);
     const int grid = static_cast<int>(std::min<int64_t>(device_sm_count(), std::max<int64_t>(max_tiles, 1)));
-    grouped_gemm_kernel<MODE><<<grid, NUM_THREADS, SMEM_BYTES, s>>>(a, b0, b1, p);
+    LaunchCfg lc(dim3(grid), dim3(NUM_THREADS), SMEM_BYTES, s, p.pdl != 0);
+    err = cudaLaunchKernelEx(&lc.cfg, grouped_gemm_kernel<MODE>, a, b0, b1, p);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
@@ -417,6 +462,12 @@ cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s) {
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
     p.ticket = a.tickets;
+    p.wait_rows = a.sem.mt_rows;
+    p.wait_h = nullptr;
+    p.wait_ntiles = 0;
+    p.weight_rows = nullptr;
+    p.post = a.sem.h_ready;
+    p.pdl = a.sem.pdl ? 1 : 0;
     return launch_mode<0>(ma, mb0, mb1, p, a.S, s);
 }
 
@@ -440,6 +491,12 @@ cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s) {
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = 0;
     p.ticket = a.tickets + 1;
+    p.wait_rows = nullptr;
+    p.wait_h = a.sem.h_ready;
+    p.wait_ntiles = (a.f + MMA_N / 2 - 1) / (MMA_N / 2);
+    p.weight_rows = a.sem.mt_rows;
+    p.post = a.sem.p_ready;
+    p.pdl = a.sem.pdl ? 2 : 0;
     return launch_mode<1>(ma, mb0, mb0, p, a.S, s);
 }
 

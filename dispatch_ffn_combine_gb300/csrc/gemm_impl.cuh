@@ -93,6 +93,13 @@ __device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, b
     epilogue_weighted_w<MMA_N>(tbase, row_ok, orow, n0, n_valid, wr);
 }
 
+// Tile-synchronised path: index of the first 128-row M-tile of a block of
+// expert e's rows that starts at row0 (a multiple of 128 rows into the
+// expert), in the tile table's numbering.
+__device__ __forceinline__ int sem_tile0(const int32_t* offsets, const int32_t* mtile_start, int e, int row0) {
+    return __ldg(mtile_start + e) + (row0 - __ldg(offsets + e)) / BM;
+}
+
 // ------------------------------------------------------------------ host side
 
 inline PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {

@@ -111,6 +111,14 @@ struct PairParams {
     uint64_t timeout_ns;
     int stall_first_stage;  // test hook: CTA 0 of the pair that claims tile 0 never loads its first stage
     uint32_t* ticket;       // a zeroed word: tiles claimed so far
+    // Tile-synchronised path (all null / 0 otherwise): per-M-tile semaphores.
+    const uint32_t* wait_rows;    // gemm1: rows the dispatch has landed per M-tile
+    const uint32_t* wait_h;       // gemm2: gemm1 epilogue completions per M-tile
+    int wait_ntiles;              // gemm2: gemm1's N blocks per pair block
+    int wait_swap_max;            // gemm2: gemm1's swap-tile threshold
+    const uint32_t* weight_rows;  // gemm2: the dispatch's row counters, acquired before row weights
+    uint32_t* post;               // this GEMM's epilogue completions per M-tile
+    int pdl;                      // 1: let the next kernel launch after the prologue; 2: once the tiles run out
 };
 
 struct PairTile {
@@ -299,6 +307,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     __syncthreads();
     cluster_sync_all();  // both CTAs' barriers exist before any copy, commit or arrive targets them
     tc_fence_after();
+    if (p.pdl == 1) pdl_launch_dependents();
     const uint32_t tmem_base = ctl->tmem_base;
     volatile uint32_t* abort_word = &ctl->abort_flag;
     const volatile uint32_t* never = &ctl->zero;
@@ -361,6 +370,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     slot_phase ^= 1u;
                 }
                 if (info.x < 0) break;
+                if (p.wait_rows != nullptr || p.wait_h != nullptr) {
+                    // tile-synchronised path: every row of the pair block has landed (gemm1) or
+                    // every gemm1 tile of the block has stored its h rows (gemm2)
+                    uint32_t ready = 1u;
+                    if (leader) {
+                        const int g0 = sem_tile0(p.offsets, p.mtile_start, info.x, info.y);
+                        for (int q = 0; q < (info.z > BM ? 2 : 1) && ready; ++q) {
+                            const uint32_t want =
+                                p.wait_rows != nullptr
+                                    ? static_cast<uint32_t>(min(BM, info.z - q * BM))
+                                    : static_cast<uint32_t>(p.wait_ntiles * (info.z <= p.wait_swap_max ? 8 : 4));
+                            const uint32_t* ctr = (p.wait_rows != nullptr ? p.wait_rows : p.wait_h) + g0 + q;
+                            ready = wait_count_bounded(ctr, want, abort_word, p.timeout_ns) ? 1u : 0u;
+                        }
+                        fence_proxy_async_global();  // the rows are read next through TMA
+                    }
+                    if (!__shfl_sync(0xffffffffu, ready, lead)) {
+                        ok = false;
+                        break;
+                    }
+                }
                 const bool swap = is_swap(info.z, p);
                 int a_row = info.y + static_cast<int>(rank) * BM;
                 int b_row = info.x * p.b_rows_per_expert + info.w + static_cast<int>(rank) * p.b_half_rows;
@@ -419,6 +449,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!ok) break;
             }
+            if (p.pdl == 2) pdl_launch_dependents();  // no tile left to claim: the next kernel may launch
             if (leader) {
                 if (!ok) {
                     raise_abort(ctl, peer);
@@ -532,6 +563,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             tc_fence_after();
             const uint32_t tbase = tmem_base + (static_cast<uint32_t>(sub * 32) << 16) + acc * MMA_N;
+            if (p.weight_rows != nullptr) {
+                // the row weights were written by the dispatch with the rows: acquire the block's row counters
+                const int g0 = sem_tile0(p.offsets, p.mtile_start, info.x, info.y);
+                if (lane == 0)
+                    for (int q = 0; q < (info.z > BM ? 2 : 1); ++q)
+                        if (!wait_count_bounded(p.weight_rows + g0 + q, static_cast<uint32_t>(min(BM, info.z - q * BM)),
+                                                abort_word, p.timeout_ns))
+                            ok = false;
+                __syncwarp();
+                if (!__shfl_sync(0xffffffffu, ok ? 1u : 0u, 0)) break;
+            }
             if (is_swap(info.z, p)) {
                 bf16* oblock = p.out + static_cast<int64_t>(info.y) * p.out_ld;
                 if (MODE == 0) {
@@ -559,6 +601,24 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive_cluster(tmem_empty0 + acc * 8u);
+            if (p.post != nullptr) {
+                // publish this warp's rows: every lane's proxy fence (gemm2 reads h through TMA),
+                // the warp barrier (orders the lanes' stores before lane 0's release increment,
+                // which is cumulative over them), then one increment per M-tile the warp wrote
+                // (a full tile: this CTA's M-tile; a swap tile: every M-tile of the block, since
+                // each warp writes all of its rows)
+                fence_proxy_async_global();
+                __syncwarp();
+                if (lane == 0) {
+                    const int g0 = sem_tile0(p.offsets, p.mtile_start, info.x, info.y);
+                    if (is_swap(info.z, p)) {
+                        red_release_gpu_add(p.post + g0, 1u);
+                        if (info.z > BM) red_release_gpu_add(p.post + g0 + 1, 1u);
+                    } else {
+                        red_release_gpu_add(p.post + g0 + static_cast<int>(rank), 1u);
+                    }
+                }
+            }
             acc ^= 1u;
             if (acc == 0) acc_phase ^= 1u;
         }
@@ -628,7 +688,8 @@ cudaError_t launch_pair_mode(const PairMaps& m, const PairParams& p, int64_t S, 
     const int64_t resident = max_clusters[slot].load(std::memory_order_relaxed);
     const int clusters = static_cast<int>(std::min<int64_t>(resident, std::max<int64_t>(max_tiles, 1)));
     cfg.gridDim = dim3(2 * clusters);
-    err = cudaLaunchKernelEx(&cfg, fn, m.a, m.b0, m.b1, m.a16, m.a32, m.a64, m.b0q, m.b1q, p);
+    LaunchCfg lc(cfg.gridDim, cfg.blockDim, PSMEM_BYTES, s, p.pdl != 0, 2);
+    err = cudaLaunchKernelEx(&lc.cfg, fn, m.a, m.b0, m.b1, m.a16, m.a32, m.a64, m.b0q, m.b1q, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
@@ -660,11 +721,18 @@ cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s) {
     p.k_blocks = a.d / BK;
     p.b_rows_per_expert = a.f;
     p.b_half_rows = 0;  // full tiles: CTA 1 reads the same rows of W3 through its own map
-    p.swap_max_rows = p.k_blocks >= 64 ? kSwapMaxRows : kSwapMaxRowsShortK;
+    p.swap_max_rows = pair_swap_max_rows(1, p.k_blocks);
     p.status = a.status;
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = (a.inject == MK_INJECT_STALL_GEMM1) ? 1 : 0;
     p.ticket = a.tickets;
+    p.wait_rows = a.sem.mt_rows;
+    p.wait_h = nullptr;
+    p.wait_ntiles = 0;
+    p.wait_swap_max = 0;
+    p.weight_rows = nullptr;
+    p.post = a.sem.h_ready;
+    p.pdl = a.sem.pdl ? 1 : 0;
     return launch_pair_mode<0>(m, p, a.S, s);
 }
 
@@ -691,6 +759,13 @@ cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s) {
     p.timeout_ns = a.timeout_ns;
     p.stall_first_stage = 0;
     p.ticket = a.tickets + 1;
+    p.wait_rows = nullptr;
+    p.wait_h = a.sem.h_ready;
+    p.wait_ntiles = (a.f + MMA_N / 2 - 1) / (MMA_N / 2);
+    p.wait_swap_max = pair_swap_max_rows(1, a.d / BK);
+    p.weight_rows = a.sem.mt_rows;
+    p.post = a.sem.p_ready;
+    p.pdl = a.sem.pdl ? 2 : 0;
     return launch_pair_mode<1>(m, p, a.S, s);
 }
 
@@ -699,6 +774,10 @@ cudaError_t launch_gemm2_pair(const FfnArgs& a, cudaStream_t s) {
 // tiles' extra rows cost more than the split operands save (same GPU,
 // alternating builds: large -6%, skewed -6%, mid -3%, decode +5% on pairs).
 bool use_pairs(const FfnArgs& a) { return a.S >= static_cast<int64_t>(PAIR_M) * a.E; }
+
+int pair_swap_max_rows(int gemm, int k_blocks) {
+    return (gemm == 1 && k_blocks < 64) ? kSwapMaxRowsShortK : kSwapMaxRows;
+}
 
 cudaError_t launch_gemm1_auto(const FfnArgs& a, cudaStream_t s) {
     return use_pairs(a) ? launch_gemm1_pair(a, s) : launch_gemm1(a, s);

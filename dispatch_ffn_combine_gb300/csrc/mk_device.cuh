@@ -315,6 +315,57 @@ __device__ __forceinline__ void st_shared_cluster_v4(uint32_t addr, int4 v) {
                  : "memory");
 }
 
+// ----------------------------------------------------------------- programmatic dependent launch
+//
+// A kernel launched with programmatic stream serialization may start before
+// the kernel ahead of it on the stream has finished: it is launched once every
+// block of that kernel has executed launch_dependents (or exited).  Without
+// that launch attribute both instructions do nothing.
+
+// Wait until the kernel ahead on the stream has completed and its memory
+// operations are visible.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
+// Allow the next kernel on the stream to be launched.
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" :::); }
+
+// ----------------------------------------------------------------- data-tile semaphores
+//
+// Counters in global memory that a producing kernel raises with release
+// semantics once its writes to a tile are done, and a consuming kernel reads
+// with acquire semantics before it touches the tile.
+
+__device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void red_release_gpu_add(uint32_t* p, uint32_t v) {
+    asm volatile("red.release.gpu.global.add.u32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Generic-proxy writes of this thread before async-proxy (TMA) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Wait until *p >= want (acquire).  Returns false if the abort word is set or
+// timeout_ns passes first.  Backs off with nanosleep between polls.
+__device__ __forceinline__ bool wait_count_bounded(const uint32_t* p, uint32_t want,
+                                                   const volatile uint32_t* abort_word, uint64_t timeout_ns) {
+    if (ld_acquire_gpu(p) >= want) return true;
+    const uint64_t t0 = globaltimer_ns();
+    uint32_t backoff = 32;
+    for (;;) {
+        asm volatile("nanosleep.u32 %0;" ::"r"(backoff));
+        if (ld_acquire_gpu(p) >= want) return true;
+        if (abort_word != nullptr && *abort_word != 0u) return false;
+        if (globaltimer_ns() - t0 > timeout_ns) return false;
+        backoff = backoff < 1024 ? 2 * backoff : 1024;
+    }
+}
+
 // ----------------------------------------------------------------- small numerics
 
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {

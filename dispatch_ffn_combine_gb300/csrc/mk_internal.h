@@ -29,6 +29,7 @@ enum : uint32_t {
     kSiteCountIds = 0x500,
     kSiteCountRepeat = 0x600,
     kSiteFusedIdle = 0x800,
+    kSiteCombineWait = 0x900,
 };
 
 // Byte offsets of every region of the caller's workspace.  The first 256
@@ -54,6 +55,7 @@ struct WsLayout {
     size_t h = 0;             // bf16  [S, f]
     size_t P = 0;             // bf16  [S, d]
     size_t sync = 0;          // fused kernel: tickets, counters and ready flags (zeroed per call)
+    size_t tile_sems = 0;     // tile-synchronised path: per-M-tile semaphores (zeroed per call)
     size_t x_stage = 0;       // bf16  [T, d]  host-buffer entry point: staged input
     size_t y_stage = 0;       // bf16  [T, d]  host-buffer entry point: staged output
     size_t total = 0;
@@ -66,9 +68,67 @@ WsLayout ws_layout_dispatch(int64_t T, int d, int E, int k);
 
 inline int64_t num_chunks(int64_t T) { return (T + kChunkTokens - 1) / kChunkTokens; }
 
+// Data-tile semaphores of the tile-synchronised path (MK_PATH_TILES): one
+// counter per 128-row M-tile of the dispatched rows (the tile table's order),
+// zeroed at the start of each call, raised with release semantics by the step
+// that fills the tile and read with acquire semantics by the step that reads
+// it.
+//   mt_rows   rows the dispatch has written into the M-tile; complete at the
+//             tile's row count, min(128, expert rows from the tile's first row)
+//   h_ready   gemm1 epilogue warps done with the tile, one N block at a time;
+//             complete at 4 per N block (8 for a CTA-pair swap tile, whose
+//             eight epilogue warps each write every row of the block)
+//   p_ready   the same for gemm2
+//   tok_done  tokens whose dispatch (slot rows, row tokens, row weights and
+//             rows) is written
+struct TileSems {
+    uint32_t* mt_rows = nullptr;
+    uint32_t* h_ready = nullptr;
+    uint32_t* p_ready = nullptr;
+    uint32_t* tok_done = nullptr;
+    bool pdl = false;  // the kernels are launched as programmatic dependents
+    bool drop_token0 = false;  // test hook: the dispatch does not publish token 0's rows
+};
+// Counters per semaphore array: an upper bound on the M-tiles (every expert
+// adds at most one partial tile).
+inline int64_t tile_sem_units(int64_t S, int E) { return (S + kTileM - 1) / kTileM + E; }
+inline size_t tile_sems_bytes(int64_t S, int E) { return 4 * static_cast<size_t>(3 * tile_sem_units(S, E) + 1); }
+TileSems tile_sems_at(void* base, int64_t S, int E, bool pdl);
+
+// cudaLaunchKernelEx configuration: `pdl` adds programmatic stream
+// serialization (the kernel may be launched before the one ahead of it on the
+// stream has finished), cluster_x > 1 a cluster dimension.
+struct LaunchCfg {
+    cudaLaunchConfig_t cfg{};
+    cudaLaunchAttribute attr[2]{};
+    LaunchCfg(dim3 grid, dim3 block, size_t smem, cudaStream_t s, bool pdl, unsigned cluster_x = 1) {
+        cfg.gridDim = grid;
+        cfg.blockDim = block;
+        cfg.dynamicSmemBytes = smem;
+        cfg.stream = s;
+        unsigned n = 0;
+        if (cluster_x > 1) {
+            attr[n].id = cudaLaunchAttributeClusterDimension;
+            attr[n].val.clusterDim.x = cluster_x;
+            attr[n].val.clusterDim.y = 1;
+            attr[n].val.clusterDim.z = 1;
+            ++n;
+        }
+        if (pdl) {
+            attr[n].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+            attr[n].val.programmaticStreamSerializationAllowed = 1;
+            ++n;
+        }
+        cfg.attrs = attr;
+        cfg.numAttrs = n;
+    }
+};
+
 // ----------------------------------------------------------------- launchers
+// `pdl`: launched as a programmatic dependent (the kernel waits for the one
+// ahead of it before reading anything, then lets the next one launch).
 cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
-                                float* logits, cudaStream_t s);
+                                float* logits, cudaStream_t s, bool pdl = false);
 // Router with the tensor-core candidate filter (route_tc.cu): approximate
 // logits with an error bound, then the fixed-order fp32 logits of the
 // candidates only, top-k and softmax.  Same outputs as launch_route_logits +
@@ -76,25 +136,35 @@ cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bia
 bool route_tc_supported(int d, int E);
 cudaError_t launch_route_approx(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* approx, bf16* wsplit, float* wnorm, uint32_t* status, uint64_t timeout_ns,
-                                cudaStream_t s);
+                                cudaStream_t s, bool pdl = false);
 cudaError_t launch_route_select(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E, int k,
                                 const float* approx, const float* wnorm, int32_t* ids, float* w, int32_t* counts,
-                                uint32_t* fallbacks, bool zero_bound, cudaStream_t s);
+                                uint32_t* fallbacks, bool zero_bound, cudaStream_t s, bool pdl = false);
 cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
-                        int32_t* counts_or_null, cudaStream_t s);
+                        int32_t* counts_or_null, cudaStream_t s, bool pdl = false);
 cudaError_t launch_count(const int32_t* ids, int64_t T, int E, int k, int32_t* chunk_counts, int32_t* rank,
-                         uint32_t* status, cudaStream_t s);
+                         uint32_t* status, cudaStream_t s, bool pdl = false);
 // `done`: a zeroed word (left zero again) that picks the last block for the expert scan.
 cudaError_t launch_scan(const int32_t* chunk_counts, int64_t nchunks, int E, int32_t* chunk_base, int32_t* counts,
-                        int32_t* offsets, int32_t* mtile_start, uint32_t* done, cudaStream_t s);
+                        int32_t* offsets, int32_t* mtile_start, uint32_t* done, cudaStream_t s, bool pdl = false);
 cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, int64_t T, int d, int E, int k,
                            const int32_t* offsets, const int32_t* chunk_base, const int32_t* rank, bf16* x_perm,
-                           int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s);
+                           int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s,
+                           const TileSems* sem = nullptr, const int32_t* mtile_start = nullptr);
 cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t* mtile_start, uint32_t* status,
                                cudaStream_t s);
 // y[t] = sum_j P[slot_row[t, j]] for t < T; p_rows = rows of P (-1: T * k).
 cudaError_t launch_combine(const bf16* P, const int32_t* slot_row, int64_t T, int d, int k, bf16* y,
                            cudaStream_t s, int64_t p_rows = -1);
+
+// The combine of the tile-synchronised path: token t's rows are summed once
+// the dispatch has written its slot rows (tok_done) and gemm2 has published
+// every M-tile they lie in (p_ready; `pairs`: gemm2 ran on CTA pairs with
+// swap tiles of at most swap_max rows, n_tiles N blocks per tile).
+cudaError_t launch_combine_sem(const bf16* P, const int32_t* slot_row, const int32_t* offsets,
+                               const int32_t* mtile_start, int64_t T, int d, int E, int k, bf16* y,
+                               const TileSems& sem, bool pairs, int n_tiles, int swap_max, uint32_t* status,
+                               uint64_t timeout_ns, cudaStream_t s);
 
 struct FfnArgs {
     const bf16* x_perm;
@@ -112,7 +182,11 @@ struct FfnArgs {
     uint64_t timeout_ns;
     int inject;                  // MK_INJECT_STALL_GEMM1 or 0
     uint32_t* tickets;           // 2 zeroed words: tile tickets of gemm1 [0] and gemm2 [1]
+    TileSems sem{};              // tile-synchronised path only (default: none)
 };
+// The pair kernels' swap-tile thresholds (gemm2's combine readiness needs it).
+int pair_swap_max_rows(int gemm, int k_blocks);
+bool use_pairs(const FfnArgs& a);
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s);
 // The same GEMMs on CTA pairs (tcgen05 cta_group::2; gemm_pair.cu).
 cudaError_t launch_gemm1_pair(const FfnArgs& a, cudaStream_t s);

@@ -20,6 +20,8 @@ __global__ void __launch_bounds__(256, MINB) route_logits_kernel(const uint16_t*
                                                               float* __restrict__ logits) {
     using RT = RouteTile<WT, WE, HT, MINB>;
     extern __shared__ __align__(128) uint8_t smem[];
+    pdl_wait();  // as a programmatic dependent: the kernel ahead has finished
+    pdl_launch_dependents();
     const int n_eg = (E + RT::CE - 1) / RT::CE;
     route_detail::route_block<WT, WE, HT, MINB>(smem, x, wg, bias, T, d, E, logits,
                                                  static_cast<int>(blockIdx.x / n_eg),
@@ -28,7 +30,7 @@ __global__ void __launch_bounds__(256, MINB) route_logits_kernel(const uint16_t*
 
 template <int WT, int WE, int HT, int MINB>
 cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float* bias, int64_t T, int d, int E,
-                                float* logits, cudaStream_t s) {
+                                float* logits, cudaStream_t s, bool pdl) {
     using RT = RouteTile<WT, WE, HT, MINB>;
     static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
@@ -41,7 +43,10 @@ cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float
         if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     const unsigned grid = static_cast<unsigned>(((E + RT::CE - 1) / RT::CE) * ((T + RT::CT - 1) / RT::CT));
-    route_logits_kernel<WT, WE, HT, MINB><<<grid, 256, RT::SMEM, s>>>(xb, wg, bias, static_cast<int>(T), d, E, logits);
+    LaunchCfg lc(dim3(grid), dim3(256), RT::SMEM, s, pdl);
+    err = cudaLaunchKernelEx(&lc.cfg, route_logits_kernel<WT, WE, HT, MINB>, xb, wg, bias, static_cast<int>(T), d, E,
+                             logits);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
@@ -50,6 +55,8 @@ cudaError_t launch_logits_shape(const uint16_t* xb, const float* wg, const float
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ logits, int64_t T, int E, int k,
                                                    int32_t* __restrict__ ids, float* __restrict__ w,
                                                    int32_t* __restrict__ counts) {
+    pdl_wait();  // as a programmatic dependent: the logits are complete
+    pdl_launch_dependents();
     const int lane = threadIdx.x & 31;
     const int64_t t = static_cast<int64_t>(blockIdx.x) * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -111,18 +118,20 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ log
 }  // namespace
 
 cudaError_t launch_route_logits(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
-                                float* logits, cudaStream_t s) {
+                                float* logits, cudaStream_t s, bool pdl) {
     const uint16_t* xb = reinterpret_cast<const uint16_t*>(x);
     // 32 x 32 blocks when there are enough experts, else 64 tokens x 16 experts
     // (expert rows past E are clamped duplicates whose logits are not stored).
-    if (E >= 32) return launch_logits_shape<2, 4, 8, 1>(xb, wg, bias, T, d, E, logits, s);
-    return launch_logits_shape<4, 2, 8, 1>(xb, wg, bias, T, d, E, logits, s);
+    if (E >= 32) return launch_logits_shape<2, 4, 8, 1>(xb, wg, bias, T, d, E, logits, s, pdl);
+    return launch_logits_shape<4, 2, 8, 1>(xb, wg, bias, T, d, E, logits, s, pdl);
 }
 
 cudaError_t launch_topk(const float* logits, int64_t T, int E, int k, int32_t* ids, float* w,
-                        int32_t* counts_or_null, cudaStream_t s) {
+                        int32_t* counts_or_null, cudaStream_t s, bool pdl) {
     const unsigned blocks = static_cast<unsigned>((T + 7) / 8);
-    topk_kernel<<<blocks, 256, 0, s>>>(logits, T, E, k, ids, w, counts_or_null);
+    LaunchCfg lc(dim3(blocks), dim3(256), 0, s, pdl);
+    const cudaError_t err = cudaLaunchKernelEx(&lc.cfg, topk_kernel, logits, T, E, k, ids, w, counts_or_null);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

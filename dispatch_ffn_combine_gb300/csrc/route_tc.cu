@@ -125,6 +125,8 @@ __global__ void __launch_bounds__(kApproxThreads, 1)
                         uint32_t* status, uint64_t timeout_ns) {
     using C = ApproxCfg<N>;
     extern __shared__ uint8_t smem_raw[];
+    pdl_wait();  // as a programmatic dependent: the split gate rows are complete
+    pdl_launch_dependents();
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     ApproxCtl* ctl = reinterpret_cast<ApproxCtl*>(smem + C::STAGES * C::STAGE_BYTES);
     const int warp = threadIdx.x >> 5;
@@ -364,6 +366,8 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
     __shared__ float s_nx;
     __shared__ int s_ncand;
     __shared__ int s_violated;
+    pdl_wait();  // as a programmatic dependent: the approximate logits are complete
+    pdl_launch_dependents();
     const int64_t t = blockIdx.x;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
@@ -542,7 +546,8 @@ __global__ void __launch_bounds__(kSelThreads) route_select_kernel(
 
 template <int N>
 cudaError_t launch_approx_n(const CUtensorMap& mx, const CUtensorMap& mw, const float* bias, int64_t T, int E,
-                            int kb_total, float* approx, uint32_t* status, uint64_t timeout_ns, cudaStream_t s) {
+                            int kb_total, float* approx, uint32_t* status, uint64_t timeout_ns, cudaStream_t s,
+                            bool pdl) {
     static std::atomic<int> configured[64];  // per device: attributes set (repeating them is harmless)
     int dev = 0;
     cudaError_t err = cudaGetDevice(&dev);
@@ -555,8 +560,9 @@ cudaError_t launch_approx_n(const CUtensorMap& mx, const CUtensorMap& mw, const 
         if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
     const unsigned grid = static_cast<unsigned>((T + 127) / 128);
-    fn<<<grid, kApproxThreads, approx_smem<N>(), s>>>(mx, mw, bias, static_cast<int>(T), E, kb_total, approx, status,
-                                                       timeout_ns);
+    LaunchCfg lc(dim3(grid), dim3(kApproxThreads), approx_smem<N>(), s, pdl);
+    err = cudaLaunchKernelEx(&lc.cfg, fn, mx, mw, bias, static_cast<int>(T), E, kb_total, approx, status, timeout_ns);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 
@@ -568,7 +574,7 @@ bool route_tc_supported(int d, int E) { return route_select_smem(d, E) <= 160 * 
 
 cudaError_t launch_route_approx(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E,
                                 float* approx, bf16* wsplit, float* wnorm, uint32_t* status, uint64_t timeout_ns,
-                                cudaStream_t s) {
+                                cudaStream_t s, bool pdl) {
     route_prep_kernel<<<E, 256, 0, s>>>(wg, d, wsplit, wnorm);
     cudaError_t err = cudaGetLastError();
     if (err != cudaSuccess) return err;
@@ -579,17 +585,17 @@ cudaError_t launch_route_approx(const bf16* x, const float* wg, const float* bia
         return cudaErrorInvalidValue;
     const int kb_total = d / 32;  // 2d / 64
     switch (N) {
-        case 16: return launch_approx_n<16>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s);
-        case 32: return launch_approx_n<32>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s);
-        case 64: return launch_approx_n<64>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s);
-        case 128: return launch_approx_n<128>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s);
-        default: return launch_approx_n<256>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s);
+        case 16: return launch_approx_n<16>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s, pdl);
+        case 32: return launch_approx_n<32>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s, pdl);
+        case 64: return launch_approx_n<64>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s, pdl);
+        case 128: return launch_approx_n<128>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s, pdl);
+        default: return launch_approx_n<256>(mx, mw, bias, T, E, kb_total, approx, status, timeout_ns, s, pdl);
     }
 }
 
 cudaError_t launch_route_select(const bf16* x, const float* wg, const float* bias, int64_t T, int d, int E, int k,
                                 const float* approx, const float* wnorm, int32_t* ids, float* w, int32_t* counts,
-                                uint32_t* fallbacks, bool zero_bound, cudaStream_t s) {
+                                uint32_t* fallbacks, bool zero_bound, cudaStream_t s, bool pdl) {
     // bound coefficients (see the top of this file), rounded up
     const double u = 1.0 / 16777216.0;
     const int kb_total = d / 32;
@@ -610,9 +616,10 @@ cudaError_t launch_route_select(const bf16* x, const float* wg, const float* bia
         if (err != cudaSuccess) return err;
         if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
-    route_select_kernel<<<static_cast<unsigned>(T), kSelThreads, smem, s>>>(x, wg, bias, approx, wnorm, d, E, k,
-                                                                          c_rel_f, c_abs_f, ids, w, counts,
-                                                                          fallbacks);
+    LaunchCfg lc(dim3(static_cast<unsigned>(T)), dim3(kSelThreads), smem, s, pdl);
+    err = cudaLaunchKernelEx(&lc.cfg, route_select_kernel, x, wg, bias, approx, wnorm, d, E, k, c_rel_f, c_abs_f, ids,
+                             w, counts, fallbacks);
+    if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }
 

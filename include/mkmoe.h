@@ -81,8 +81,8 @@ enum {
     MK_PHASE_COMBINE = 7,      /* y[t] = sum_j P[slot_row[t,j]] in j order           */
     MK_PHASE_COUNT_ALL = 8
 };
-/* On the fused path (opts->path = MK_PATH_FUSED) the steps overlap inside one kernel: phase_events then
- * gets event 0 before the kernels and events 1..MK_PHASE_COUNT_ALL after them. */
+/* On the fused and tile-synchronised paths (opts->path = MK_PATH_FUSED or MK_PATH_TILES) the steps
+ * overlap: phase_events then gets event 0 before the kernels and events 1..MK_PHASE_COUNT_ALL after them. */
 
 /* Optional per-call settings (pass NULL for defaults). */
 typedef struct {
@@ -119,8 +119,18 @@ typedef struct {
 
 #define MK_PATH_STEPS 0
 #define MK_PATH_FUSED 1
+#define MK_PATH_TILES 2  /* one kernel per step, each launched as a programmatic dependent of the one before
+                            it, synchronised per 128-row tile of dispatched rows by data-tile semaphores in
+                            the workspace (rows landed -> gemm1; h tile stored -> gemm2; P tile stored ->
+                            the combine of its tokens), so each step starts on the tiles whose inputs are
+                            ready; the MegaOps page's kernel-per-operator design with tile semaphores.
+                            Same bits as the other paths.  Test hook: MK_INJECT_DROP_TILE_SIGNAL only.  */
 
 #define MK_INJECT_STALL_GEMM1 1
+#define MK_INJECT_DROP_TILE_SIGNAL 3  /* test hook, tile-synchronised path only: the dispatch never
+                                         publishes token 0's rows, so the M-tiles holding them never
+                                         complete; every wait on them runs out after timeout_ns and the
+                                         call reports MK_ERR_TIMEOUT (no fault, no hang).            */
 #define MK_INJECT_ROUTE_ZERO_BOUND 2  /* test hook: the router's candidate filter runs with a zero
                                          error bound, so (almost) every token takes the exact
                                          fallback (all E logits in the fixed order); the results
