@@ -465,7 +465,7 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
                                status + 3, s));
             fa.routed = true;
         }
-        MK_TRY(launch_fused(fa, s));
+        MK_TRY(launch_fused_pair(fa, s));
         for (int i = 1; i <= MK_PHASE_COUNT_ALL; ++i) MK_TRY(pm.mark(i));
         return MK_OK;
     }

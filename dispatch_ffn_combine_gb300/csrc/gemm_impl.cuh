@@ -93,6 +93,66 @@ __device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, b
     epilogue_weighted_w<MMA_N>(tbase, row_ok, orow, n0, n_valid, wr);
 }
 
+constexpr int PAIR_M = 2 * BM;  // rows of a CTA-pair tile
+
+// Swap-tile epilogues: this thread's TMEM lane is one weight row (output
+// column), its columns the block's rows.  A warp stores one output row per
+// step (32 or 16 consecutive columns).
+//   gemm2:  out[j][n] = bf16(wr[j] * acc_j), j < rows; the block's row weights
+//           are loaded once, lane i holding rows i, i + 32, ...
+__device__ __forceinline__ void epilogue_weighted_swap(uint32_t tbase, int rows, bf16* ocol, int64_t ld, bool n_ok,
+                                                       const float* wr) {
+    const int lane = threadIdx.x & 31;
+    float wv[PAIR_M / 32];
+#pragma unroll
+    for (int c = 0; c < PAIR_M / 32; ++c) {
+        const int j = 32 * c + lane;
+        wv[c] = (wr != nullptr && j < rows) ? wr[j] : 1.0f;
+    }
+#pragma unroll 1
+    for (int c = 0; 32 * c < rows; ++c) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(tbase + 32 * c, a);
+        float w_lane = wv[0];
+#pragma unroll
+        for (int q = 1; q < PAIR_M / 32; ++q)
+            if (q == c) w_lane = wv[q];
+        tmem_ld_wait();
+        const int nj = rows - 32 * c;
+        bf16* o = ocol + static_cast<int64_t>(32 * c) * ld;
+#pragma unroll
+        for (int jj = 0; jj < 32; ++jj) {
+            const float wj = __shfl_sync(0xffffffffu, w_lane, jj);
+            if (n_ok && jj < nj) *o = __float2bfloat16_rn(__uint_as_float(a[jj]) * wj);
+            o += ld;
+        }
+    }
+}
+
+//   gemm1:  lanes l and l + 16 hold the gate and up rows of one column; one
+//           exchange per pair of block rows gives lane l the up value of the
+//           even row and lane l + 16 the gate value of the odd one:
+//           h[j][col] = bf16(silu(g_j) * u_j), even j by lanes 0-15, odd j by 16-31
+__device__ __forceinline__ void epilogue_swiglu_swap(uint32_t tbase, int rows, bf16* ocol, int64_t ld, bool c_ok) {
+    const bool lo = (threadIdx.x & 16) == 0;
+#pragma unroll 1
+    for (int j0 = 0; j0 < rows; j0 += 32) {
+        uint32_t a[32];
+        tmem_ld_32x32b_x32(tbase + j0, a);
+        tmem_ld_wait();
+        const int nj = rows - j0;
+        bf16* o = ocol + static_cast<int64_t>(j0 + (lo ? 0 : 1)) * ld;
+#pragma unroll
+        for (int m = 0; m < 16; ++m) {
+            const float x = __shfl_xor_sync(0xffffffffu, __uint_as_float(lo ? a[2 * m + 1] : a[2 * m]), 16);
+            const float g = lo ? __uint_as_float(a[2 * m]) : x;
+            const float u = lo ? x : __uint_as_float(a[2 * m + 1]);
+            if (c_ok && 2 * m + (lo ? 0 : 1) < nj) *o = __float2bfloat16_rn(silu_mul(g, u));
+            o += 2 * ld;
+        }
+    }
+}
+
 // Tile-synchronised path: index of the first 128-row M-tile of a block of
 // expert e's rows that starts at row0 (a multiple of 128 rows into the
 // expert), in the tile table's numbering.

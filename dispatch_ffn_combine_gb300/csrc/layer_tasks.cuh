@@ -218,7 +218,9 @@ __device__ __forceinline__ void dispatch_tokens(const int32_t* __restrict__ ids,
 
 // y[t] = bf16( sum_j P[slot_row[t, j]] ), j ascending, fp32 sum, for tokens
 // [t0, t0 + nt).  A warp per token; each lane loads its 16-byte piece of all
-// k rows before adding them in slot order.
+// k rows before adding them in slot order.  P is written earlier in the same
+// launch by other blocks, so it is read from L2 (ld.global.cg), never through
+// the non-coherent read-only path.
 __device__ __forceinline__ void combine_tokens(const bf16* __restrict__ P, const int32_t* __restrict__ slot_row,
                                                int64_t t0, int nt, int d, int k, bf16* __restrict__ y) {
     const int warp = threadIdx.x >> 5;
@@ -233,7 +235,7 @@ __device__ __forceinline__ void combine_tokens(const bf16* __restrict__ P, const
             uint4 v[kMaxTopK];
 #pragma unroll
             for (int j = 0; j < kMaxTopK; ++j)
-                if (j < k) v[j] = reinterpret_cast<const uint4*>(P + rows[j] * d)[cc];
+                if (j < k) v[j] = __ldcg(reinterpret_cast<const uint4*>(P + rows[j] * d) + cc);
             float acc[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) acc[q] = 0.0f;

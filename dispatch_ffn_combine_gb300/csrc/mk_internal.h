@@ -211,6 +211,7 @@ struct FusedSync {
     uint32_t abort_flag;      // set by a block whose bounded wait ran out
     uint32_t ntask[2];        // finished tasks per role (mover, compute)
     uint32_t trace_n;         // trace records claimed
+    uint32_t h_tiles;         // CTA-pair kernel: gemm1 epilogue warps finished, all pair blocks
     unsigned long long cyc[2];  // summed task cycles per role
 };
 
@@ -248,7 +249,8 @@ struct FusedArgs {
     bool routed = false;  // ids, w, chunk_counts, rank and the scans are already computed
 };
 size_t fused_sync_bytes(int64_t T, int E, int k);
-cudaError_t launch_fused(const FusedArgs& a, cudaStream_t s);
+// The layer as one persistent kernel on CTA pairs (fused_pair.cu).
+cudaError_t launch_fused_pair(const FusedArgs& a, cudaStream_t s);
 cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s);
 
 // Argument checks every entry point shares: sizes within the limits the

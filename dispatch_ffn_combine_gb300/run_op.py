@@ -21,7 +21,7 @@ import json
 
 import torch
 
-from . import (MK_PATH_FUSED, MK_PATH_STEPS, TRACE_KINDS, alloc_dispatch_gemm_workspace, alloc_workspace,
+from . import (MK_PATH_FUSED, MK_PATH_STEPS, MK_PATH_TILES, TRACE_KINDS, alloc_dispatch_gemm_workspace, alloc_workspace,
                mk_moe_combine, mk_moe_dispatch, mk_moe_dispatch_gemm, mk_moe_expert_ffn, mk_moe_layer,
                mk_moe_layer_trace_count, mk_moe_route)
 from .workloads import CONFIGS, make_inputs
@@ -74,7 +74,7 @@ def main(argv=None) -> dict:
     ap.add_argument("--tokens", type=int, default=None, help="override the workload's token count")
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--calls", type=int, default=1)
-    ap.add_argument("--path", choices=("steps", "fused"), default="steps", help="layer path (op=layer)")
+    ap.add_argument("--path", choices=("steps", "fused", "tiles"), default="steps", help="layer path (op=layer)")
     ap.add_argument("--trace", action="store_true", help="op=layer, path=fused: summarise one traced call")
     args = ap.parse_args(argv)
     if args.trace and (args.op != "layer" or args.path != "fused"):
@@ -88,7 +88,7 @@ def main(argv=None) -> dict:
     T, d = x.shape
     E, k, f = cfg.E, cfg.k, cfg.f
     ws = alloc_workspace(T, d, E, k, f, dev)
-    path = MK_PATH_STEPS if args.path == "steps" else MK_PATH_FUSED
+    path = {"steps": MK_PATH_STEPS, "fused": MK_PATH_FUSED, "tiles": MK_PATH_TILES}[args.path]
 
     dg_ws = alloc_dispatch_gemm_workspace(T, d, E, k, dev) if args.op == "dispatch_gemm" else None
     ids, w, _ = mk_moe_route(x, wg, bias, k, ws=ws)
