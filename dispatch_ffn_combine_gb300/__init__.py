@@ -36,9 +36,10 @@ ENTRY_POINTS = (
     "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
     "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count", "mk_moe_route_fallbacks",
     "mk_moe_grouped_gemm", "mk_moe_dispatch_gemm_workspace_size", "mk_moe_dispatch_gemm",
-    "mk_moe_route_approx_logits", "mk_moe_workspace_region",
+    "mk_moe_route_approx_logits", "mk_moe_workspace_region", "mk_moe_ep_regroup_workspace_size",
+    "mk_moe_ep_regroup",
 )
-_SIZE_RESULT = ("mk_moe_workspace_size", "mk_moe_dispatch_gemm_workspace_size")
+_SIZE_RESULT = ("mk_moe_workspace_size", "mk_moe_dispatch_gemm_workspace_size", "mk_moe_ep_regroup_workspace_size")
 
 _lock = threading.Lock()
 _lib = None
@@ -95,6 +96,9 @@ def load_library():
         lib.mk_moe_dispatch_gemm.argtypes = [P, P, P, P, I64, I, I, I, I, P, P, P, P, P, SZ, P]
         lib.mk_moe_route_approx_logits.argtypes = [P, I64, I, I, I, P, P]
         lib.mk_moe_workspace_region.argtypes = [I64, I, I, I, I, I, ctypes.POINTER(SZ), ctypes.POINTER(SZ)]
+        lib.mk_moe_ep_regroup_workspace_size.restype = SZ
+        lib.mk_moe_ep_regroup_workspace_size.argtypes = [I, I]
+        lib.mk_moe_ep_regroup.argtypes = [P, P, P, I, I, I64, I, I, P, P, SZ, P]
         for name in ENTRY_POINTS:
             if name not in _SIZE_RESULT + ("mk_moe_status_string",):
                 getattr(lib, name).restype = I
@@ -444,3 +448,30 @@ def workspace_view(ws, T, d, E, k, ffn, region):
     _, dtype, shape = WS_REGIONS[region]
     off, nb = mk_moe_workspace_region(T, d, E, k, ffn, region)
     return ws[off:off + nb].view(dtype).view(shape(T, d, E, k, ffn))
+
+
+def mk_moe_ep_regroup(rows_in, counts, to_expert_major, rows_out=None, expert_offsets=None, ws=None, stream=None):
+    """Rows between source-major [q][e][rows] and expert-major [e][q][rows]
+    order (expert parallelism).  counts: int32 [G, E_local] on the device;
+    expert_offsets: optional int32 [E_local + 1] output (expert-major starts)."""
+    import math
+
+    G, El = counts.shape
+    _need(counts, torch.int32, (G, El), "counts")
+    if not rows_in.is_contiguous() or not rows_in.is_cuda:
+        raise ValueError("rows_in must be a contiguous CUDA tensor")
+    rows = rows_in.shape[0]
+    row_bytes = math.prod(rows_in.shape[1:]) * rows_in.element_size()
+    rows_out = torch.empty_like(rows_in) if rows_out is None else rows_out
+    if expert_offsets is not None:
+        _need(expert_offsets, torch.int32, (El + 1,), "expert_offsets")
+    if ws is None:
+        n = int(load_library().mk_moe_ep_regroup_workspace_size(G, El))
+        if n == 0:
+            raise ValueError("invalid G, E_local for the regroup")
+        ws = torch.empty(n, dtype=torch.uint8, device=rows_in.device)
+    st = load_library().mk_moe_ep_regroup(_p(rows_in), _p(rows_out), _p(counts), G, El, rows, row_bytes,
+                                          1 if to_expert_major else 0, _p(expert_offsets), _p(ws), ws.numel(),
+                                          _stream(stream))
+    _check(st, "mk_moe_ep_regroup")
+    return rows_out

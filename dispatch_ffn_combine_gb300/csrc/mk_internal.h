@@ -30,6 +30,7 @@ enum : uint32_t {
     kSiteCountRepeat = 0x600,
     kSiteFusedIdle = 0x800,
     kSiteCombineWait = 0x900,
+    kSiteRegroup = 0xA00,
 };
 
 // Byte offsets of every region of the caller's workspace.  The first 256

@@ -306,6 +306,35 @@ MK_API mk_status mk_moe_route_approx_logits(const void* ws, int64_t T, int d, in
 MK_API mk_status mk_moe_layer_trace_count(void* ws, int64_t T, int d, int E, int k, int ffn, void* stream,
                                           uint32_t* count);
 
+/* Expert parallelism (README kernel table, row "MoE Dispatch + FFN + Combine":
+ * tokens go "to their expert ranks" and the weighted outputs "back to each
+ * token's source rank"; paper section 3.1 and Table 3).  Over G ranks, rank r
+ * owns experts [r E_local, (r + 1) E_local).  After mk_moe_route and
+ * mk_moe_dispatch a rank's rows are expert-contiguous, so the rows for rank q
+ * are one contiguous range; the ranks exchange them (an all-to-all) and each
+ * receives, from every source q, the rows of its local experts grouped by
+ * expert: source-major order [q][e][rows].  mk_moe_ep_regroup moves rows
+ * between that order and expert-major order [e][q][rows] (what
+ * mk_moe_expert_ffn needs), and back (what the return all-to-all needs, so
+ * that every source gets its rows in the order it sent them).
+ *   rows_in, rows_out  device, `rows` rows of row_bytes bytes (a multiple of 4;
+ *                      both 16-byte aligned), distinct buffers
+ *   counts   int32 [G, E_local] (device): rows from source q for local expert e
+ *   to_expert_major    1: source-major -> expert-major; 0: the inverse
+ *   expert_offsets     int32 [E_local + 1] (out, device) or NULL: local expert e
+ *                      owns expert-major rows [off[e], off[e+1]) -- the
+ *                      offsets mk_moe_expert_ffn takes
+ *   ws       at least mk_moe_ep_regroup_workspace_size(G, E_local) bytes,
+ *            256-byte aligned (control block and offset tables)
+ * Limits: G * E_local <= 2048, rows < 2^31 (rows == 0 writes only the offsets).  Counts below zero or summing to
+ * anything but `rows` set MK_ERR_BOUNDS on the device (mk_moe_last_device_error
+ * on ws); the rows are then copied unmoved.  A row keeps its position inside
+ * its (source, expert) group, so the two directions are inverse permutations. */
+MK_API size_t mk_moe_ep_regroup_workspace_size(int G, int E_local);
+MK_API mk_status mk_moe_ep_regroup(const void* rows_in, void* rows_out, const int32_t* counts, int G, int E_local,
+                                   int64_t rows, int row_bytes, int to_expert_major, int32_t* expert_offsets,
+                                   void* ws, size_t ws_bytes, void* stream);
+
 /* Regions of a layer workspace (mk_moe_workspace_size(T, d, E, k, ffn) bytes)
  * that mk_moe_layer leaves filled when its call has finished, for checks and
  * diagnostics; both paths fill the same regions with the same bits.
