@@ -54,7 +54,7 @@ class MoEError(RuntimeError):
 class MkMoeOpts(ctypes.Structure):
     _fields_ = [("timeout_ns", ctypes.c_uint64), ("phase_events", ctypes.POINTER(ctypes.c_void_p)),
                 ("inject", ctypes.c_int), ("path", ctypes.c_int), ("mover_ctas", ctypes.c_int),
-                ("trace_cap", ctypes.c_int), ("trace", ctypes.c_void_p)]
+                ("trace_cap", ctypes.c_int), ("trace", ctypes.c_void_p), ("gather_rows", ctypes.c_int)]
 
 
 MK_INJECT_STALL_GEMM1 = 1
@@ -307,11 +307,12 @@ def mk_moe_combine(P, slot_row, y=None, stream=None):
     return y
 
 
-def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None):
+def _opts(phase_events, timeout_ns, inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None, gather_rows=False):
     if (phase_events is None and not timeout_ns and not inject and path == MK_PATH_STEPS and mover_ctas == 0
-            and trace is None):
+            and trace is None and not gather_rows):
         return None
     o = MkMoeOpts()
+    o.gather_rows = 1 if gather_rows else 0
     if trace is not None:
         if trace.dtype != torch.int32 or trace.dim() != 2 or trace.shape[1] != 8 or not trace.is_cuda:
             raise ValueError("trace must be a CUDA int32 tensor of shape [records, 8]")
@@ -344,18 +345,20 @@ def _layer_shapes(x, wg, bias, w1, w3, w2, device=True):
 
 
 def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None, timeout_ns=0, stream=None,
-                 inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None):
+                 inject=0, path=MK_PATH_STEPS, mover_ctas=0, trace=None, gather_rows=False):
     """The whole layer on device tensors; returns y [T, d] bf16.
 
     path: MK_PATH_STEPS (one kernel per step, default), MK_PATH_FUSED (one
     persistent kernel) or MK_PATH_TILES (one kernel per step, launched as
     programmatic dependents and synchronised per tile by data-tile
-    semaphores).  mover_ctas: fused-path SM split, 0 = adaptive."""
+    semaphores).  mover_ctas: fused-path SM split, 0 = adaptive.  gather_rows:
+    kernel-per-step path, gemm1 gathers its rows from x (no dispatched copy)."""
     T, d, E, f = _layer_shapes(x, wg, bias, w1, w3, w2)
     y = torch.empty((T, d), dtype=torch.bfloat16, device=x.device) if y is None else y
     ws = alloc_workspace(T, d, E, k, f, x.device) if ws is None else ws
     st = load_library().mk_moe_layer(_p(x), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k, f, _p(y), _p(ws),
-                                     ws.numel(), _opts(phase_events, timeout_ns, inject, path, mover_ctas, trace),
+                                     ws.numel(),
+                                     _opts(phase_events, timeout_ns, inject, path, mover_ctas, trace, gather_rows),
                                      _stream(stream))
     _check(st, "mk_moe_layer")
     return y

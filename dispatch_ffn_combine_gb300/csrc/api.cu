@@ -390,8 +390,9 @@ mk_status route_dispatch_steps(const bf16* xb, const float* wg, const float* bia
     MK_TRY(launch_scan(chunk_counts, num_chunks(T), E, chunk_base, at<int32_t>(ws, L.counts), o.offsets,
                        at<int32_t>(ws, L.mtile_start), status + 3, s));
     MK_TRY(pm.mark(MK_PHASE_SCATTER));
+    const bool gather = opts != nullptr && opts->gather_rows != 0;  // gemm1 reads x itself: no row copies
     MK_TRY(launch_scatter(xb, ids, w, T, d, E, k, o.offsets, chunk_base, rank, o.x_perm, o.row_token, o.row_weight,
-                          o.slot_row, s));
+                          o.slot_row, s, nullptr, nullptr, !gather));
     return MK_OK;
 }
 
@@ -552,10 +553,16 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
     a.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.inject = opts ? opts->inject : 0;  // only MK_INJECT_STALL_GEMM1 acts in the GEMMs
     a.tickets = status + 4;
+    const bool gather = opts != nullptr && opts->gather_rows != 0;
+    if (gather) {  // gemm1 gathers its rows from x by their source tokens (single-CTA tiles)
+        a.gather_x = static_cast<const bf16*>(x);
+        a.gather_T = T;
+        a.row_token = at<int32_t>(ws, L.row_token);
+    }
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
-    MK_TRY(launch_gemm1_auto(a, s));
+    MK_TRY(gather ? launch_gemm1(a, s) : launch_gemm1_auto(a, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
-    MK_TRY(launch_gemm2_auto(a, s));
+    MK_TRY(gather ? launch_gemm2(a, s) : launch_gemm2_auto(a, s));
     MK_TRY(pm.mark(MK_PHASE_COMBINE));
     if (hk.skip_combine) return MK_OK;
     MK_TRY(launch_combine(a.P, slot_row, T, d, k, static_cast<bf16*>(y), s));
@@ -583,6 +590,7 @@ mk_status validate_layer(const void* x, const float* wg, const void* w1, const v
         if (opts->path == MK_PATH_TILES && opts->inject != 0 && opts->inject != MK_INJECT_DROP_TILE_SIGNAL)
             return MK_ERR_INVALID_ARG;
         if (opts->mover_ctas < -1) return MK_ERR_INVALID_ARG;
+        if (opts->gather_rows != 0 && (opts->path != MK_PATH_STEPS || opts->inject != 0)) return MK_ERR_INVALID_ARG;
     }
     if ((st = check_ws(ws, ws_bytes, ws_layout(T, d, E, k, ffn))) != MK_OK) return st;
     return device_ok();

@@ -211,7 +211,7 @@ __global__ void __launch_bounds__(128) scatter_kernel(const bf16* __restrict__ x
                                                       int32_t* __restrict__ row_token, float* __restrict__ row_weight,
                                                       int32_t* __restrict__ slot_row, uint32_t* mt_rows,
                                                       uint32_t* tok_done, const int32_t* __restrict__ mtile_start,
-                                                      int drop_token0) {
+                                                      int drop_token0, int copy_rows) {
     __shared__ int64_t rows[kMaxTopK];
     __shared__ int32_t tiles[kMaxTopK];
     pdl_wait();  // as a programmatic dependent: offsets, chunk bases and ranks are complete
@@ -238,7 +238,7 @@ __global__ void __launch_bounds__(128) scatter_kernel(const bf16* __restrict__ x
         }
     }
     __syncthreads();
-    const int n16 = d / 8;  // 16-byte chunks per row
+    const int n16 = copy_rows ? d / 8 : 0;  // 16-byte chunks per row (none: only the index tables)
     const uint4* src = reinterpret_cast<const uint4*>(x + t * d);
     for (int c = threadIdx.x; c < n16; c += blockDim.x) {
         const uint4 v = __ldg(src + c);
@@ -287,13 +287,14 @@ cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t
 cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, int64_t T, int d, int E, int k,
                            const int32_t* offsets, const int32_t* chunk_base, const int32_t* rank, bf16* x_perm,
                            int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s,
-                           const TileSems* sem, const int32_t* mtile_start) {
+                           const TileSems* sem, const int32_t* mtile_start, bool copy_rows) {
     uint32_t* mt_rows = sem != nullptr ? sem->mt_rows : nullptr;
     uint32_t* tok_done = sem != nullptr ? sem->tok_done : nullptr;
     LaunchCfg lc(dim3(static_cast<unsigned>(T)), dim3(128), 0, s, sem != nullptr && sem->pdl);
     const cudaError_t err = cudaLaunchKernelEx(&lc.cfg, scatter_kernel, x, ids, w, T, d, E, k, offsets, chunk_base,
                                                rank, x_perm, row_token, row_weight, slot_row, mt_rows, tok_done,
-                                               mtile_start, (sem != nullptr && sem->drop_token0) ? 1 : 0);
+                                               mtile_start, (sem != nullptr && sem->drop_token0) ? 1 : 0,
+                                               copy_rows ? 1 : 0);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
 }

@@ -82,6 +82,7 @@ struct GemmParams {
     const uint32_t* weight_rows;  // gemm2: the dispatch's row counters, acquired before row weights
     uint32_t* post;               // this GEMM's epilogue completions per M-tile
     int pdl;                      // 1: let the next kernel launch after the prologue; 2: once the tiles run out
+    const int32_t* row_token;     // gemm1 reading x directly: source token of every dispatched row (else null)
 };
 
 struct TileInfo {
@@ -228,20 +229,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                 }
                 const int b_row = ti.e * p.b_rows_per_expert + ti.n0;
+                // gemm1 reading x directly: lane i gathers rows 4i .. 4i+3 of the tile by their
+                // source tokens (rows past the expert's end reuse a valid token; never stored)
+                int tok[4] = {0, 0, 0, 0};
+                if (p.row_token != nullptr) {
+                    const int first = p.row_token[ti.row0];
+#pragma unroll
+                    for (int j = 0; j < 4; ++j) {
+                        const int r = 4 * lane + j;
+                        tok[j] = (r < ti.rows) ? p.row_token[ti.row0 + r] : first;
+                    }
+                }
                 for (int kb = 0; kb < p.k_blocks; ++kb) {
                     if (!__all_sync(0xffffffffu, mbar_wait_bounded(smem_u32(&ctl->empty[stage]), phase ^ 1u,
                                                                   abort_word, p.timeout_ns))) {
                         ok = false;
                         break;
                     }
+                    const uint32_t fb = smem_u32(&ctl->full[stage]);
+                    const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
+                    if (p.row_token != nullptr) {
+                        // the stage is armed (with its full byte count) before the gathers
+                        if (leader) mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        __syncwarp();
+                        tma_gather4(sa + 512u * lane, &tmA, kb * BK, tok[0], tok[1], tok[2], tok[3], fb);
+                    }
                     if (leader) {
-                        const uint32_t fb = smem_u32(&ctl->full[stage]);
-                        const uint32_t sa = smem_u32(smem + stage * STAGE_BYTES);
                         const uint32_t sb = sa + A_BYTES;
-                        mbar_arrive_expect_tx(fb, STAGE_BYTES);
+                        if (p.row_token == nullptr) mbar_arrive_expect_tx(fb, STAGE_BYTES);
                         const bool stall = p.stall_first_stage && tile == 0 && kb == 0;
                         if (!stall) {  // injected stall: the stage is announced but never filled
-                            tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
+                            if (p.row_token == nullptr) tma_load_2d(sa, &tmA, kb * BK, ti.row0, fb);
                             if (MODE == 0) {
                                 tma_load_2d(sb, &tmB0, kb * BK, b_row, fb);
                                 tma_load_2d(sb + B_BYTES / 2, &tmB1, kb * BK, b_row, fb);
@@ -442,7 +460,10 @@ cudaError_t launch_mode(const CUtensorMap& a, const CUtensorMap& b0, const CUten
 
 cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s) {
     CUtensorMap ma, mb0, mb1;
-    if (!make_map(&ma, a.x_perm, a.d, a.S, BM) ||
+    // A: the dispatched rows in 128-row boxes, or, reading x directly, x's rows one at a time (gather4)
+    const bool gather = a.gather_x != nullptr;
+    if (!(gather ? make_map(&ma, a.gather_x, a.d, static_cast<uint64_t>(a.gather_T), 1)
+                 : make_map(&ma, a.x_perm, a.d, a.S, BM)) ||
         !make_map(&mb0, a.w1, a.d, static_cast<uint64_t>(a.E) * a.f, MMA_N / 2) ||
         !make_map(&mb1, a.w3, a.d, static_cast<uint64_t>(a.E) * a.f, MMA_N / 2))
         return cudaErrorInvalidValue;
@@ -468,6 +489,7 @@ cudaError_t launch_gemm1(const FfnArgs& a, cudaStream_t s) {
     p.weight_rows = nullptr;
     p.post = a.sem.h_ready;
     p.pdl = a.sem.pdl ? 1 : 0;
+    p.row_token = gather ? a.row_token : nullptr;
     return launch_mode<0>(ma, mb0, mb1, p, a.S, s);
 }
 
@@ -497,6 +519,7 @@ cudaError_t launch_gemm2(const FfnArgs& a, cudaStream_t s) {
     p.weight_rows = a.sem.mt_rows;
     p.post = a.sem.p_ready;
     p.pdl = a.sem.pdl ? 2 : 0;
+    p.row_token = nullptr;
     return launch_mode<1>(ma, mb0, mb0, p, a.S, s);
 }
 

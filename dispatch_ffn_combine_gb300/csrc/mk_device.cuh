@@ -103,6 +103,18 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
         : "memory");
 }
 
+// Four rows r0..r3 (any order, any distance) of a 2-D tensor whose box is one
+// row high, columns [c0, c0 + box width), written as four consecutive rows at
+// `dst` with the map's swizzle; completion as transaction bytes on `bar`.
+__device__ __forceinline__ void tma_gather4(uint32_t dst, const CUtensorMap* map, int32_t c0, int32_t r0, int32_t r1,
+                                            int32_t r2, int32_t r3, uint32_t bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes "
+        "[%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(dst),
+        "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(r0), "r"(r1), "r"(r2), "r"(r3), "r"(bar)
+        : "memory");
+}
+
 // Untiled bulk copy of `bytes` (a multiple of 16; both addresses 16-byte
 // aligned) from global memory into this CTA's shared memory; completion as
 // transaction bytes on `bar`.

@@ -151,7 +151,8 @@ cudaError_t launch_scan(const int32_t* chunk_counts, int64_t nchunks, int E, int
 cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, int64_t T, int d, int E, int k,
                            const int32_t* offsets, const int32_t* chunk_base, const int32_t* rank, bf16* x_perm,
                            int32_t* row_token, float* row_weight, int32_t* slot_row, cudaStream_t s,
-                           const TileSems* sem = nullptr, const int32_t* mtile_start = nullptr);
+                           const TileSems* sem = nullptr, const int32_t* mtile_start = nullptr,
+                           bool copy_rows = true);
 cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t* mtile_start, uint32_t* status,
                                cudaStream_t s);
 // y[t] = sum_j P[slot_row[t, j]] for t < T; p_rows = rows of P (-1: T * k).
@@ -184,6 +185,11 @@ struct FfnArgs {
     int inject;                  // MK_INJECT_STALL_GEMM1 or 0
     uint32_t* tickets;           // 2 zeroed words: tile tickets of gemm1 [0] and gemm2 [1]
     TileSems sem{};              // tile-synchronised path only (default: none)
+    // gemm1 reading its A rows straight from x (single-CTA kernel, TMA gather4):
+    // x [gather_T, d] and the source token of every dispatched row; x_perm unused
+    const bf16* gather_x = nullptr;
+    int64_t gather_T = 0;
+    const int32_t* row_token = nullptr;
 };
 // The pair kernels' swap-tile thresholds (gemm2's combine readiness needs it).
 int pair_swap_max_rows(int gemm, int k_blocks);

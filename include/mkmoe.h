@@ -115,6 +115,11 @@ typedef struct {
                               when its first tile is a gemm2 tile).
                               min(trace_cap, tasks run) records are written; the task count
                               is left in the workspace (mk_moe_layer_trace_count).          */
+    int gather_rows;       /* kernel-per-step path only, 0 = off: the dispatch writes only its
+                              index tables (no copy of x into dispatched rows) and gemm1 loads
+                              each tile's rows straight from x by their source tokens (TMA
+                              gather4, four rows per copy, single-CTA tiles).  Same bits;
+                              slower on GB300 (the gathers, not the MMAs, bound gemm1).     */
 } mk_moe_opts;
 
 #define MK_PATH_STEPS 0

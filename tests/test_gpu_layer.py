@@ -224,3 +224,22 @@ def test_layer_full_size(name, n_sample):
     del wl, y, y_f, ws, xp, rt
     gc.collect()
     torch.cuda.empty_cache()
+
+
+@pytest.mark.parametrize("name", ["ragged", "ragged_pair", "many_experts", "mid", "large"])
+def test_layer_gemm1_gathering_from_x_is_bitwise(name):
+    """gemm1 reading its rows straight from x by their source tokens (TMA
+    gather4, no dispatched copy of x) gives the same h, P and y bits as the
+    kernel-per-step path: the MMA sees the same rows."""
+    wl = Workload(name)
+    c = wl.cfg
+    y, ws = _run_layer(wl)
+    h = mk.workspace_view(ws, wl.T, c.d, c.E, c.k, c.f, "h").clone()
+    y_g = mk.mk_moe_layer(wl.g["x"], wl.g["wg"], wl.g["bias"], wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k, ws=ws,
+                          gather_rows=True)
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    assert torch.equal(mk.workspace_view(ws, wl.T, c.d, c.E, c.k, c.f, "h").view(torch.int16), h.view(torch.int16))
+    assert torch.equal(y_g.view(torch.int16), y.view(torch.int16))
+    del wl, ws, y, y_g, h
+    gc.collect()
+    torch.cuda.empty_cache()
