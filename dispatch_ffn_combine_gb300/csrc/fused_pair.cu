@@ -12,7 +12,8 @@
 // exchanges of the README's "MoE Dispatch + FFN + Combine" row become HBM
 // copies, so the mover role runs the router, the dispatch and the combine.
 //
-// GB300 layout: the kernel is launched as clusters of two CTAs on two SMs.  A
+// GB300 layout: the kernel is launched as clusters of two CTAs on two SMs, as
+// many clusters as fit on the GPU at once (all co-resident).  A
 // cluster takes one role at a time, decided by CTA 0's first thread and sent
 // to CTA 1 through distributed shared memory:
 //   mover    each CTA runs its own mover task (two tickets per decision):
@@ -1141,21 +1142,12 @@ cudaError_t launch_shape(const FMaps& maps, const FPParams& p, cudaStream_t s) {
         max_clusters[slot].store(n, std::memory_order_relaxed);
         if (dev < 64) configured[dev].store(1, std::memory_order_release);
     }
-    // every cluster co-resident (the blocks wait on one another's tasks): at
-    // most the clusters that fit at once, with a cooperative launch when the
-    // runtime accepts one with clusters
+    // every cluster co-resident (the blocks wait on one another's tasks): the grid
+    // is the number of clusters that fit at once (the runtime takes no cooperative
+    // launch with a cluster dimension; with other work on the GPU a cluster that
+    // cannot start makes the others' bounded waits run out: MK_ERR_TIMEOUT)
     const int clusters = max_clusters[slot].load(std::memory_order_relaxed);
     LaunchCfg lc(dim3(2 * clusters), dim3(kThreads), kFusedSmem, s, false, 2);
-    cudaLaunchAttribute attrs[2] = {lc.attr[0], {}};
-    attrs[1].id = cudaLaunchAttributeCooperative;
-    attrs[1].val.cooperative = 1;
-    lc.cfg.attrs = attrs;
-    lc.cfg.numAttrs = 2;
-    err = cudaLaunchKernelEx(&lc.cfg, fn, maps, p);
-    if (err == cudaSuccess) return cudaGetLastError();
-    (void)cudaGetLastError();
-    lc.cfg.attrs = lc.attr;
-    lc.cfg.numAttrs = 1;
     err = cudaLaunchKernelEx(&lc.cfg, fn, maps, p);
     if (err != cudaSuccess) return err;
     return cudaGetLastError();
