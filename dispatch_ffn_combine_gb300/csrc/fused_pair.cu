@@ -29,10 +29,12 @@
 //            TMA (cta_group::2, both CTAs' copies completing on CTA 0's
 //            barrier), warp 1 of CTA 0 issues tcgen05.mma.cta_group::2
 //            (M = 256, N = 256) into both CTAs' TMEM, warps 2-5 of each CTA
-//            run the fused epilogue; 256 x 256 tiles, an expert's partial last
-//            block as a swap tile; gemm1 tiles (pair block x 128 h columns)
-//            then gemm2 tiles (pair block x 256 output columns), claimed one
-//            ticket at a time in the stand-alone kernels' grouped order.
+//            run the fused epilogue, warp 6 of CTA 0 claims tiles and writes
+//            them into both CTAs' slot rings (warp 6 of CTA 1 relays CTA 1's
+//            slot releases); 256 x 256 tiles, an expert's partial last block as
+//            a swap tile; gemm1 tiles (pair block x 128 h columns) then gemm2
+//            tiles (pair block x 256 output columns), claimed one ticket at a
+//            time in the stand-alone kernels' grouped order.
 // Readiness (bounded waits, every one):
 //   dispatch tasks need the scans;
 //   gemm1 tiles are claimable once every dispatch task has been claimed (so
@@ -65,8 +67,13 @@ constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;  // 32 KB
 constexpr uint32_t PTX_BYTES = 2 * PSTAGE_BYTES;        // both CTAs' copies of one stage
 constexpr uint32_t PIDESC = idesc_bf16_f32(PAIR_M, MMA_N);
 constexpr int kPairNGroup = 4;
-constexpr int kSlots = 4;
-constexpr uint32_t kSlotConsumers = 10;  // CTA 0: MMA + 4 epilogue warps; CTA 1: producer + 4 epilogue warps
+constexpr int kSlots = 3;
+// Readers of a tile slot that release it on their own CTA's `slot_empty`: CTA 0
+// its producer, MMA and 4 epilogue warps, plus CTA 1's relay (one arrive for
+// CTA 1's producer and 4 epilogue warps).
+constexpr uint32_t kSlotConsumers0 = 7;
+constexpr uint32_t kSlotConsumers1 = 5;
+constexpr int kSchedWarp = 6;  // GEMM sessions: tile scheduler (CTA 0) / slot-release relay (CTA 1)
 constexpr int kCombineBufs = 8;   // tokens whose rows are in flight per CTA in the combine (at most)
 constexpr int kCombineClaim = 8;  // tokens per claim of the combine counter
 constexpr int kCombineUnit = 32;  // tokens counted as one combine task by the controller
@@ -82,6 +89,7 @@ struct PipeState {
     uint32_t pr_stage, pr_phase, pr_slot, pr_slot_phase, pr_issued, pr_last_par;
     uint32_t mm_stage, mm_phase, mm_acc, mm_acc_phase, mm_slot, mm_slot_phase;
     uint32_t ep_acc, ep_acc_phase, ep_slot, ep_slot_phase;
+    uint32_t sc_slot, sc_slot_phase;
     int role;
     int pad;
     unsigned long long last_progress;
@@ -547,44 +555,25 @@ __device__ __forceinline__ void raise_abort(FCtl* ctl, uint32_t peer) {
     st_shared_cluster_u32(mapa_shared(smem_u32(&ctl->abort_local), peer), 1u);
 }
 
-// Producer warp of both CTAs.  CTA 0's elected lane decodes and claims tiles,
-// writes each into both CTAs' slot rings and issues its copies; CTA 1 follows
-// the slots.  The first tile of the session is `first`.  Returns the number of
-// tiles the session ran (CTA 0).
-__device__ __noinline__ int gemm_producer(const FPParams& p, const FMaps& m, FCtl* ctl, uint8_t* smem, int first,
-                                          uint32_t rank) {
+// The session's pair-block table: every lane gets the layer's pair-block count;
+// with `write`, the prefix over experts of their pair blocks goes to pstart
+// (an expert with t 128-row tiles has ceil(t / 2) pair blocks).  Whole warp.
+__device__ __forceinline__ int session_table(const FPParams& p, FCtl* ctl, bool write) {
     const int lane = threadIdx.x & 31;
-    FusedSync* sync = p.sync;
-    PipeState* ps = &ctl->ps;
-    volatile uint32_t* abort_word = &ctl->abort_local;
-    const volatile uint32_t* never = &ctl->zero;
-    const bool leader = elect_one();
-    const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
-    const uint32_t peer = rank ^ 1u;
-    uint32_t stage = ps->pr_stage, phase = ps->pr_phase, slot = ps->pr_slot, slot_phase = ps->pr_slot_phase,
-             issued = ps->pr_issued, last_par = ps->pr_last_par;
-    const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);
-    const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);
-    const uint32_t peer_slot0 = mapa_shared(smem_u32(&ctl->slot[0]), peer);
-    const uint32_t peer_slot2_0 = mapa_shared(smem_u32(&ctl->slot2[0]), peer);
-    const uint32_t peer_slot_full0 = mapa_shared(smem_u32(&ctl->slot_full[0]), peer);
-    int nblocks = 0, total = 0;
-    {
-        // tile table for this session: the pair-block prefix over experts (both CTAs: CTA 0
-        // decodes tiles with it, both need the pair-block count)
-        int cnt[kMaxExperts / 32], sum = 0;
+    int cnt[kMaxExperts / 32], sum = 0;
 #pragma unroll
-        for (int i = 0; i < kMaxExperts / 32; ++i) {
-            const int e = lane * (kMaxExperts / 32) + i;
-            cnt[i] = (e < p.E) ? (p.mtile_start[e + 1] - p.mtile_start[e] + 1) / 2 : 0;
-            sum += cnt[i];
-        }
-        int inc = sum;
+    for (int i = 0; i < kMaxExperts / 32; ++i) {
+        const int e = lane * (kMaxExperts / 32) + i;
+        cnt[i] = (e < p.E) ? (p.mtile_start[e + 1] - p.mtile_start[e] + 1) / 2 : 0;
+        sum += cnt[i];
+    }
+    int inc = sum;
 #pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int u = __shfl_up_sync(0xffffffffu, inc, o);
-            if (lane >= o) inc += u;
-        }
+    for (int o = 1; o < 32; o <<= 1) {
+        const int u = __shfl_up_sync(0xffffffffu, inc, o);
+        if (lane >= o) inc += u;
+    }
+    if (write) {
         int run = inc - sum;
 #pragma unroll
         for (int i = 0; i < kMaxExperts / 32; ++i) {
@@ -593,23 +582,42 @@ __device__ __noinline__ int gemm_producer(const FPParams& p, const FMaps& m, FCt
             run += cnt[i];
         }
         if (lane == 31) ctl->pstart[p.E] = inc;
-        nblocks = __shfl_sync(0xffffffffu, inc, 31);
-        total = nblocks * (p.NT1 + p.NT2);
-        __syncwarp();
     }
-    int tile = first;
-    int tiles_run = 0;
+    __syncwarp();
+    return __shfl_sync(0xffffffffu, inc, 31);
+}
+
+// Warp 6 of both CTAs during a GEMM session.
+//   CTA 0, tile scheduler: once a slot is free, writes the next tile into both
+//   CTAs' slot rings (the peer's through distributed shared memory), then claims
+//   the one after it (one atomic ticket) unless the cluster should turn mover;
+//   the session's first tile is `first`, an end marker closes it.
+//   CTA 1, slot-release relay: once this CTA's producer and epilogue warps have
+//   read a slot, one arrive (release at cluster scope, cumulative over theirs)
+//   frees it on CTA 0.
+// Keeping both off the producers means that neither pays a ticket's round trip
+// or a cluster-scope release between two tiles' loads.
+__device__ __noinline__ void gemm_scheduler(const FPParams& p, FCtl* ctl, int first, uint32_t rank) {
+    FusedSync* sync = p.sync;
+    PipeState* ps = &ctl->ps;
+    volatile uint32_t* abort_word = &ctl->abort_local;
+    const bool leader = elect_one();
+    const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
+    const uint32_t peer = rank ^ 1u;
+    uint32_t slot = ps->sc_slot, slot_phase = ps->sc_slot_phase;
     bool ok = true;
-    bool rows_all = false, h_all = false;  // every row landed / every gemm1 tile done (seen once)
-    const uint32_t h_total = 8u * static_cast<uint32_t>(nblocks * p.NT1);  // gemm1 epilogue warps in all
-    for (;;) {
-        int4 info, info2;
-        if (rank == 0) {
-            info = make_int4(-1, 0, 0, 0);
-            info2 = make_int4(0, 0, 0, 0);
-            PTile t{};
+    if (rank == 0) {
+        const int nblocks = session_table(p, ctl, true);
+        const int total = nblocks * (p.NT1 + p.NT2);
+        const uint32_t peer_slot0 = mapa_shared(smem_u32(&ctl->slot[0]), peer);
+        const uint32_t peer_slot2_0 = mapa_shared(smem_u32(&ctl->slot2[0]), peer);
+        const uint32_t peer_slot_full0 = mapa_shared(smem_u32(&ctl->slot_full[0]), peer);
+        int tile = first;
+        for (;;) {
+            int4 info = make_int4(-1, 0, 0, 0);
+            int4 info2 = make_int4(0, 0, 0, 0);
             if (tile >= 0) {
-                t = decode_ptile(tile, ctl, p, nblocks);
+                const PTile t = decode_ptile(tile, ctl, p, nblocks);
                 info = make_int4(t.e | (t.mode << 16), t.row0, t.rows, t.n0);
                 info2 = make_int4(t.pb, t.g0, 0, 0);
             }
@@ -638,17 +646,71 @@ __device__ __noinline__ int gemm_producer(const FPParams& p, const FMaps& m, FCt
                 }
             }
             tile = __shfl_sync(0xffffffffu, next, lead);
-        } else {
-            if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase,
+            if (++slot == kSlots) {
+                slot = 0;
+                slot_phase ^= 1u;
+            }
+            if (info.x < 0) break;
+        }
+    } else {
+        const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);
+        for (;;) {
+            if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]), slot_phase,
                                                                   abort_word, p.timeout_ns))) {
                 ok = false;
                 break;
             }
-            info = ctl->slot[slot];
-            info2 = ctl->slot2[slot];
+            const int e = ctl->slot[slot].x;
             __syncwarp();
             if (leader) mbar_arrive_cluster(slot_empty0 + slot * 8u);
+            if (++slot == kSlots) {
+                slot = 0;
+                slot_phase ^= 1u;
+            }
+            if (e < 0) break;
         }
+    }
+    if (leader) {
+        if (!ok) {
+            raise_abort(ctl, peer);
+            atomicExch(&sync->abort_flag, 1u);
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+        }
+        ps->sc_slot = slot;
+        ps->sc_slot_phase = slot_phase;
+    }
+    __syncwarp();
+}
+
+// Producer warp of both CTAs: follows the slots the scheduler writes and issues
+// each tile's copies.  Returns the number of tiles the session ran.
+__device__ __noinline__ int gemm_producer(const FPParams& p, const FMaps& m, FCtl* ctl, uint8_t* smem,
+                                          uint32_t rank) {
+    FusedSync* sync = p.sync;
+    PipeState* ps = &ctl->ps;
+    volatile uint32_t* abort_word = &ctl->abort_local;
+    const volatile uint32_t* never = &ctl->zero;
+    const bool leader = elect_one();
+    const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
+    const uint32_t peer = rank ^ 1u;
+    uint32_t stage = ps->pr_stage, phase = ps->pr_phase, slot = ps->pr_slot, slot_phase = ps->pr_slot_phase,
+             issued = ps->pr_issued, last_par = ps->pr_last_par;
+    const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);
+    const int nblocks = session_table(p, ctl, false);
+    int tiles_run = 0;
+    bool ok = true;
+    bool rows_all = false, h_all = false;  // every row landed / every gemm1 tile done (seen once)
+    const uint32_t h_total = 8u * static_cast<uint32_t>(nblocks * p.NT1);  // gemm1 epilogue warps in all
+    for (;;) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase,
+                                                              abort_word, p.timeout_ns))) {
+            ok = false;
+            break;
+        }
+        const int4 info = ctl->slot[slot];
+        const int4 info2 = ctl->slot2[slot];
+        __syncwarp();
+        if (leader) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
         if (++slot == kSlots) {
             slot = 0;
             slot_phase ^= 1u;
@@ -861,7 +923,6 @@ __device__ __noinline__ void gemm_epilogue(const FPParams& p, FCtl* ctl, uint32_
     volatile uint32_t* abort_word = &ctl->abort_local;
     const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
     const int lane_in_tile = sub * 32 + lane;
-    const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);
     const uint32_t tmem_empty0 = mapa_shared(smem_u32(&ctl->tmem_empty[0]), 0);
     uint32_t acc = ps->ep_acc, acc_phase = ps->ep_acc_phase, slot = ps->ep_slot, slot_phase = ps->ep_slot_phase;
     uint32_t p_tiles = 0;
@@ -874,7 +935,7 @@ __device__ __noinline__ void gemm_epilogue(const FPParams& p, FCtl* ctl, uint32_
         const int4 info = ctl->slot[slot];
         const int4 info2 = ctl->slot2[slot];
         __syncwarp();
-        if (lane == 0) mbar_arrive_cluster(slot_empty0 + slot * 8u);
+        if (lane == 0) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
         if (++slot == kSlots) {
             slot = 0;
             slot_phase ^= 1u;
@@ -975,7 +1036,7 @@ __global__ void __launch_bounds__(kThreads, 1) fused_pair_kernel(const __grid_co
         }
         for (int i = 0; i < kSlots; ++i) {
             mbar_init(smem_u32(&ctl->slot_full[i]), 1);
-            mbar_init(smem_u32(&ctl->slot_empty[i]), kSlotConsumers);
+            mbar_init(smem_u32(&ctl->slot_empty[i]), rank == 0 ? kSlotConsumers0 : kSlotConsumers1);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         for (int i = 0; i < kCombineBufs; ++i) mbar_init(smem_u32(&ctl->cbar[i]), 1);
@@ -1058,11 +1119,13 @@ __global__ void __launch_bounds__(kThreads, 1) fused_pair_kernel(const __grid_co
             fused_combine_loop(p, ctl, smem);
         } else if (action == kActGemm) {
             if (warp == 0) {
-                gemm_tiles = gemm_producer(p, maps, ctl, smem, first_tile, rank);
+                gemm_tiles = gemm_producer(p, maps, ctl, smem, rank);
             } else if (warp == 1) {
                 if (rank == 0) gemm_mma(p, ctl, smem, tmem_base);
             } else if (warp >= 2 && warp <= 5) {
                 gemm_epilogue(p, ctl, tmem_base, rank);
+            } else if (warp == kSchedWarp) {
+                gemm_scheduler(p, ctl, first_tile, rank);
             }
         }
         __syncthreads();

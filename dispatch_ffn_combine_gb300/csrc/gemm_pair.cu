@@ -30,16 +30,17 @@
 //   copies      each CTA loads its own A and B halves with TMA; all four
 //               copies of a stage complete on CTA 0's `full` barrier, which
 //               CTA 0 arms with both CTAs' bytes.
-//   schedule    CTA 0's producer claims tiles in list order (one atomic ticket
-//               each; the list keeps an expert's tiles in groups of 4 N blocks
-//               over its pair blocks, so tiles claimed together share weight
-//               and row blocks in L2) and writes each tile into both CTAs'
-//               tile-slot rings (the peer's through distributed shared
-//               memory) one tile ahead of its own loads of that tile, so CTA
-//               1 starts a tile's loads without waiting for CTA 0 (gemm2 on
-//               the large layer: 5.13 -> 4.93 ms).  The 10 consumers of a slot (both CTAs' epilogue
-//               warps, CTA 0's MMA thread, CTA 1's producer) release it on
-//               CTA 0's barrier.
+//   schedule    a scheduler warp of CTA 0 claims tiles in list order (one
+//               atomic ticket each; the list keeps an expert's tiles in groups
+//               of 4 N blocks over its pair blocks, so tiles claimed together
+//               share weight and row blocks in L2) and writes each tile into
+//               both CTAs' tile-slot rings (the peer's through distributed
+//               shared memory).  Each CTA's slot readers release a slot on their
+//               own CTA's barrier, and a relay warp of CTA 1 passes CTA 1's
+//               release on to CTA 0, so no producer makes a cluster-scope
+//               release or waits for a ticket between two tiles' loads (each
+//               did, and the ~2 us gap drained the stage ring at every tile
+//               start: gemm2 on the large layer 4.88 -> 4.64 ms).
 //   release     the MMA commits arrive on both CTAs' `empty` and `tmem_full`
 //               barriers (multicast); the 8 epilogue warps release an
 //               accumulator on CTA 0's `tmem_empty` barrier.
@@ -64,8 +65,14 @@ constexpr uint32_t PSTAGE_BYTES = PA_BYTES + PB_BYTES;  // 32 KB
 constexpr uint32_t PTX_BYTES = 2 * PSTAGE_BYTES;        // both CTAs' copies of one stage
 constexpr uint32_t PIDESC = idesc_bf16_f32(PAIR_M, MMA_N);
 constexpr int kPairNGroup = 4;
-constexpr int kPairSlots = 4;
-constexpr uint32_t kSlotConsumers = 10;  // CTA 0: MMA + 4 epilogue warps; CTA 1: producer + 4 epilogue warps
+constexpr int kPairSlots = 3;
+constexpr int PNUM_THREADS = NUM_THREADS + 32;  // + warp 6: tile scheduler (CTA 0) / slot-release relay (CTA 1)
+constexpr int kSchedWarp = PNUM_THREADS / 32 - 1;
+// Readers of a tile slot that release it on their own CTA's `slot_empty`:
+// CTA 0 its producer, MMA and 4 epilogue warps, plus CTA 1's relay (one
+// arrive for CTA 1's producer and 4 epilogue warps).
+constexpr uint32_t kSlotConsumers0 = 7;
+constexpr uint32_t kSlotConsumers1 = 5;
 // Which partial pair blocks run as swap tiles.  Measured (same GPU, every
 // expert 256 + t rows): a swap tile costs 0.24-0.34 of a full tile for t <= 64
 // and less than the full tile it replaces up to t ~ 240 with K = 7168; with
@@ -81,9 +88,10 @@ struct PairCtl {
     uint64_t tmem_full[2];    // each CTA: accumulator complete
     uint64_t tmem_empty[2];   // CTA 0: all 8 epilogue warps have read the accumulator
     uint64_t drain;           // CTA 0: every MMA issued has completed
-    uint64_t slot_full[kPairSlots];   // each CTA: CTA 0 wrote the tile slot
-    uint64_t slot_empty[kPairSlots];  // CTA 0: the slot's 10 consumers have read it
+    uint64_t slot_full[kPairSlots];   // each CTA: the scheduler wrote the tile slot
+    uint64_t slot_empty[kPairSlots];  // each CTA: the slot's readers in this CTA have read it (CTA 0: and CTA 1's)
     int4 slot[kPairSlots];            // {e, row0, rows, n0}; e < 0 ends the list
+    int slot_tile[kPairSlots];        // the tile's index in the list
     uint32_t tmem_base;
     uint32_t abort_flag;
     uint32_t zero;
@@ -175,7 +183,7 @@ __device__ __forceinline__ void raise_abort(PairCtl* ctl, uint32_t peer) {
 }
 
 template <int MODE>  // 0: gemm1 + SwiGLU, 1: gemm2 + row weight
-__global__ void __launch_bounds__(NUM_THREADS, 1)
+__global__ void __launch_bounds__(PNUM_THREADS, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                              const __grid_constant__ CUtensorMap tmB1, const __grid_constant__ CUtensorMap tmA16,
                              const __grid_constant__ CUtensorMap tmA32, const __grid_constant__ CUtensorMap tmA64,
@@ -225,7 +233,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < kPairSlots; ++i) {
             mbar_init(smem_u32(&ctl->slot_full[i]), 1);
-            mbar_init(smem_u32(&ctl->slot_empty[i]), kSlotConsumers);
+            mbar_init(smem_u32(&ctl->slot_empty[i]), rank == 0 ? kSlotConsumers0 : kSlotConsumers1);
         }
         mbar_init(smem_u32(&ctl->drain), 1);
         ctl->abort_flag = 0;
@@ -255,79 +263,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     volatile uint32_t* abort_word = &ctl->abort_flag;
     const volatile uint32_t* never = &ctl->zero;
     const int total_tiles = ctl->pstart[p.E] * p.n_tiles;
-    const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);  // CTA 0's barriers
 
     if (warp == 0) {
         {
-            // ------------------------------------------------ claims (CTA 0) + TMA producer (both)
-            // whole warp, one elected lane claims, writes the slots, arrives and issues the copies
+            // ------------------------------------------------ TMA producer (both CTAs)
+            // whole warp, one elected lane arrives and issues the copies.  The slot is
+            // released on this CTA's own barrier: a local arrive, which does not wait for
+            // the copies in flight the way a release at cluster scope would.
             const bool leader = elect_one();
             const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
             const uint32_t full0 = mapa_shared(smem_u32(&ctl->full[0]), 0);
-            const uint32_t peer_slot0 = mapa_shared(smem_u32(&ctl->slot[0]), peer);
-            const uint32_t peer_slot_full0 = mapa_shared(smem_u32(&ctl->slot_full[0]), peer);
             const CUtensorMap* mb = (MODE == 0 && rank == 1) ? &tmB1 : &tmB0;
             uint32_t stage = 0, phase = 0, issued = 0, last_par = 0, slot = 0, slot_phase = 0;
             bool ok = true;
-            // CTA 0 takes one ticket per tile.  The leader takes the next ticket
-            // before this tile's loads and the warp reads it after them, so the
-            // atomic's round trip hides behind the loads.
-            uint32_t tk = (rank == 0 && leader) ? atomicAdd(p.ticket, 1u) : 0u;
-            // CTA 0 publishes each tile's slot one tile ahead of its own loads of that tile, so
-            // CTA 1's producer (and the MMA and epilogue roles) know the next tile while this
-            // one still loads: neither CTA waits for the other at a tile boundary.
-            int4 ahead = make_int4(-1, 0, 0, 0);  // CTA 0: the tile published last, loaded next
-            int ahead_tile = -1;
-            auto publish = [&]() -> bool {  // CTA 0: take the claimed ticket, write its slot, claim the next
-                const uint32_t tkw = __shfl_sync(0xffffffffu, tk, lead);
-                const int tile = tkw < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tkw) : -1;
-                int4 nfo = make_int4(-1, 0, 0, 0);
-                if (tile >= 0) {
-                    const PairTile ti = decode_pair_tile(tile, ctl, p);
-                    nfo = make_int4(ti.e, ti.row0, ti.rows, ti.n0);
+            while (ok) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]), slot_phase,
+                                                                      abort_word, p.timeout_ns))) {
+                    ok = false;
+                    break;
                 }
-                if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]),
-                                                                      slot_phase ^ 1u, abort_word, p.timeout_ns)))
-                    return false;
-                if (leader) {
-                    ctl->slot[slot] = nfo;
-                    st_shared_cluster_v4(peer_slot0 + slot * static_cast<uint32_t>(sizeof(int4)), nfo);
-                    mbar_arrive(smem_u32(&ctl->slot_full[slot]));
-                    mbar_arrive_cluster(peer_slot_full0 + slot * 8u);
-                    if (tile >= 0) tk = atomicAdd(p.ticket, 1u);  // read at the next publish
-                }
+                const int4 info = ctl->slot[slot];
+                const int cur_tile = ctl->slot_tile[slot];
+                __syncwarp();
+                if (leader) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
                 if (++slot == kPairSlots) {
                     slot = 0;
                     slot_phase ^= 1u;
-                }
-                ahead = nfo;
-                ahead_tile = tile;
-                return true;
-            };
-            if (rank == 0 && !publish()) ok = false;
-            while (ok) {
-                int4 info;
-                int cur_tile = -1;  // CTA 0 only: the tile's index
-                if (rank == 0) {
-                    info = ahead;
-                    cur_tile = ahead_tile;
-                    if (info.x >= 0 && !publish()) {  // the next tile's slot, before this tile's loads
-                        ok = false;
-                        break;
-                    }
-                } else {
-                    if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_full[slot]),
-                                                                          slot_phase, abort_word, p.timeout_ns))) {
-                        ok = false;
-                        break;
-                    }
-                    info = ctl->slot[slot];
-                    __syncwarp();
-                    if (leader) mbar_arrive_cluster(slot_empty0 + slot * 8u);
-                    if (++slot == kPairSlots) {
-                        slot = 0;
-                        slot_phase ^= 1u;
-                    }
                 }
                 if (info.x < 0) break;
                 if (p.wait_rows != nullptr || p.wait_h != nullptr) {
@@ -497,6 +458,76 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
         }
         __syncwarp();
+    } else if (warp == kSchedWarp) {
+        const bool leader = elect_one();
+        const int lead = __ffs(__ballot_sync(0xffffffffu, leader)) - 1;
+        uint32_t slot = 0, slot_phase = 0;
+        bool ok = true;
+        if (rank == 0) {
+            // ------------------------------------------------ tile scheduler (CTA 0)
+            // Once a slot is free: claim the next tile (one atomic ticket), decode it and
+            // write it into both CTAs' slot rings (the peer's through distributed shared
+            // memory).  Kept off the producers so that neither pays the ticket's round trip
+            // or a cluster-scope release between two tiles' loads.
+            const uint32_t peer_slot0 = mapa_shared(smem_u32(&ctl->slot[0]), peer);
+            const uint32_t peer_tile0 = mapa_shared(smem_u32(&ctl->slot_tile[0]), peer);
+            const uint32_t peer_slot_full0 = mapa_shared(smem_u32(&ctl->slot_full[0]), peer);
+            for (;;) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]),
+                                                                      slot_phase ^ 1u, abort_word, p.timeout_ns))) {
+                    ok = false;
+                    break;
+                }
+                uint32_t tk = 0;
+                if (leader) tk = atomicAdd(p.ticket, 1u);
+                tk = __shfl_sync(0xffffffffu, tk, lead);
+                const int tile = tk < static_cast<uint32_t>(total_tiles) ? static_cast<int>(tk) : -1;
+                int4 nfo = make_int4(-1, 0, 0, 0);
+                if (tile >= 0) {
+                    const PairTile ti = decode_pair_tile(tile, ctl, p);
+                    nfo = make_int4(ti.e, ti.row0, ti.rows, ti.n0);
+                }
+                if (leader) {
+                    ctl->slot[slot] = nfo;
+                    ctl->slot_tile[slot] = tile;
+                    st_shared_cluster_v4(peer_slot0 + slot * static_cast<uint32_t>(sizeof(int4)), nfo);
+                    st_shared_cluster_u32(peer_tile0 + slot * 4u, static_cast<uint32_t>(tile));
+                    mbar_arrive(smem_u32(&ctl->slot_full[slot]));
+                    mbar_arrive_cluster(peer_slot_full0 + slot * 8u);
+                }
+                __syncwarp();
+                if (++slot == kPairSlots) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+                if (tile < 0) break;
+            }
+        } else {
+            // ------------------------------------------------ slot-release relay (CTA 1)
+            // Once this CTA's producer and epilogue warps have read a slot, one arrive
+            // (release at cluster scope, cumulative over theirs) frees it on CTA 0.
+            const uint32_t slot_empty0 = mapa_shared(smem_u32(&ctl->slot_empty[0]), 0);
+            for (;;) {
+                if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]), slot_phase,
+                                                                      abort_word, p.timeout_ns))) {
+                    ok = false;
+                    break;
+                }
+                const int e = ctl->slot[slot].x;
+                __syncwarp();
+                if (leader) mbar_arrive_cluster(slot_empty0 + slot * 8u);
+                if (++slot == kPairSlots) {
+                    slot = 0;
+                    slot_phase ^= 1u;
+                }
+                if (e < 0) break;
+            }
+        }
+        if (!ok && leader) {
+            raise_abort(ctl, peer);
+            report_error(p.status, MK_ERR_TIMEOUT, kSiteGemmProducer);
+        }
+        __syncwarp();
     } else {
         // ---------------------------------------------------- epilogue (both CTAs)
         const int sub = warp & 3;  // TMEM lanes [32*sub, 32*sub+32) are this warp's
@@ -511,7 +542,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             const int4 info = ctl->slot[slot];
             __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(slot_empty0 + slot * 8u);
+            if (lane == 0) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
             if (++slot == kPairSlots) {
                 slot = 0;
                 slot_phase ^= 1u;
@@ -627,7 +658,7 @@ cudaError_t launch_pair_mode(const PairMaps& m, const PairParams& p, int64_t S, 
     attr[0].val.clusterDim.x = 2;
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
-    cfg.blockDim = dim3(NUM_THREADS);
+    cfg.blockDim = dim3(PNUM_THREADS);
     cfg.dynamicSmemBytes = PSMEM_BYTES;
     cfg.stream = s;
     cfg.attrs = attr;
