@@ -35,52 +35,103 @@ __device__ __forceinline__ float silu_mul(float g, float u) { return (g / (1.0f 
 //   weighted, C columns at tbase:  P[n0 + c] = bf16(wr * acc_c), c < C
 // A 128 x 256 single-CTA or 256 x 256 pair accumulator gives each lane
 // G = 128 (gate | up) or C = 256.
-template <int G>
-__device__ __forceinline__ void epilogue_swiglu_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
-#pragma unroll 1
-    for (int c = 0; c < G; c += 32) {
-        uint32_t g[32], u[32];
-        tmem_ld_32x32b_x32(tbase + c, g);
-        tmem_ld_32x32b_x32(tbase + G + c, u);
-        tmem_ld_wait();
-        if (row_ok) {
-            uint32_t pk[16];
+//
+// Stores: a lane holds one output row, so a plain store of 16 bytes per lane
+// touches 32 rows per warp instruction.  Each lane's 64 outputs (128 bytes, 8
+// pieces of 16 bytes) are first exchanged within groups of 8 lanes (an 8 x 8
+// transpose of pieces by three butterfly rounds of shuffles), after which a
+// warp store writes 128 contiguous bytes of each of 4 rows: 8x fewer L2 write
+// requests for the same bytes.
+
+// pk[4q .. 4q+3] is piece q of this lane's row.  Afterwards it is piece gi of
+// row (group base + q), gi = this lane's position in its group of 8.
+__device__ __forceinline__ void transpose_pieces8(uint32_t (&pk)[32], int gi) {
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                pk[q] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * q]), __uint_as_float(u[2 * q])),
-                                    silu_mul(__uint_as_float(g[2 * q + 1]), __uint_as_float(u[2 * q + 1])));
+    for (int b = 4; b >= 1; b >>= 1) {
+        const bool hi = (gi & b) != 0;
 #pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int col = n0 + c + 8 * v;
-                if (col < n_valid)
-                    *reinterpret_cast<uint4*>(orow + col) =
-                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+        for (int q0 = 0; q0 < 8; ++q0) {
+            if (q0 & b) continue;
+            const int q1 = q0 | b;
+#pragma unroll
+            for (int w = 0; w < 4; ++w) {
+                const uint32_t send = hi ? pk[4 * q0 + w] : pk[4 * q1 + w];
+                const uint32_t recv = __shfl_xor_sync(0xffffffffu, send, b);
+                if (hi)
+                    pk[4 * q0 + w] = recv;
+                else
+                    pk[4 * q1 + w] = recv;
             }
         }
+    }
+}
+
+// Stores 64 outputs per row for the warp's 32 rows after transpose_pieces8:
+// lane (8 g + gi) writes piece gi of row 8 g + s with its s-th store.
+// rows[s] is row 8 g + s's pointer, ok the rows that store (bit = lane), col
+// this lane's first column (n0 + chunk + 8 gi).
+__device__ __forceinline__ void store_pieces8(const uint32_t (&pk)[32], bf16* const (&rows)[8], uint32_t ok, int gbase,
+                                              int col, int n_valid) {
+#pragma unroll
+    for (int s = 0; s < 8; ++s)
+        if (((ok >> (gbase + s)) & 1u) && col < n_valid)
+            *reinterpret_cast<uint4*>(rows[s] + col) = make_uint4(pk[4 * s], pk[4 * s + 1], pk[4 * s + 2], pk[4 * s + 3]);
+}
+
+__device__ __forceinline__ void group_rows8(bf16* orow, bf16* (&rows)[8], int gbase) {
+    const uint64_t mine = reinterpret_cast<uint64_t>(orow);
+#pragma unroll
+    for (int s = 0; s < 8; ++s) rows[s] = reinterpret_cast<bf16*>(__shfl_sync(0xffffffffu, mine, gbase + s));
+}
+
+template <int G>
+__device__ __forceinline__ void epilogue_swiglu_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid) {
+    const int lane = threadIdx.x & 31;
+    const int gi = lane & 7, gbase = lane & ~7;
+    const uint32_t ok = __ballot_sync(0xffffffffu, row_ok);
+    bf16* rows[8];
+    group_rows8(orow, rows, gbase);
+#pragma unroll 1
+    for (int c = 0; c < G; c += 64) {
+        uint32_t pk[32];
+#pragma unroll
+        for (int half = 0; half < 2; ++half) {
+            uint32_t g[32], u[32];
+            tmem_ld_32x32b_x32(tbase + c + 32 * half, g);
+            tmem_ld_32x32b_x32(tbase + G + c + 32 * half, u);
+            tmem_ld_wait();
+#pragma unroll
+            for (int q = 0; q < 16; ++q)
+                pk[16 * half + q] = pack_bf16x2(silu_mul(__uint_as_float(g[2 * q]), __uint_as_float(u[2 * q])),
+                                                silu_mul(__uint_as_float(g[2 * q + 1]), __uint_as_float(u[2 * q + 1])));
+        }
+        transpose_pieces8(pk, gi);
+        store_pieces8(pk, rows, ok, gbase, n0 + c + 8 * gi, n_valid);
     }
 }
 
 template <int C>
 __device__ __forceinline__ void epilogue_weighted_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
                                                     float wr) {
+    const int lane = threadIdx.x & 31;
+    const int gi = lane & 7, gbase = lane & ~7;
+    const uint32_t ok = __ballot_sync(0xffffffffu, row_ok);
+    bf16* rows[8];
+    group_rows8(orow, rows, gbase);
 #pragma unroll 1
-    for (int c = 0; c < C; c += 32) {
-        uint32_t a[32];
+    for (int c = 0; c < C; c += 64) {
+        uint32_t a[32], b[32];
         tmem_ld_32x32b_x32(tbase + c, a);
+        tmem_ld_32x32b_x32(tbase + c + 32, b);
         tmem_ld_wait();
-        if (row_ok) {
-            uint32_t pk[16];
+        uint32_t pk[32];
 #pragma unroll
-            for (int q = 0; q < 16; ++q)
-                pk[q] = pack_bf16x2(__uint_as_float(a[2 * q]) * wr, __uint_as_float(a[2 * q + 1]) * wr);
-#pragma unroll
-            for (int v = 0; v < 4; ++v) {
-                const int col = n0 + c + 8 * v;
-                if (col < n_valid)
-                    *reinterpret_cast<uint4*>(orow + col) =
-                        make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
-            }
+        for (int q = 0; q < 16; ++q) {
+            pk[q] = pack_bf16x2(__uint_as_float(a[2 * q]) * wr, __uint_as_float(a[2 * q + 1]) * wr);
+            pk[16 + q] = pack_bf16x2(__uint_as_float(b[2 * q]) * wr, __uint_as_float(b[2 * q + 1]) * wr);
         }
+        transpose_pieces8(pk, gi);
+        store_pieces8(pk, rows, ok, gbase, n0 + c + 8 * gi, n_valid);
     }
 }
 
