@@ -213,20 +213,28 @@ def roofline(work: dict, ms: float, peaks: dict) -> dict:
     return roof
 
 
-def traffic_record(kernel: str, cfg_name: str):
-    """DRAM bytes per launch from a committed ncu summary, only while the kernel
-    source is unchanged since the counters were taken (else None)."""
-    path = os.path.join(ROOT, "profiles", "traffic.json")
+def sources_digest(names) -> str:
+    """First 16 hex digits of the SHA-256 over the named csrc files, in order."""
+    h = hashlib.sha256()
+    for name in names:
+        with open(os.path.join(ROOT, "dispatch_ffn_combine_gb300", "csrc", name), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel: str, cfg_name: str, path: str | None = None):
+    """DRAM bytes per launch from a committed ncu summary, only while every
+    source file the kernel is built from is unchanged since the counters were
+    taken (else None)."""
+    path = path or os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as fh:
         rec = json.load(fh).get(kernel, {}).get(cfg_name)
-    if not rec:
+    if not rec or "sources" not in rec:
         return None
-    src = os.path.join(ROOT, "dispatch_ffn_combine_gb300", "csrc", rec["source"])
-    with open(src, "rb") as fh:
-        if hashlib.sha256(fh.read()).hexdigest()[:16] != rec["sha256_16"]:
-            return None
+    if sources_digest(rec["sources"]) != rec["sha256_16"]:
+        return None
     return rec["dram_bytes_per_launch"]
 
 
@@ -350,6 +358,7 @@ def time_layer(mk, cfg, inp, ws, y, stream, path, mover_ctas, steps, warmup, scr
 
 
 PATH_KEYS = {1: "fused_layer", 2: "tiles_layer"}
+ALT_ROUNDS, ALT_STEPS = 5, 8  # the alternating comparison of the three paths
 PATH_NAMES = {0: "one kernel per step", 1: "fused persistent kernel",
               2: "kernel per step, tile semaphores and programmatic dependent launch"}
 
@@ -469,6 +478,14 @@ def run_ours(args):
                                               scrub=scrub)
         others[other] = (max_over_ranks(other_total, dev, dist) / args.steps, other_phase)
 
+    # ---- the three paths once more, alternating in rounds so that no path is
+    # measured only at a later (warmer, slower-clocked) time than another
+    alt = {o: [] for o in (mk.MK_PATH_STEPS, mk.MK_PATH_FUSED, mk.MK_PATH_TILES)}
+    for _ in range(ALT_ROUNDS):
+        for o in alt:
+            t, _ = time_layer(mk, cfg, inp, ws, y, stream, o, 0, ALT_STEPS, 1, scrub=scrub)
+            alt[o].append(max_over_ranks(t, dev, dist) / ALT_STEPS)
+
     if rank != 0:
         if dist:
             tdist.destroy_process_group()
@@ -521,6 +538,10 @@ def run_ours(args):
                          "unit": "tokens/s", "roofline": dominant_roofline(fb, ph, o, peaks)}
                         for o, (ms, ph) in others.items()],
         "other_paths_note": "same inputs and timing rules, measured after the main run; not the headline",
+        "paths_alternating": {
+            "rounds": ALT_ROUNDS, "steps_per_round": ALT_STEPS,
+            "median_ms_per_step": {PATH_NAMES[o]: statistics.median(v) for o, v in alt.items()},
+            "note": "each round times the three paths back to back on the same inputs, one warm-up step each"},
         "configs": configs,
         "clocks": clk,
         "peaks": {k: peaks.get(k) for k in ("hbm_gbs", "bf16_tflops", "bf16_tflops_sustained", "source")},

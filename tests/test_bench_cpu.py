@@ -62,3 +62,22 @@ def test_roofline_without_a_sustained_figure():
     peaks = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
     r = bench.roofline({"flops": 1e12, "bytes": 1e9}, 1.0, peaks)
     assert r["bound"] == "tensor" and r["peak"] == 1900.0 and "sustained" not in r
+
+
+def test_traffic_record_needs_every_source_unchanged(tmp_path):
+    # The record is used only while the digest over all of its source files
+    # matches; a record naming one file too few, or a changed file, reads None.
+    import json
+
+    srcs = ["gemm_pair.cu", "gemm_impl.cuh", "mk_device.cuh", "mk_internal.h"]
+    rec = {"sources": srcs, "sha256_16": bench.sources_digest(srcs), "dram_bytes_per_launch": 123}
+    path = tmp_path / "traffic.json"
+    path.write_text(json.dumps({"gemm1": {"large": rec}}))
+    assert bench.traffic_record("gemm1", "large", str(path)) == 123
+    assert bench.traffic_record("gemm2", "large", str(path)) is None
+    stale = dict(rec, sha256_16=bench.sources_digest(srcs[:1]))
+    path.write_text(json.dumps({"gemm1": {"large": stale}}))
+    assert bench.traffic_record("gemm1", "large", str(path)) is None
+    legacy = {"source": "gemm_pair.cu", "sha256_16": "0" * 16, "dram_bytes_per_launch": 1}
+    path.write_text(json.dumps({"gemm1": {"large": legacy}}))
+    assert bench.traffic_record("gemm1", "large", str(path)) is None
