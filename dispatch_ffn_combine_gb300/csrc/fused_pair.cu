@@ -74,6 +74,7 @@ constexpr int kSlots = 3;
 constexpr uint32_t kSlotConsumers0 = 7;
 constexpr uint32_t kSlotConsumers1 = 5;
 constexpr int kSchedWarp = 6;  // GEMM sessions: tile scheduler (CTA 0) / slot-release relay (CTA 1)
+constexpr uint32_t kEpiPacePerKb = 80;  // gemm2's epilogue chunk spacing per k-block, as in gemm_pair.cu
 constexpr int kCombineBufs = 8;   // tokens whose rows are in flight per CTA in the combine (at most)
 constexpr int kCombineClaim = 8;  // tokens per claim of the combine counter
 constexpr int kCombineUnit = 32;  // tokens counted as one combine task by the controller
@@ -106,7 +107,7 @@ struct FCtl {
     uint64_t slot_full[kSlots];
     uint64_t slot_empty[kSlots];
     int4 slot[kSlots];   // {e | mode << 16 (-1: end of session), row0, rows, n0}
-    int4 slot2[kSlots];  // {pair block index, first M-tile index, 0, 0}
+    int4 slot2[kSlots];  // {pair block index, first M-tile index, more tiles follow, 0}
     PipeState ps;
     int32_t pstart[kMaxExperts + 1];  // CTA 0, per session: prefix over experts of their pair blocks
     uint32_t tmem_base;
@@ -619,7 +620,9 @@ __device__ __noinline__ void gemm_scheduler(const FPParams& p, FCtl* ctl, int fi
             if (tile >= 0) {
                 const PTile t = decode_ptile(tile, ctl, p, nblocks);
                 info = make_int4(t.e | (t.mode << 16), t.row0, t.rows, t.n0);
-                info2 = make_int4(t.pb, t.g0, 0, 0);
+                // z: more tiles follow than the clusters can hold at once (gemm2's epilogue paces
+                // its stores only then)
+                info2 = make_int4(t.pb, t.g0, tile + static_cast<int>(gridDim.x / 2) < total ? 1 : 0, 0);
             }
             if (!__all_sync(0xffffffffu, mbar_wait_bounded_cluster(smem_u32(&ctl->slot_empty[slot]), slot_phase ^ 1u,
                                                                   abort_word, p.timeout_ns))) {
@@ -971,7 +974,8 @@ __device__ __noinline__ void gemm_epilogue(const FPParams& p, FCtl* ctl, uint32_
                 epilogue_swiglu(tbase, row_ok, orow, info.w, n_valid);
             } else {
                 const float wr = row_ok ? p.row_weight[r] : 1.0f;
-                epilogue_weighted(tbase, row_ok, orow, info.w, n_valid, wr);
+                epilogue_weighted(tbase, row_ok, orow, info.w, n_valid, wr,
+                                  info2.z != 0 ? static_cast<uint32_t>(p.kb2) * kEpiPacePerKb : 0u);
             }
         }
         tc_fence_before();

@@ -110,16 +110,23 @@ __device__ __forceinline__ void epilogue_swiglu_w(uint32_t tbase, bool row_ok, b
     }
 }
 
+// `pace` (SM cycles, 0: none) spaces the starts of the 64-column chunks at
+// least that far apart, so that a tile's stores spread over the next tile's
+// main loop instead of landing in a burst while its first operand loads are
+// in flight (gemm2's output is 4x its operand bytes per tile).
 template <int C>
 __device__ __forceinline__ void epilogue_weighted_w(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
-                                                    float wr) {
+                                                    float wr, uint32_t pace = 0) {
     const int lane = threadIdx.x & 31;
     const int gi = lane & 7, gbase = lane & ~7;
     const uint32_t ok = __ballot_sync(0xffffffffu, row_ok);
     bf16* rows[8];
     group_rows8(orow, rows, gbase);
+    const long long t0 = clock64();
 #pragma unroll 1
     for (int c = 0; c < C; c += 64) {
+        if (pace != 0u && c != 0)
+            while (clock64() - t0 < static_cast<long long>(c / 64) * pace) __nanosleep(128);
         uint32_t a[32], b[32];
         tmem_ld_32x32b_x32(tbase + c, a);
         tmem_ld_32x32b_x32(tbase + c + 32, b);
@@ -140,8 +147,8 @@ __device__ __forceinline__ void epilogue_swiglu(uint32_t tbase, bool row_ok, bf1
 }
 
 __device__ __forceinline__ void epilogue_weighted(uint32_t tbase, bool row_ok, bf16* orow, int n0, int n_valid,
-                                                  float wr) {
-    epilogue_weighted_w<MMA_N>(tbase, row_ok, orow, n0, n_valid, wr);
+                                                  float wr, uint32_t pace = 0) {
+    epilogue_weighted_w<MMA_N>(tbase, row_ok, orow, n0, n_valid, wr, pace);
 }
 
 constexpr int PAIR_M = 2 * BM;  // rows of a CTA-pair tile

@@ -81,6 +81,14 @@ constexpr uint32_t kSlotConsumers1 = 5;
 // k-block against a short main loop), gemm2's none.
 constexpr int kSwapMaxRows = PAIR_M - 1;
 constexpr int kSwapMaxRowsShortK = BM;  // gemm1 with K < 64 k-blocks
+// gemm2's full-tile epilogue spaces its four 64-column chunks by this many SM
+// cycles per k-block of the tile (a k-block is 512 cycles of MMA work, so the
+// chunks spread over ~60 % of the next tile's main loop).  Measured on the
+// large layer: the MMA issuer's long operand waits at k-blocks 8-15 of a tile,
+// where the previous tile's stores used to land in one burst, fell from 5.6 %
+// to 1.9 % of its cycles (spacing 100), and gemm2 took 4.48-4.50 ms instead of
+// 4.57-4.61 (spacing 80; 100: 4.53-4.56, 120: 4.56-4.61).
+constexpr uint32_t kEpiPacePerKb = 80;
 
 struct PairCtl {
     uint64_t full[PSTAGES];   // CTA 0: both CTAs' copies of the stage landed
@@ -541,6 +549,7 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
                 break;
             }
             const int4 info = ctl->slot[slot];
+            const int tile_index = ctl->slot_tile[slot];
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&ctl->slot_empty[slot]));
             if (++slot == kPairSlots) {
@@ -586,7 +595,10 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
                     epilogue_swiglu(tbase, row_ok, orow, info.w, p.n_valid);
                 } else {
                     const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
-                    epilogue_weighted(tbase, row_ok, orow, info.w, p.n_valid, wr);
+                    // paced over ~80 % of a full tile's MMA cycles while more tiles follow
+                    const bool more = tile_index + static_cast<int>(gridDim.x / 2) < total_tiles;
+                    const uint32_t pace = more ? static_cast<uint32_t>(p.k_blocks) * kEpiPacePerKb : 0u;
+                    epilogue_weighted(tbase, row_ok, orow, info.w, p.n_valid, wr, pace);
                 }
             }
             tc_fence_before();
