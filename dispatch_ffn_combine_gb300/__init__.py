@@ -33,7 +33,8 @@ PHASES = ("route_logits", "topk", "count", "scan", "scatter", "gemm1", "gemm2", 
 # Every entry point the header declares (checked against the library's exports).
 ENTRY_POINTS = (
     "mk_moe_workspace_size", "mk_moe_route", "mk_moe_dispatch", "mk_moe_expert_ffn", "mk_moe_combine",
-    "mk_moe_layer", "mk_moe_layer_host", "mk_moe_last_device_error", "mk_moe_status_string",
+    "mk_moe_layer", "mk_moe_layer_host", "mk_moe_layer_host_async", "mk_moe_last_device_error",
+    "mk_moe_status_string",
     "mk_moe_layer_routing", "mk_moe_route_noalloc", "mk_moe_layer_trace_count", "mk_moe_route_fallbacks",
     "mk_moe_grouped_gemm", "mk_moe_dispatch_gemm_workspace_size", "mk_moe_dispatch_gemm",
     "mk_moe_route_approx_logits", "mk_moe_workspace_region", "mk_moe_ep_regroup_workspace_size",
@@ -85,6 +86,7 @@ def load_library():
         lib.mk_moe_combine.argtypes = [P, P, I64, I, I, P, P]
         lib.mk_moe_layer.argtypes = [P, P, P, P, P, P, I64, I, I, I, I, P, P, SZ, ctypes.POINTER(MkMoeOpts), P]
         lib.mk_moe_layer_host.argtypes = lib.mk_moe_layer.argtypes
+        lib.mk_moe_layer_host_async.argtypes = lib.mk_moe_layer.argtypes + [P]
         lib.mk_moe_last_device_error.argtypes = [P, P, ctypes.POINTER(ctypes.c_uint32)]
         lib.mk_moe_layer_routing.argtypes = [P, I64, I, I, I, I, P, P, P, P, P]
         lib.mk_moe_route_noalloc.argtypes = [P, P, P, I64, I, I, I, P, P, P, P]
@@ -373,6 +375,24 @@ def mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, k, y_host, ws, phase_events=
                                           _p(y_host), _p(ws), ws.numel(),
                                           _opts(phase_events, timeout_ns, 0, path, mover_ctas), _stream(stream))
     _check(st, "mk_moe_layer_host")
+    return y_host
+
+
+def mk_moe_layer_host_async(x_host, wg, bias, w1, w3, w2, k, y_host, ws, y_ready, phase_events=None, timeout_ns=0,
+                            stream=None, path=MK_PATH_STEPS, mover_ctas=0):
+    """The layer on host buffers with y's download off `stream`: y_ready (a
+    torch.cuda.Event) is recorded once y_host holds the output; wait for it
+    before reading y_host."""
+    T, d, E, f = _layer_shapes(x_host, wg, bias, w1, w3, w2, device=False)
+    _need(y_host, torch.bfloat16, (T, d), "y_host", device=False)
+    s = torch.cuda.current_stream() if stream is None else stream
+    if y_ready.cuda_event == 0:  # torch creates the event on its first record
+        y_ready.record(s)
+    st = load_library().mk_moe_layer_host_async(_p(x_host), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k,
+                                                f, _p(y_host), _p(ws), ws.numel(),
+                                                _opts(phase_events, timeout_ns, 0, path, mover_ctas),
+                                                ctypes.c_void_p(s.cuda_stream), ctypes.c_void_p(y_ready.cuda_event))
+    _check(st, "mk_moe_layer_host_async")
     return y_host
 
 

@@ -798,6 +798,56 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     return MK_OK;
 }
 
+mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, const float* bias, const void* w1,
+                                  const void* w3, const void* w2, int64_t T, int d, int E, int k, int ffn,
+                                  void* y_host, void* ws, size_t ws_bytes, const mk_moe_opts* opts, void* stream,
+                                  void* y_ready) {
+    if (y_ready == nullptr) return MK_ERR_INVALID_ARG;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    cudaEvent_t done = static_cast<cudaEvent_t>(y_ready);
+    if (T == 0 && check_sizes(T, d, E, k, ffn) == MK_OK) {
+        MK_TRY(cudaEventRecord(done, s));
+        return MK_OK;
+    }
+    mk_status st = validate_layer(x_host, wg, w1, w3, w2, T, d, E, k, ffn, y_host, ws, ws_bytes, opts, false);
+    if (st != MK_OK) return st;
+    if (opts && opts->path != MK_PATH_STEPS) {
+        st = mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, T, d, E, k, ffn, y_host, ws, ws_bytes, opts, stream);
+        if (st != MK_OK) return st;
+        MK_TRY(cudaEventRecord(done, s));
+        return MK_OK;
+    }
+    const WsLayout L = ws_layout(T, d, E, k, ffn);
+    const size_t bytes = static_cast<size_t>(T) * d * 2;
+    bf16* xd = at<bf16>(ws, L.x_stage);
+    bf16* yd = at<bf16>(ws, L.y_stage);
+    HostPipe* hp = nullptr;
+    MK_TRY(get_pipe(ws, &hp));
+    // upload of x as in mk_moe_layer_host: after the previous call's scatter
+    MK_TRY(cudaStreamWaitEvent(hp->h2d, hp->x_free, 0));
+    MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
+    MK_TRY(cudaEventRecord(hp->x_ready, hp->h2d));
+    MK_TRY(cudaStreamWaitEvent(s, hp->x_ready, 0));
+    LayerHooks hk;
+    hk.after_scatter = hp->x_free;
+    hk.skip_combine = true;
+    st = layer_impl(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, L, opts, s, hk);
+    if (st != MK_OK) return st;
+    // the staged y is rewritten only after every earlier download from it
+    for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+    MK_TRY(launch_combine(at<bf16>(ws, L.P), at<int32_t>(ws, L.slot_row), T, d, k, yd, s));
+    if (opts && opts->phase_events && opts->phase_events[MK_PHASE_COUNT_ALL])
+        MK_TRY(cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[MK_PHASE_COUNT_ALL]), s));
+    MK_TRY(cudaEventRecord(hp->y_ready[0], s));
+    // one download by the copy engine, off `stream`
+    cudaStream_t q = hp->d2h[0];
+    MK_TRY(cudaStreamWaitEvent(q, hp->y_ready[0], 0));
+    MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, q));
+    MK_TRY(cudaEventRecord(hp->y_done[0], q));
+    MK_TRY(cudaEventRecord(done, q));
+    return MK_OK;
+}
+
 
 
 mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail) {

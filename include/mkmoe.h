@@ -285,6 +285,29 @@ MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const fl
                             void* y_host, void* ws, size_t ws_bytes,
                             const mk_moe_opts* opts, void* stream);
 
+/* The layer on HOST buffers for a stream of batches (same operation, inputs
+ * and layouts as mk_moe_layer_host), with the output's download left off
+ * `stream`: the combine writes y into a staging region of `ws`, the copy
+ * engine downloads it into y_host on the workspace's copy stream, and the
+ * event `y_ready` (a cudaEvent_t created by the caller, passed as void*) is
+ * recorded there once y_host holds the output.  `stream` itself does not wait
+ * for the download, so work enqueued on it after this call -- typically the
+ * next batch's call on the same workspace -- runs while y is still crossing
+ * the host link.  The caller waits for `y_ready` (cudaEventSynchronize, or
+ * cudaStreamWaitEvent) before reading y_host, and does not overwrite y_host
+ * before then.  x_host is read as for mk_moe_layer_host (its upload may start
+ * before earlier work on `stream`; keep it unchanged until `y_ready`).  The
+ * next call's combine on the same workspace waits for this download.  On the
+ * fused and tile-synchronised paths the call runs as mk_moe_layer_host and
+ * records `y_ready` on `stream`.  Errors as mk_moe_layer_host, plus
+ * MK_ERR_INVALID_ARG for a NULL y_ready.  The paper has no host-buffer entry
+ * point; this one is for serving loops that feed batches back to back. */
+MK_API mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, const float* bias,
+                                  const void* w1, const void* w3, const void* w2,
+                                  int64_t T, int d, int E, int k, int ffn,
+                                  void* y_host, void* ws, size_t ws_bytes,
+                                  const mk_moe_opts* opts, void* stream, void* y_ready);
+
 /* Synchronises `stream`, then returns and clears the device-side status of
  * `ws` (MK_OK if no device error).  *detail (may be NULL) receives the site
  * code of the error. */

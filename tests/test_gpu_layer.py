@@ -117,6 +117,58 @@ def test_layer_host_calls_back_to_back(T):
         assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
 
 
+@pytest.mark.parametrize("T", [7, 1000])
+def test_layer_host_async_back_to_back(T):
+    """The pipelined host entry point issued back to back on one workspace,
+    interleaved with the blocking one and the fused path, each output its
+    own y_host and event: once its event has completed, every y_host equals
+    the device-buffer result for its own input; the stream never waited for
+    the downloads of the async calls."""
+    wl = Workload("ragged", T=T)
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    g = torch.Generator().manual_seed(11)
+    xs = [wl.g["x"].cpu()] + [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(4)]
+    xs_host = [x.pin_memory() for x in xs]
+    ys_host = [torch.full((wl.T, c.d), -1.0, dtype=torch.bfloat16).pin_memory() for _ in xs]
+    kinds = ["async", "async", "blocking", "async_fused", "async"]
+    args = (wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
+    events = []
+    for xh, yh, kind in zip(xs_host, ys_host, kinds):
+        if kind == "blocking":
+            mk.mk_moe_layer_host(xh, *args, yh, ws)
+            events.append(None)
+        else:
+            ev = torch.cuda.Event()
+            path = mk.MK_PATH_FUSED if kind == "async_fused" else mk.MK_PATH_STEPS
+            mk.mk_moe_layer_host_async(xh, *args, yh, ws, ev, path=path)
+            events.append(ev)
+    for ev in events:
+        if ev is not None:
+            ev.synchronize()
+    torch.cuda.synchronize()
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    ws2 = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    for x, yh in zip(xs, ys_host):
+        y_dev = mk.mk_moe_layer(x.to(wl.dev), *args, ws=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+
+def test_layer_host_async_needs_an_event():
+    wl = Workload("tiny")
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    x_host = wl.g["x"].cpu().pin_memory()
+    y_host = torch.empty((wl.T, c.d), dtype=torch.bfloat16).pin_memory()
+    lib = mk.load_library()
+    import ctypes
+    st = lib.mk_moe_layer_host_async(mk._p(x_host), mk._p(wl.g["wg"]), None, mk._p(wl.g["w1"]), mk._p(wl.g["w3"]),
+                                     mk._p(wl.g["w2"]), wl.T, c.d, c.E, c.k, c.f, mk._p(y_host), mk._p(ws),
+                                     ws.numel(), None, ctypes.c_void_p(torch.cuda.current_stream().cuda_stream), None)
+    assert st == mk.MK_ERR_INVALID_ARG
+
+
 def test_layer_route_fallback_path_is_exact():
     """With the candidate filter's bound forced to zero, (almost) every token
     takes the exact fallback (all E logits in the fixed order): the layer's
