@@ -75,6 +75,7 @@ constexpr uint32_t kSlotConsumers0 = 7;
 constexpr uint32_t kSlotConsumers1 = 5;
 constexpr int kSchedWarp = 6;  // GEMM sessions: tile scheduler (CTA 0) / slot-release relay (CTA 1)
 constexpr uint32_t kEpiPacePerKb = 80;  // gemm2's epilogue chunk spacing per k-block, as in gemm_pair.cu
+constexpr int kEpiPaceMaxKb = 64;       // ... for K below this many k-blocks only
 constexpr int kCombineBufs = 8;   // tokens whose rows are in flight per CTA in the combine (at most)
 constexpr int kCombineClaim = 8;  // tokens per claim of the combine counter
 constexpr int kCombineUnit = 32;  // tokens counted as one combine task by the controller
@@ -974,8 +975,9 @@ __device__ __noinline__ void gemm_epilogue(const FPParams& p, FCtl* ctl, uint32_
                 epilogue_swiglu(tbase, row_ok, orow, info.w, n_valid);
             } else {
                 const float wr = row_ok ? p.row_weight[r] : 1.0f;
+                const bool pace = info2.z != 0 && p.kb2 < kEpiPaceMaxKb;
                 epilogue_weighted(tbase, row_ok, orow, info.w, n_valid, wr,
-                                  info2.z != 0 ? static_cast<uint32_t>(p.kb2) * kEpiPacePerKb : 0u);
+                                  pace ? static_cast<uint32_t>(p.kb2) * kEpiPacePerKb : 0u);
             }
         }
         tc_fence_before();

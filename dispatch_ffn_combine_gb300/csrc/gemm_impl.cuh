@@ -75,7 +75,8 @@ __device__ __forceinline__ void store_pieces8(const uint32_t (&pk)[32], bf16* co
 #pragma unroll
     for (int s = 0; s < 8; ++s)
         if (((ok >> (gbase + s)) & 1u) && col < n_valid)
-            *reinterpret_cast<uint4*>(rows[s] + col) = make_uint4(pk[4 * s], pk[4 * s + 1], pk[4 * s + 2], pk[4 * s + 3]);
+            *reinterpret_cast<uint4*>(rows[s] + col) =
+                make_uint4(pk[4 * s], pk[4 * s + 1], pk[4 * s + 2], pk[4 * s + 3]);
 }
 
 __device__ __forceinline__ void group_rows8(bf16* orow, bf16* (&rows)[8], int gbase) {

@@ -87,8 +87,13 @@ constexpr int kSwapMaxRowsShortK = BM;  // gemm1 with K < 64 k-blocks
 // large layer: the MMA issuer's long operand waits at k-blocks 8-15 of a tile,
 // where the previous tile's stores used to land in one burst, fell from 5.6 %
 // to 1.9 % of its cycles (spacing 100), and gemm2 took 4.48-4.50 ms instead of
-// 4.57-4.61 (spacing 80; 100: 4.53-4.56, 120: 4.56-4.61).
+// 4.57-4.61 (spacing 80; 100: 4.53-4.56, 120: 4.56-4.61).  Only for short K
+// (fewer than kEpiPaceMaxKb k-blocks), where a tile's output is a large share
+// of its traffic: the Dispatch + GEMM kernel's K = 7168 tiles ran 2-4 % slower
+// paced (their stores are a quarter as dense, and pacing holds the accumulator
+// longer ahead of short swap tiles).
 constexpr uint32_t kEpiPacePerKb = 80;
+constexpr int kEpiPaceMaxKb = 64;
 
 struct PairCtl {
     uint64_t full[PSTAGES];   // CTA 0: both CTAs' copies of the stage landed
@@ -596,7 +601,8 @@ __global__ void __launch_bounds__(PNUM_THREADS, 1)
                 } else {
                     const float wr = (row_ok && p.row_weight != nullptr) ? p.row_weight[r] : 1.0f;
                     // paced over ~80 % of a full tile's MMA cycles while more tiles follow
-                    const bool more = tile_index + static_cast<int>(gridDim.x / 2) < total_tiles;
+                    const bool more = tile_index + static_cast<int>(gridDim.x / 2) < total_tiles &&
+                                      p.k_blocks < kEpiPaceMaxKb;
                     const uint32_t pace = more ? static_cast<uint32_t>(p.k_blocks) * kEpiPacePerKb : 0u;
                     epilogue_weighted(tbase, row_ok, orow, info.w, p.n_valid, wr, pace);
                 }
