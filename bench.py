@@ -465,6 +465,15 @@ def run_ours(args):
         e2e_step(i)
     for ev in y_evs:
         ev.synchronize()
+    # the host link's copy rates into and out of these pinned buffers, for the record
+    link = {}
+    for name, dst, src in (("h2d", y, x_host), ("d2h", y_hosts[0], y)):
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c0.record(stream)
+        dst.copy_(src, non_blocking=True)
+        c1.record(stream)
+        torch.cuda.synchronize()
+        link[name] = src.numel() * src.element_size() / (c0.elapsed_time(c1) / 1e3) / 1e9
     e2e_clocks = ClockSampler(local)
     e2e_clocks.start()
     torch.cuda.synchronize()
@@ -549,7 +558,8 @@ def run_ours(args):
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2, "entry_point": "mk_moe_layer_host_async",
                 "note": "each step's y download overlaps the next step's kernels; every download is inside "
-                        "the timed region", "clocks": e2e_clk},
+                        "the timed region", "clocks": e2e_clk,
+                "host_link_gbs": {k: round(v, 1) for k, v in link.items()}},
         "gpu_launches": launches_per_step(cfg, args.path) * args.steps,
         "path": PATH_NAMES[args.path],
         "mover_ctas": args.mover_ctas,
