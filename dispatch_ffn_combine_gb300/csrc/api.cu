@@ -52,6 +52,7 @@ WsLayout make_layout(int64_t T, int d, int E, int k, int f, bool full) {
     L.tile_sems = take(tile_sems_bytes(static_cast<int64_t>(S), E));
     L.x_stage = take(static_cast<size_t>(T) * d * 2);
     L.y_stage = take(static_cast<size_t>(T) * d * 2);
+    L.y_stage2 = take(static_cast<size_t>(T) * d * 2);
     L.total = o;
     return L;
 }
@@ -601,6 +602,7 @@ mk_status validate_layer(const void* x, const float* wg, const void* w1, const v
 // recently used replaced after its copies have drained).
 constexpr int kHostChunks = 8;
 constexpr int kHostPipes = 8;
+constexpr int kCopyOutCtas = 16;  // CTAs of the pipelined entry point's download kernel
 
 struct HostPipe {
     int dev = -1;
@@ -611,6 +613,8 @@ struct HostPipe {
     cudaEvent_t x_ready = nullptr;              // staged x uploaded
     cudaEvent_t y_ready[kHostChunks] = {};      // combine of output chunk c done
     cudaEvent_t y_done[kHostChunks] = {};       // download of output chunk c done
+    uint32_t async_calls = 0;                   // pipelined calls so far: they alternate two staging regions
+    cudaEvent_t y_async_done[2] = {};           // download of the last pipelined call from region r done
 };
 
 std::mutex g_pipe_mu;
@@ -628,6 +632,8 @@ void release_pipe(HostPipe& p) {
         if (p.y_ready[c]) cudaEventDestroy(p.y_ready[c]);
         if (p.y_done[c]) cudaEventDestroy(p.y_done[c]);
     }
+    for (cudaEvent_t e : p.y_async_done)
+        if (e) cudaEventDestroy(e);
     if (p.h2d) cudaStreamDestroy(p.h2d);
     for (cudaStream_t q : p.d2h)
         if (q) cudaStreamDestroy(q);
@@ -660,6 +666,8 @@ cudaError_t get_pipe(const void* ws, HostPipe** out) {
         if ((err = cudaEventCreateWithFlags(&p.y_ready[c], ef)) != cudaSuccess) return err;
         if ((err = cudaEventCreateWithFlags(&p.y_done[c], ef)) != cudaSuccess) return err;
     }
+    for (cudaEvent_t& e : p.y_async_done)
+        if ((err = cudaEventCreateWithFlags(&e, ef)) != cudaSuccess) return err;
     p.dev = dev;
     p.ws = ws;
     p.used = ++g_pipe_clock;
@@ -731,6 +739,7 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
         // earlier call's use of the staging buffers and before any later one
         MK_TRY(cudaStreamWaitEvent(s, hp->x_free, 0));
         for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+        MK_TRY(cudaStreamWaitEvent(s, hp->y_async_done[0], 0));
         MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, s));
         st = layer_impl(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, L, opts, s, LayerHooks{});
         if (st != MK_OK) return st;
@@ -777,6 +786,7 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     // the staged y is rewritten only after every download of an earlier call
     // (which may have cut it into other chunks) has finished
     for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+    MK_TRY(cudaStreamWaitEvent(s, hp->y_async_done[0], 0));
     int last = -1;
     for (int c = 0; c < chunks; ++c) {
         const int64_t t0 = c * tc;
@@ -820,9 +830,12 @@ mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, const flo
     const WsLayout L = ws_layout(T, d, E, k, ffn);
     const size_t bytes = static_cast<size_t>(T) * d * 2;
     bf16* xd = at<bf16>(ws, L.x_stage);
-    bf16* yd = at<bf16>(ws, L.y_stage);
     HostPipe* hp = nullptr;
     MK_TRY(get_pipe(ws, &hp));
+    // consecutive pipelined calls stage y in alternate regions, so a call's
+    // combine waits only for the download two calls back
+    const int r = static_cast<int>(hp->async_calls++ & 1u);
+    bf16* yd = at<bf16>(ws, r ? L.y_stage2 : L.y_stage);
     // upload of x as in mk_moe_layer_host: after the previous call's scatter
     MK_TRY(cudaStreamWaitEvent(hp->h2d, hp->x_free, 0));
     MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
@@ -834,16 +847,28 @@ mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, const flo
     st = layer_impl(xd, wg, bias, w1, w3, w2, T, d, E, k, ffn, yd, ws, L, opts, s, hk);
     if (st != MK_OK) return st;
     // the staged y is rewritten only after every earlier download from it
-    for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+    // (region 0 is also the blocking entry point's staging region)
+    if (r == 0)
+        for (int c = 0; c < kHostChunks; ++c) MK_TRY(cudaStreamWaitEvent(s, hp->y_done[c], 0));
+    MK_TRY(cudaStreamWaitEvent(s, hp->y_async_done[r], 0));
     MK_TRY(launch_combine(at<bf16>(ws, L.P), at<int32_t>(ws, L.slot_row), T, d, k, yd, s));
     if (opts && opts->phase_events && opts->phase_events[MK_PHASE_COUNT_ALL])
         MK_TRY(cudaEventRecord(static_cast<cudaEvent_t>(opts->phase_events[MK_PHASE_COUNT_ALL]), s));
-    MK_TRY(cudaEventRecord(hp->y_ready[0], s));
-    // one download by the copy engine, off `stream`
+    MK_TRY(cudaEventRecord(hp->y_ready[r], s));
+    // the download, off `stream`: into page-locked memory mapped for the device
+    // by a few CTAs' stores (running beside the next call's kernels), else by the
+    // copy engine
     cudaStream_t q = hp->d2h[0];
-    MK_TRY(cudaStreamWaitEvent(q, hp->y_ready[0], 0));
-    MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, q));
-    MK_TRY(cudaEventRecord(hp->y_done[0], q));
+    MK_TRY(cudaStreamWaitEvent(q, hp->y_ready[r], 0));
+    cudaPointerAttributes ya{};
+    if (cudaPointerGetAttributes(&ya, y_host) == cudaSuccess && ya.type == cudaMemoryTypeHost &&
+        ya.devicePointer != nullptr && aligned16(ya.devicePointer)) {
+        MK_TRY(launch_copy_out(yd, ya.devicePointer, bytes, kCopyOutCtas, q));
+    } else {
+        cudaGetLastError();  // a pointer unknown to CUDA (pageable memory) is not an error here
+        MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, q));
+    }
+    MK_TRY(cudaEventRecord(hp->y_async_done[r], q));
     MK_TRY(cudaEventRecord(done, q));
     return MK_OK;
 }

@@ -49,6 +49,24 @@ __global__ void __launch_bounds__(128) combine_kernel(const bf16* __restrict__ P
     }
 }
 
+// Copy of `n16` 16-byte words into page-locked host memory mapped for the
+// device, by a few CTAs' plain loads and stores (grid-stride): the pipelined
+// host-buffer entry point's download of y, run beside the next call's kernels
+// on a handful of SMs instead of the copy engine.
+__global__ void __launch_bounds__(256) copy_out_kernel(const uint4* __restrict__ src, uint4* dst, int64_t n16) {
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+    int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    for (; i + 3 * stride < n16; i += 4 * stride) {  // four loads in flight per thread
+        const uint4 a = __ldg(src + i), b = __ldg(src + i + stride), c = __ldg(src + i + 2 * stride),
+                    e = __ldg(src + i + 3 * stride);
+        dst[i] = a;
+        dst[i + stride] = b;
+        dst[i + 2 * stride] = c;
+        dst[i + 3 * stride] = e;
+    }
+    for (; i < n16; i += stride) dst[i] = __ldg(src + i);
+}
+
 // The tile-synchronised path's combine, launched while gemm2 may still run:
 // thread 0 waits until the dispatch has written every token's slot rows
 // (tok_done), then threads j < k find the M-tile of row slot_row[t, j] (its
@@ -141,6 +159,13 @@ cudaError_t launch_combine_sem(const bf16* P, const int32_t* slot_row, const int
                            static_cast<const uint32_t*>(sem.tok_done), static_cast<const uint32_t*>(sem.p_ready),
                            pairs ? 1 : 0, n_tiles, swap_max, status, timeout_ns);
     if (err != cudaSuccess) return err;
+    return cudaGetLastError();
+}
+
+cudaError_t launch_copy_out(const void* src, void* dst_mapped, size_t bytes, int blocks, cudaStream_t s) {
+    if (bytes == 0) return cudaSuccess;
+    copy_out_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst_mapped),
+                                           static_cast<int64_t>(bytes / 16));
     return cudaGetLastError();
 }
 

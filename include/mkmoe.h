@@ -287,17 +287,20 @@ MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const fl
 
 /* The layer on HOST buffers for a stream of batches (same operation, inputs
  * and layouts as mk_moe_layer_host), with the output's download left off
- * `stream`: the combine writes y into a staging region of `ws`, the copy
- * engine downloads it into y_host on the workspace's copy stream, and the
- * event `y_ready` (a cudaEvent_t created by the caller, passed as void*) is
- * recorded there once y_host holds the output.  `stream` itself does not wait
+ * `stream`: the combine writes y into a staging region of `ws`, a small
+ * kernel on the workspace's copy stream stores it into y_host (page-locked
+ * and mapped for the device: any cudaHostAlloc / pin_memory buffer; the copy
+ * engine otherwise), and the event `y_ready` (a cudaEvent_t created by the
+ * caller, passed as void*) is recorded there once y_host holds the output.  `stream` itself does not wait
  * for the download, so work enqueued on it after this call -- typically the
  * next batch's call on the same workspace -- runs while y is still crossing
  * the host link.  The caller waits for `y_ready` (cudaEventSynchronize, or
  * cudaStreamWaitEvent) before reading y_host, and does not overwrite y_host
  * before then.  x_host is read as for mk_moe_layer_host (its upload may start
- * before earlier work on `stream`; keep it unchanged until `y_ready`).  The
- * next call's combine on the same workspace waits for this download.  On the
+ * before earlier work on `stream`; keep it unchanged until `y_ready`).
+ * Consecutive calls on a workspace stage y in two alternating regions of it,
+ * so a call's combine waits only for the download two calls back (a slow
+ * download delays a later step less).  On the
  * fused and tile-synchronised paths the call runs as mk_moe_layer_host and
  * records `y_ready` on `stream`.  Errors as mk_moe_layer_host, plus
  * MK_ERR_INVALID_ARG for a NULL y_ready.  The paper has no host-buffer entry
