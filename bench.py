@@ -486,15 +486,21 @@ def run_ours(args):
         tdist.barrier()
     e0 = torch.cuda.Event(enable_timing=True)
     e1 = torch.cuda.Event(enable_timing=True)
+    step_marks = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     e2e_clocks.begin()
     e0.record(stream)
     for i in range(args.steps):
         e2e_step(i)
+        step_marks[i].record(stream)
     stream.wait_event(y_evs[(args.steps - 1) % nbuf])  # the last step's output is in host memory
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_clocks.end()
     e2e_clk = e2e_clocks.stop()
+    # per-step intervals on the caller's stream (each step's kernels, after the previous step's)
+    step_ms = [e0.elapsed_time(step_marks[0])] + [step_marks[i - 1].elapsed_time(step_marks[i])
+                                                    for i in range(1, args.steps)]
+    step_med = statistics.median(step_ms)
     te = max_over_ranks(e0.elapsed_time(e1), dev, dist)
     if dist:
         tdist.barrier()
@@ -565,7 +571,9 @@ def run_ours(args):
                 "note": f"each step's y download overlaps the next step's kernels; every download is inside "
                         f"the timed region; {E2E_BUFFERS} pinned output buffers, each reused after its event",
                 "clocks": e2e_clk,
-                "host_link_gbs": {k: round(v, 1) for k, v in link.items()}},
+                "host_link_gbs": {k: round(v, 1) for k, v in link.items()},
+                "median_step_ms": step_med,
+                "steps_over_1.5x_median": sum(1 for v in step_ms if v > 1.5 * step_med)},
         "gpu_launches": launches_per_step(cfg, args.path) * args.steps,
         "path": PATH_NAMES[args.path],
         "mover_ctas": args.mover_ctas,
