@@ -422,6 +422,20 @@ def dominant_roofline(fb, phase_ms, path, peaks):
     return roof
 
 
+def phase_rooflines(fb, phase_ms, peaks):
+    """Each step of the kernel-per-step path against its own roof: the two
+    GEMMs (tensor), the scatter and the combine (HBM), and the router (its
+    kernels together; HBM by its algorithmic intensity, x read once)."""
+    out = {}
+    for name in ("gemm1", "gemm2", "scatter", "combine"):
+        if name in phase_ms:
+            out[name] = dict(roofline(fb[name], phase_ms[name], peaks), ms=phase_ms[name])
+    if "route_logits" in phase_ms and "topk" in phase_ms:
+        ms = phase_ms["route_logits"] + phase_ms["topk"]
+        out["route"] = dict(roofline(fb["route_logits"], ms, peaks), ms=ms)
+    return out
+
+
 def needs_flush(inp) -> bool:
     """Inputs that fit twice in L2 are flushed out of it between steps."""
     nbytes = sum(t.numel() * t.element_size() for k, t in inp.items() if t is not None and k != "bias")
@@ -453,6 +467,7 @@ def other_configs(mk, names, dev, stream, steps, warmup, peaks):
                  "roofline": dominant_roofline(fb, phase, path, peaks)}
             if path == mk.MK_PATH_STEPS:
                 r["phase_ms"] = phase
+                r["phase_roofline"] = phase_rooflines(fb, phase, peaks)
             res[key] = r
         # the kernel-per-step and tile-synchronised calls replayed from a CUDA graph (no host
         # work per call: what a serving loop that captures the layer gets)
@@ -616,6 +631,7 @@ def run_ours(args):
         "tflops": layer_tflops,
         "tflops_frac_of_measured_bf16": layer_tflops / world / peaks["bf16_tflops"],
         "phase_ms": phase_ms,
+        "phase_roofline": phase_rooflines(fb, phase_ms, peaks) if args.path == mk.MK_PATH_STEPS else None,
         "roofline": roof,
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,

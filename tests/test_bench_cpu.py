@@ -81,3 +81,21 @@ def test_traffic_record_needs_every_source_unchanged(tmp_path):
     legacy = {"source": "gemm_pair.cu", "sha256_16": "0" * 16, "dram_bytes_per_launch": 1}
     path.write_text(json.dumps({"gemm1": {"large": legacy}}))
     assert bench.traffic_record("gemm1", "large", str(path)) is None
+
+
+def test_phase_rooflines_per_step():
+    cfg = CONFIGS["large"]
+    offsets = np.arange(0, 257, dtype=np.int64) * 1024
+    fb = bench.flops_bytes(cfg, offsets)
+    phase = {"route_logits": 0.25, "topk": 0.75, "count": 0.01, "scan": 0.01, "scatter": 0.65,
+             "gemm1": 8.9, "gemm2": 4.5, "combine": 0.68}
+    pr = bench.phase_rooflines(fb, phase, PEAKS)
+    assert set(pr) == {"gemm1", "gemm2", "scatter", "combine", "route"}
+    assert pr["gemm1"]["bound"] == "tensor" and pr["gemm1"]["ms"] == 8.9
+    # the scatter reads x once and writes the k copies: 32768*7168*2*(1+8) bytes in 0.65 ms
+    assert pr["scatter"]["bound"] == "hbm"
+    assert pr["scatter"]["achieved"] == pytest.approx(32768 * 7168 * 2 * 9 / 0.65e-3 / 1e9)
+    # the router's kernels together, against HBM at its intensity (x read once)
+    assert pr["route"]["ms"] == pytest.approx(1.0) and pr["route"]["bound"] == "hbm"
+    assert pr["route"]["achieved"] == pytest.approx(
+        (32768 * 7168 * 2 + 256 * 7168 * 4 + 32768 * 256 * 4) / 1.0e-3 / 1e9)
