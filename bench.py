@@ -636,7 +636,8 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": e2e_value, "unit": "tokens/s", "h2d_bytes_per_step": cfg.T * cfg.d * 2,
                 "d2h_bytes_per_step": cfg.T * cfg.d * 2, "entry_point": "mk_moe_layer_host_async",
-                "note": f"each step's y download overlaps the next step's kernels; every download is inside "
+                "note": f"each step's x upload and y download (small copy kernels) overlap other steps' kernels; "
+                        f"every upload and download is inside "
                         f"the timed region; {E2E_BUFFERS} pinned output buffers, each reused after its event",
                 "clocks": e2e_clk,
                 "host_link_gbs": {k: round(v, 1) for k, v in link.items()},

@@ -603,6 +603,18 @@ mk_status validate_layer(const void* x, const float* wg, const void* w1, const v
 constexpr int kHostChunks = 8;
 constexpr int kHostPipes = 8;
 constexpr int kCopyOutCtas = 16;  // CTAs of the pipelined entry point's download kernel
+constexpr int kCopyInCtas = 32;   // and of its upload kernel (loads from host memory wait a link round trip)
+
+// The device address of page-locked host memory mapped for the device, 16-byte
+// aligned; null for any other pointer (pageable memory is not an error here).
+const void* mapped_host_ptr(const void* p) {
+    cudaPointerAttributes a{};
+    if (cudaPointerGetAttributes(&a, p) == cudaSuccess && a.type == cudaMemoryTypeHost && a.devicePointer != nullptr &&
+        aligned16(a.devicePointer))
+        return a.devicePointer;
+    cudaGetLastError();
+    return nullptr;
+}
 
 struct HostPipe {
     int dev = -1;
@@ -836,9 +848,14 @@ mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, const flo
     // combine waits only for the download two calls back
     const int r = static_cast<int>(hp->async_calls++ & 1u);
     bf16* yd = at<bf16>(ws, r ? L.y_stage2 : L.y_stage);
-    // upload of x as in mk_moe_layer_host: after the previous call's scatter
+    // upload of x, after the previous call's scatter (as in mk_moe_layer_host):
+    // from page-locked memory mapped for the device by a few CTAs' loads
+    // (running beside the previous call's GEMMs), else by the copy engine
     MK_TRY(cudaStreamWaitEvent(hp->h2d, hp->x_free, 0));
-    MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
+    if (const void* xm = mapped_host_ptr(x_host))
+        MK_TRY(launch_bulk_copy(xm, xd, bytes, kCopyInCtas, hp->h2d));
+    else
+        MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
     MK_TRY(cudaEventRecord(hp->x_ready, hp->h2d));
     MK_TRY(cudaStreamWaitEvent(s, hp->x_ready, 0));
     LayerHooks hk;
@@ -860,14 +877,10 @@ mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, const flo
     // copy engine
     cudaStream_t q = hp->d2h[0];
     MK_TRY(cudaStreamWaitEvent(q, hp->y_ready[r], 0));
-    cudaPointerAttributes ya{};
-    if (cudaPointerGetAttributes(&ya, y_host) == cudaSuccess && ya.type == cudaMemoryTypeHost &&
-        ya.devicePointer != nullptr && aligned16(ya.devicePointer)) {
-        MK_TRY(launch_copy_out(yd, ya.devicePointer, bytes, kCopyOutCtas, q));
-    } else {
-        cudaGetLastError();  // a pointer unknown to CUDA (pageable memory) is not an error here
+    if (void* ym = const_cast<void*>(mapped_host_ptr(y_host)))
+        MK_TRY(launch_bulk_copy(yd, ym, bytes, kCopyOutCtas, q));
+    else
         MK_TRY(cudaMemcpyAsync(y_host, yd, bytes, cudaMemcpyDeviceToHost, q));
-    }
     MK_TRY(cudaEventRecord(hp->y_async_done[r], q));
     MK_TRY(cudaEventRecord(done, q));
     return MK_OK;

@@ -49,11 +49,12 @@ __global__ void __launch_bounds__(128) combine_kernel(const bf16* __restrict__ P
     }
 }
 
-// Copy of `n16` 16-byte words into page-locked host memory mapped for the
-// device, by a few CTAs' plain loads and stores (grid-stride): the pipelined
-// host-buffer entry point's download of y, run beside the next call's kernels
-// on a handful of SMs instead of the copy engine.
-__global__ void __launch_bounds__(256) copy_out_kernel(const uint4* __restrict__ src, uint4* dst, int64_t n16) {
+// Copy of `n16` 16-byte words between device memory and page-locked host
+// memory mapped for the device, by a few CTAs' plain loads and stores
+// (grid-stride): the pipelined host-buffer entry point's upload of x and
+// download of y, each run beside another call's kernels on a handful of SMs
+// instead of the copy engine.
+__global__ void __launch_bounds__(256) bulk_copy_kernel(const uint4* __restrict__ src, uint4* dst, int64_t n16) {
     const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
     int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     for (; i + 3 * stride < n16; i += 4 * stride) {  // four loads in flight per thread
@@ -162,9 +163,9 @@ cudaError_t launch_combine_sem(const bf16* P, const int32_t* slot_row, const int
     return cudaGetLastError();
 }
 
-cudaError_t launch_copy_out(const void* src, void* dst_mapped, size_t bytes, int blocks, cudaStream_t s) {
+cudaError_t launch_bulk_copy(const void* src, void* dst, size_t bytes, int blocks, cudaStream_t s) {
     if (bytes == 0) return cudaSuccess;
-    copy_out_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst_mapped),
+    bulk_copy_kernel<<<blocks, 256, 0, s>>>(static_cast<const uint4*>(src), static_cast<uint4*>(dst),
                                            static_cast<int64_t>(bytes / 16));
     return cudaGetLastError();
 }

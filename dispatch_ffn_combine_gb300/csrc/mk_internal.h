@@ -157,9 +157,10 @@ cudaError_t launch_scatter(const bf16* x, const int32_t* ids, const float* w, in
 cudaError_t launch_mtile_table(const int32_t* offsets, int E, int64_t S, int32_t* mtile_start, uint32_t* status,
                                cudaStream_t s);
 // y[t] = sum_j P[slot_row[t, j]] for t < T; p_rows = rows of P (-1: T * k).
-// Copy `bytes` (a multiple of 16; both pointers 16-byte aligned) into mapped
-// page-locked host memory with `blocks` CTAs of plain stores.
-cudaError_t launch_copy_out(const void* src, void* dst_mapped, size_t bytes, int blocks, cudaStream_t s);
+// Copy `bytes` (a multiple of 16; both pointers 16-byte aligned) between
+// device memory and mapped page-locked host memory with `blocks` CTAs of plain
+// loads and stores.
+cudaError_t launch_bulk_copy(const void* src, void* dst, size_t bytes, int blocks, cudaStream_t s);
 cudaError_t launch_combine(const bf16* P, const int32_t* slot_row, int64_t T, int d, int k, bf16* y,
                            cudaStream_t s, int64_t p_rows = -1);
 

@@ -291,7 +291,9 @@ MK_API mk_status mk_moe_layer_host(const void* x_host, const float* wg, const fl
  * kernel on the workspace's copy stream stores it into y_host (page-locked
  * and mapped for the device: any cudaHostAlloc / pin_memory buffer; the copy
  * engine otherwise), and the event `y_ready` (a cudaEvent_t created by the
- * caller, passed as void*) is recorded there once y_host holds the output.  `stream` itself does not wait
+ * caller, passed as void*) is recorded there once y_host holds the output.
+ * x's upload is likewise a small kernel's loads when x_host is page-locked
+ * and mapped (the copy engine otherwise).  `stream` itself does not wait
  * for the download, so work enqueued on it after this call -- typically the
  * next batch's call on the same workspace -- runs while y is still crossing
  * the host link.  The caller waits for `y_ready` (cudaEventSynchronize, or
