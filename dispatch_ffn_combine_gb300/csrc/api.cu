@@ -603,7 +603,7 @@ mk_status validate_layer(const void* x, const float* wg, const void* w1, const v
 constexpr int kHostChunks = 8;
 constexpr int kHostPipes = 8;
 constexpr int kCopyOutCtas = 16;  // CTAs of the pipelined entry point's download kernel
-constexpr int kCopyInCtas = 32;   // and of its upload kernel (loads from host memory wait a link round trip)
+constexpr int kCopyInCtas = 32;   // CTAs of the host entry points' upload kernel (its loads wait a link round trip)
 
 // The device address of page-locked host memory mapped for the device, 16-byte
 // aligned; null for any other pointer (pageable memory is not an error here).
@@ -762,7 +762,9 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     }
     // Kernel-per-step path, pipelined copies on the workspace's copy streams:
     //  - the upload of x waits only for the previous call on this workspace to
-    //    have read the staged x (its scatter), so it overlaps that call's GEMMs;
+    //    have read the staged x (its scatter), so it overlaps that call's GEMMs
+    //    (from mapped page-locked x_host by a few CTAs' loads, else by the copy
+    //    engine);
     //  - the combine runs in chunks of tokens (about 16 MB of output each, at
     //    most kHostChunks) and each chunk is downloaded as soon as it is
     //    combined, alternating between two copy streams (the staged y is
@@ -770,7 +772,10 @@ mk_status mk_moe_layer_host(const void* x_host, const float* wg, const float* bi
     //  - `stream` waits for the last download, so the output is in y_host once
     //    the stream reaches this point, as for the plain sequence.
     MK_TRY(cudaStreamWaitEvent(hp->h2d, hp->x_free, 0));
-    MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
+    if (const void* xm = mapped_host_ptr(x_host))
+        MK_TRY(launch_bulk_copy(xm, xd, bytes, kCopyInCtas, hp->h2d));
+    else
+        MK_TRY(cudaMemcpyAsync(xd, x_host, bytes, cudaMemcpyHostToDevice, hp->h2d));
     MK_TRY(cudaEventRecord(hp->x_ready, hp->h2d));
     MK_TRY(cudaStreamWaitEvent(s, hp->x_ready, 0));
     LayerHooks hk;

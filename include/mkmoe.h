@@ -273,7 +273,8 @@ MK_API mk_status mk_moe_dispatch_gemm(const void* x, const float* wg, const floa
  * On the kernel-per-step path the copies run on two copy streams the library
  * keeps per (device, workspace): the upload of x waits only until the
  * previous call on `ws` has read its staged x, so it overlaps that call's
- * GEMMs.  If y_host is page-locked memory mapped for the device, the combine
+ * GEMMs (a small kernel's loads when x_host is page-locked memory mapped for
+ * the device).  If y_host is page-locked memory mapped for the device, the combine
  * writes y straight into it; otherwise y is combined and downloaded in token
  * chunks (~16 MB each, up to 8) while later chunks are still being combined.
  * The library

@@ -94,14 +94,15 @@ def test_layer_host_buffers_match_device_call():
 def test_layer_host_calls_back_to_back(T):
     """Host-buffer calls issued back to back on one workspace (their copies
     overlap the previous call's kernels), alternating paths, inputs and
-    pinned / pageable outputs: every y_host equals the device-buffer result
-    for its own input."""
+    pinned / pageable inputs and outputs: every y_host equals the
+    device-buffer result for its own input."""
     wl = Workload("ragged", T=T)
     c = wl.cfg
     ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
     g = torch.Generator().manual_seed(7)
     xs = [wl.g["x"].cpu()] + [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(3)]
-    xs_host = [x.pin_memory() for x in xs]
+    # pinned inputs take the upload kernel, the pageable one (call 1) the copy engine
+    xs_host = [x.clone() if i == 1 else x.pin_memory() for i, x in enumerate(xs)]
     # pinned outputs take the direct write, pageable ones the chunked downloads
     ys_host = [torch.empty((wl.T, c.d), dtype=torch.bfloat16) for _ in xs]
     ys_host = [y.pin_memory() if i % 2 == 0 else y for i, y in enumerate(ys_host)]
@@ -121,15 +122,16 @@ def test_layer_host_calls_back_to_back(T):
 def test_layer_host_async_back_to_back(T):
     """The pipelined host entry point issued back to back on one workspace,
     interleaved with the blocking one and the fused path, each output its
-    own y_host and event: once its event has completed, every y_host equals
-    the device-buffer result for its own input; the stream never waited for
-    the downloads of the async calls."""
+    own y_host and event, one input pageable: once its event has completed,
+    every y_host equals the device-buffer result for its own input; the
+    stream never waited for the downloads of the async calls."""
     wl = Workload("ragged", T=T)
     c = wl.cfg
     ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
     g = torch.Generator().manual_seed(11)
     xs = [wl.g["x"].cpu()] + [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(4)]
-    xs_host = [x.pin_memory() for x in xs]
+    # pinned inputs take the upload kernel, the pageable one (call 1) the copy engine
+    xs_host = [x.clone() if i == 1 else x.pin_memory() for i, x in enumerate(xs)]
     # pinned outputs, and one pageable one (its download still completes before the event)
     ys_host = [torch.full((wl.T, c.d), -1.0, dtype=torch.bfloat16) for _ in xs]
     ys_host = [y if i == 4 else y.pin_memory() for i, y in enumerate(ys_host)]
