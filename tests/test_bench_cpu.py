@@ -99,3 +99,16 @@ def test_phase_rooflines_per_step():
     assert pr["route"]["ms"] == pytest.approx(1.0) and pr["route"]["bound"] == "hbm"
     assert pr["route"]["achieved"] == pytest.approx(
         (32768 * 7168 * 2 + 256 * 7168 * 4 + 32768 * 256 * 4) / 1.0e-3 / 1e9)
+
+
+def test_launches_per_step_by_path_and_router():
+    import dispatch_ffn_combine_gb300 as mk
+    # large: the candidate-filter router (prep, approximate logits, select), then
+    # count, scan, scatter, gemm1, gemm2, combine
+    assert bench.launches_per_step(CONFIGS["large"], mk.MK_PATH_STEPS) == 9
+    assert bench.launches_per_step(CONFIGS["large"], mk.MK_PATH_TILES) == 9
+    # the fused path: the filter's three kernels, count and scan, then the persistent kernel
+    assert bench.launches_per_step(CONFIGS["large"], mk.MK_PATH_FUSED) == 6
+    # tiny: the plain router (logits, top-k) and the same six; fused: one kernel
+    assert bench.launches_per_step(CONFIGS["tiny"], mk.MK_PATH_STEPS) == 8
+    assert bench.launches_per_step(CONFIGS["tiny"], mk.MK_PATH_FUSED) == 1
