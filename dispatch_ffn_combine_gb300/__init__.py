@@ -367,19 +367,20 @@ def mk_moe_layer(x, wg, bias, w1, w3, w2, k, y=None, ws=None, phase_events=None,
 
 
 def mk_moe_layer_host(x_host, wg, bias, w1, w3, w2, k, y_host, ws, phase_events=None, timeout_ns=0, stream=None,
-                      path=MK_PATH_STEPS, mover_ctas=0):
+                      path=MK_PATH_STEPS, mover_ctas=0, gather_rows=False):
     """The layer on host buffers (pinned for asynchronous copies): x_host in, y_host out."""
     T, d, E, f = _layer_shapes(x_host, wg, bias, w1, w3, w2, device=False)
     _need(y_host, torch.bfloat16, (T, d), "y_host", device=False)
     st = load_library().mk_moe_layer_host(_p(x_host), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k, f,
                                           _p(y_host), _p(ws), ws.numel(),
-                                          _opts(phase_events, timeout_ns, 0, path, mover_ctas), _stream(stream))
+                                          _opts(phase_events, timeout_ns, 0, path, mover_ctas,
+                                                gather_rows=gather_rows), _stream(stream))
     _check(st, "mk_moe_layer_host")
     return y_host
 
 
 def mk_moe_layer_host_async(x_host, wg, bias, w1, w3, w2, k, y_host, ws, y_ready, phase_events=None, timeout_ns=0,
-                            stream=None, path=MK_PATH_STEPS, mover_ctas=0):
+                            stream=None, path=MK_PATH_STEPS, mover_ctas=0, gather_rows=False):
     """The layer on host buffers with y's download off `stream`: y_ready (a
     torch.cuda.Event) is recorded once y_host holds the output; wait for it
     before reading y_host."""
@@ -390,7 +391,7 @@ def mk_moe_layer_host_async(x_host, wg, bias, w1, w3, w2, k, y_host, ws, y_ready
         y_ready.record(s)
     st = load_library().mk_moe_layer_host_async(_p(x_host), _p(wg), _p(bias), _p(w1), _p(w3), _p(w2), T, d, E, k,
                                                 f, _p(y_host), _p(ws), ws.numel(),
-                                                _opts(phase_events, timeout_ns, 0, path, mover_ctas),
+                                                _opts(phase_events, timeout_ns, 0, path, mover_ctas, gather_rows=gather_rows),
                                                 ctypes.c_void_p(s.cuda_stream), ctypes.c_void_p(y_ready.cuda_event))
     _check(st, "mk_moe_layer_host_async")
     return y_host

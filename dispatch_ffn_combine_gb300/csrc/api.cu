@@ -339,7 +339,7 @@ namespace {
 
 // Hooks for the host-buffer entry point's pipelined copies (kernel-per-step path).
 struct LayerHooks {
-    cudaEvent_t after_scatter = nullptr;  // recorded once x has been read for the last time
+    cudaEvent_t after_scatter = nullptr;  // recorded once x has been read for the last time (scatter or gemm1)
     bool skip_combine = false;            // the caller runs the combine itself (in chunks)
 };
 
@@ -535,7 +535,9 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
     const DispatchOut dout{offsets, at<int32_t>(ws, L.row_token), row_weight, slot_row, x_perm};
     mk_status st = route_dispatch_steps(static_cast<const bf16*>(x), wg, bias, T, d, E, k, ws, L, dout, opts, pm, s);
     if (st != MK_OK) return st;
-    if (hk.after_scatter != nullptr) MK_TRY(cudaEventRecord(hk.after_scatter, s));
+    // x is read for the last time by the scatter, or by gemm1 when it gathers its rows from x
+    const bool gather = opts != nullptr && opts->gather_rows != 0;
+    if (hk.after_scatter != nullptr && !gather) MK_TRY(cudaEventRecord(hk.after_scatter, s));
     FfnArgs a;
     a.x_perm = x_perm;
     a.offsets = offsets;
@@ -554,7 +556,6 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
     a.timeout_ns = (opts && opts->timeout_ns) ? opts->timeout_ns : kDefaultTimeoutNs;
     a.inject = opts ? opts->inject : 0;  // only MK_INJECT_STALL_GEMM1 acts in the GEMMs
     a.tickets = status + 4;
-    const bool gather = opts != nullptr && opts->gather_rows != 0;
     if (gather) {  // gemm1 gathers its rows from x by their source tokens (single-CTA tiles)
         a.gather_x = static_cast<const bf16*>(x);
         a.gather_T = T;
@@ -562,6 +563,7 @@ mk_status layer_impl(const void* x, const float* wg, const float* bias, const vo
     }
     MK_TRY(pm.mark(MK_PHASE_GEMM1));
     MK_TRY(gather ? launch_gemm1(a, s) : launch_gemm1_auto(a, s));
+    if (hk.after_scatter != nullptr && gather) MK_TRY(cudaEventRecord(hk.after_scatter, s));
     MK_TRY(pm.mark(MK_PHASE_GEMM2));
     MK_TRY(gather ? launch_gemm2(a, s) : launch_gemm2_auto(a, s));
     MK_TRY(pm.mark(MK_PHASE_COMBINE));

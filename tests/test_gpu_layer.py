@@ -118,6 +118,38 @@ def test_layer_host_calls_back_to_back(T):
         assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
 
 
+def test_layer_host_calls_gathering_rows_back_to_back():
+    """With gemm1 gathering its rows from the staged x (gather_rows), back-to-back
+    host-buffer calls (blocking and pipelined, pinned inputs uploaded beside the
+    previous call's kernels) keep each call's x until its gemm1 has read it:
+    every y_host equals the device-buffer result for its own input."""
+    wl = Workload("ragged", T=1000)
+    c = wl.cfg
+    ws = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    g = torch.Generator().manual_seed(13)
+    xs = [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(4)]
+    xs_host = [x.pin_memory() for x in xs]
+    ys_host = [torch.full((wl.T, c.d), -1.0, dtype=torch.bfloat16).pin_memory() for _ in xs]
+    args = (wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
+    events = []
+    for i, (xh, yh) in enumerate(zip(xs_host, ys_host)):
+        if i % 2 == 0:
+            ev = torch.cuda.Event()
+            mk.mk_moe_layer_host_async(xh, *args, yh, ws, ev, gather_rows=True)
+            events.append(ev)
+        else:
+            mk.mk_moe_layer_host(xh, *args, yh, ws, gather_rows=True)
+    for ev in events:
+        ev.synchronize()
+    torch.cuda.synchronize()
+    assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    ws2 = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    for x, yh in zip(xs, ys_host):
+        y_dev = mk.mk_moe_layer(x.to(wl.dev), *args, ws=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+
 @pytest.mark.parametrize("T", [7, 1000])
 def test_layer_host_async_back_to_back(T):
     """The pipelined host entry point issued back to back on one workspace,
