@@ -636,6 +636,18 @@ HostPipe g_pipes[kHostPipes];
 uint64_t g_pipe_clock = 0;
 
 void release_pipe(HostPipe& p) {
+    // The workspace's last call may still run on the caller's stream: wait for
+    // every event it recorded there (a no-op once complete or never recorded),
+    // so that a later call on this workspace, which gets a new pipe whose events
+    // order nothing yet, cannot overwrite its staged x or y under it.
+    for (cudaEvent_t e : {p.x_free, p.x_ready})
+        if (e) cudaEventSynchronize(e);
+    for (int c = 0; c < kHostChunks; ++c) {
+        if (p.y_ready[c]) cudaEventSynchronize(p.y_ready[c]);
+        if (p.y_done[c]) cudaEventSynchronize(p.y_done[c]);
+    }
+    for (cudaEvent_t e : p.y_async_done)
+        if (e) cudaEventSynchronize(e);
     if (p.h2d) cudaStreamSynchronize(p.h2d);
     for (cudaStream_t q : p.d2h)
         if (q) cudaStreamSynchronize(q);

@@ -150,6 +150,37 @@ def test_layer_host_calls_gathering_rows_back_to_back():
         assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
 
 
+def test_layer_host_async_more_workspaces_than_pipes():
+    """Pipelined host-buffer calls rotating over more workspaces than the
+    library keeps copy pipes for (each workspace's pipe is evicted and made
+    again while its last call may still run), without synchronising between
+    calls: every y_host equals the device-buffer result for its own input."""
+    wl = Workload("ragged", T=256)
+    c = wl.cfg
+    n_ws = 10  # more than the library's pipe cache
+    wss = [mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev) for _ in range(n_ws)]
+    g = torch.Generator().manual_seed(17)
+    xs = [torch.randn((wl.T, c.d), generator=g).to(torch.bfloat16) for _ in range(2 * n_ws)]
+    xs_host = [x.pin_memory() for x in xs]
+    ys_host = [torch.full((wl.T, c.d), -1.0, dtype=torch.bfloat16).pin_memory() for _ in xs]
+    args = (wl.g["wg"], None, wl.g["w1"], wl.g["w3"], wl.g["w2"], c.k)
+    events = []
+    for i, (xh, yh) in enumerate(zip(xs_host, ys_host)):
+        ev = torch.cuda.Event()
+        mk.mk_moe_layer_host_async(xh, *args, yh, wss[i % n_ws], ev)
+        events.append(ev)
+    for ev in events:
+        ev.synchronize()
+    torch.cuda.synchronize()
+    for ws in wss:
+        assert mk.mk_moe_last_device_error(ws)[0] == mk.MK_OK
+    ws2 = mk.alloc_workspace(wl.T, c.d, c.E, c.k, c.f, wl.dev)
+    for x, yh in zip(xs, ys_host):
+        y_dev = mk.mk_moe_layer(x.to(wl.dev), *args, ws=ws2)
+        torch.cuda.synchronize()
+        assert torch.equal(yh.view(torch.int16), y_dev.cpu().view(torch.int16))
+
+
 @pytest.mark.parametrize("T", [7, 1000])
 def test_layer_host_async_back_to_back(T):
     """The pipelined host entry point issued back to back on one workspace,
