@@ -316,7 +316,9 @@ MK_API mk_status mk_moe_layer_host_async(const void* x_host, const float* wg, co
 
 /* Synchronises `stream`, then returns and clears the device-side status of
  * `ws` (MK_OK if no device error).  *detail (may be NULL) receives the site
- * code of the error. */
+ * code of the error.  Every call that runs kernels on `ws` starts from a
+ * cleared status, so a call's device error is seen only until the next call
+ * on `ws` is issued: read it in between. */
 MK_API mk_status mk_moe_last_device_error(void* ws, void* stream, uint32_t* detail);
 
 /* Router diagnostics: *count receives the number of tokens of the last router
